@@ -1,0 +1,213 @@
+"""Program-id -> output-tile maps and the cluster-persistent schedule (oracle).
+
+Sources:
+  [TBS] Lei Mao, "CUDA Thread Block Swizzle": sections "Linear Swizzle",
+        "Grouped 2D Panel Swizzle", "Morton / Z-order Swizzle", "Bitwise XOR
+        Swizzle" (8x8 tables) and the benchmark script's CPU mapping functions
+        and persistent tile loop.
+  [CPS] TVM TIRx docs, "ClusterPersistentScheduler2D": "Tile Ordering"
+        (group-major), "Serpentine Mode", "Example 1: Basic persistent kernel",
+        "Example 2: 2SM GEMM".
+
+All functions return (m, n): m indexes output-tile rows (the M dimension),
+n output-tile columns (N).  The pages' tables print the program id at
+(row = m, column = n).
+"""
+from __future__ import annotations
+
+ROW, COL, PANEL, MORTON, XOR, SERPENTINE = 0, 1, 2, 3, 4, 5
+ORDER_NAMES = {ROW: "row", COL: "col", PANEL: "panel", MORTON: "morton",
+               XOR: "xor", SERPENTINE: "serpentine"}
+
+
+def row_major(pid, gm, gn):
+    """[TBS] Linear Swizzle: consecutive ids walk along N, then the next row."""
+    return pid // gn, pid % gn
+
+
+def col_major(pid, gm, gn):
+    """[TBS] linear column-major mapper: consecutive ids walk along M first."""
+    return pid % gm, pid // gm
+
+
+def panel(pid, gm, gn, group):
+    """[TBS] Grouped 2D Panel Swizzle with group size G along M.
+
+    Ids are dealt out group by group; a group is a band of G tile rows spanning
+    all gn columns.  Inside a band the ids run down a column of the band first
+    (column-major inside the band).  The last band holds only the rows that are
+    left (gm - first_row of that band), and that smaller height is the period
+    used inside it.  [CPS] "Tile Ordering" (group-major with l2_group_size) is
+    the same map.
+    """
+    ids_per_band = group * gn
+    band = pid // ids_per_band
+    first_row = band * group
+    band_rows = min(gm - first_row, group)
+    within = pid - band * ids_per_band
+    return first_row + within % band_rows, within // band_rows
+
+
+def morton(pid, gm, gn):
+    """[TBS] Morton / Z-order: bit 2i of the id is bit i of m, bit 2i+1 is bit
+    i of n (16 bit pairs), each then reduced modulo its grid extent."""
+    m = 0
+    n = 0
+    for i in range(16):
+        m |= ((pid >> (2 * i)) & 1) << i
+        n |= ((pid >> (2 * i + 1)) & 1) << i
+    return m % gm, n % gn
+
+
+def xor_swizzle(pid, gm, gn):
+    """[TBS] Bitwise XOR: with x = id mod gn and y = id div gn, the tile row is
+    (x XOR y) mod gm and the tile column is y mod gn."""
+    x = pid % gn
+    y = pid // gn
+    return (x ^ y) % gm, y % gn
+
+
+def serpentine(pid, gm, gn, size):
+    """[CPS] Serpentine Mode, read from its 4x4 table (swizzle_size = S).
+
+    The N axis is cut into strips S tiles wide.  Strip s is walked one tile row
+    at a time, left to right inside the row; even strips go down the rows
+    (m = 0 .. gm-1), odd strips go up (m = gm-1 .. 0).  A last strip narrower
+    than S (when S does not divide gn) uses its own width as the row length.
+    """
+    strip = pid // (size * gm)
+    r = pid - strip * size * gm
+    width = min(size, gn - strip * size)
+    step = r // width
+    m = step if strip % 2 == 0 else gm - 1 - step
+    n = strip * size + r % width
+    return m, n
+
+
+def tile_of(order, pid, gm, gn, group=1):
+    """Dispatch on the order id ([TBS] mode ids 0..4; 5 = serpentine)."""
+    if order == ROW:
+        return row_major(pid, gm, gn)
+    if order == COL:
+        return col_major(pid, gm, gn)
+    if order == PANEL:
+        return panel(pid, gm, gn, group)
+    if order == MORTON:
+        return morton(pid, gm, gn)
+    if order == XOR:
+        return xor_swizzle(pid, gm, gn)
+    if order == SERPENTINE:
+        return serpentine(pid, gm, gn, group)
+    raise ValueError(f"unknown order {order}")
+
+
+def tile_sequence(order, gm, gn, group=1):
+    """[(m, n) for pid in 0 .. gm*gn-1]."""
+    return [tile_of(order, p, gm, gn, group) for p in range(gm * gn)]
+
+
+def is_bijective(order, gm, gn, group=1):
+    """True when the map visits every one of the gm*gn tiles exactly once."""
+    seen = set(tile_sequence(order, gm, gn, group))
+    if len(seen) != gm * gn:
+        return False
+    return all(0 <= m < gm and 0 <= n < gn for m, n in seen)
+
+
+def id_table(order, gm, gn, group=1):
+    """gm x gn table whose entry (m, n) is the id mapped to tile (m, n), as
+    the pages print it.  Entries never reached stay None."""
+    t = [[None] * gn for _ in range(gm)]
+    for p, (m, n) in enumerate(tile_sequence(order, gm, gn, group)):
+        t[m][n] = p
+    return t
+
+
+class ClusterSchedule:
+    """[CPS] cluster-persistent work distribution, restated.
+
+    A cluster starts at work index ``cluster_id`` and advances by
+    ``num_clusters``; it is valid while the work index is below the number of
+    tiles; the current (m, n) is the tile order applied to the work index;
+    ``tile_count`` counts the tiles handed out so far.
+    """
+
+    def __init__(self, gm, gn, num_clusters, order=PANEL, group=8):
+        self.gm, self.gn = gm, gn
+        self.num_clusters = num_clusters
+        self.order, self.group = order, group
+        self.work_idx = 0
+        self.tile_count = 0
+        self.m_idx = self.n_idx = 0
+
+    def _update(self):
+        if self.valid():
+            self.m_idx, self.n_idx = tile_of(self.order, self.work_idx,
+                                             self.gm, self.gn, self.group)
+
+    def init(self, cluster_id):
+        self.work_idx = cluster_id
+        self.tile_count = 0
+        self._update()
+
+    def valid(self):
+        return self.work_idx < self.gm * self.gn
+
+    def next_tile_stride(self, stride):
+        self.work_idx += stride
+        self.tile_count += 1
+        self._update()
+
+    def next_tile(self):
+        self.next_tile_stride(self.num_clusters)
+
+
+def cluster_sequences(gm, gn, num_clusters, order=PANEL, group=8):
+    """For every cluster, its list of (work_idx, m, n) in execution order."""
+    out = []
+    for c in range(num_clusters):
+        s = ClusterSchedule(gm, gn, num_clusters, order, group)
+        s.init(c)
+        seq = []
+        while s.valid():
+            seq.append((s.work_idx, s.m_idx, s.n_idx))
+            s.next_tile()
+        out.append(seq)
+    return out
+
+
+def cta_tile(m_idx, n_idx, cta_idx, cluster_m, cluster_n):
+    """[CPS] Example 2: a cluster-level tile becomes per-CTA tiles outside the
+    scheduler.  rank = cta_idx mod cluster size; the rank's position inside the
+    cluster is (rank mod cluster_m, rank div cluster_m)."""
+    rank = cta_idx % (cluster_m * cluster_n)
+    cb_m = rank % cluster_m
+    cb_n = rank // cluster_m
+    return m_idx * cluster_m + cb_m, n_idx * cluster_n + cb_n
+
+
+def persistent_trace(order, gm, gn, group, num_programs, cluster_m=1):
+    """What a persistent launch of ``num_programs`` CTAs does, CTA by CTA.
+
+    Programs are grouped into clusters of ``cluster_m`` CTAs along M; the
+    scheduler works on the cluster-tile grid (gm / cluster_m) x gn and every
+    CTA of a cluster takes its own row of the cluster tile ([CPS] Example 2).
+    With cluster_m = 1 and num_programs = tiles this is the non-persistent
+    launch of [TBS] (one program per tile, one loop iteration each).
+
+    Returns {(cta_m, cta_n): (program, iteration)} over all CTA tiles.
+    """
+    if gm % cluster_m:
+        raise ValueError("cluster_m must divide gm")
+    num_clusters = num_programs // cluster_m
+    seqs = cluster_sequences(gm // cluster_m, gn, num_clusters, order, group)
+    trace = {}
+    for c, seq in enumerate(seqs):
+        for it, (_, m_idx, n_idx) in enumerate(seq):
+            for r in range(cluster_m):
+                prog = c * cluster_m + r
+                key = cta_tile(m_idx, n_idx, prog, cluster_m, 1)
+                if key in trace:
+                    raise AssertionError(f"tile {key} visited twice")
+                trace[key] = (prog, it)
+    return trace

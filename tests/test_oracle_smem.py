@@ -1,0 +1,112 @@
+"""Pins of the shared-memory oracle: the second page's Triton tables and
+transpose conflict arithmetic, swizzle invariants and closed forms (CPU)."""
+import pytest
+
+from conftest import read_lines
+from oracle import smem_bank as sb
+
+
+def _triton_tables():
+    out, cur = [], None
+    for ln in read_lines("sbc_triton_tables.txt"):
+        if ln[0] == "table":
+            cur = {"params": tuple(int(v) for v in ln[1:]), "rows": []}
+            out.append(cur)
+        else:
+            cur["rows"].append([int(v) for v in ln])
+    return out
+
+
+def test_triton_tables():
+    tabs = _triton_tables()
+    assert len(tabs) == 5
+    for t in tabs:
+        vec, per_phase, max_phase, rows, cols = t["params"]
+        assert sb.triton_table(rows, cols, vec, per_phase, max_phase) == t["rows"], t["params"]
+
+
+def _fixture():
+    return {ln[0]: int(ln[1]) for ln in read_lines("sbc_transpose_conflicts.txt")
+            if ln[0] != "M"}
+
+
+def test_transpose_conflict_counts():
+    g = _fixture()
+    st, ld = sb.transpose_conflict_totals("naive", 1024, 2048)
+    assert st == g["naive_store_conflicts"]
+    assert ld == 0
+    # wavefronts: one per conflict plus one per warp store
+    warp_stores = (1024 * 2048) // 32
+    assert st + warp_stores == g["naive_store_wavefronts"]
+    assert sb.transpose_conflict_totals("padded", 1024, 2048) == (g["padded_store_conflicts"], 0)
+    assert sb.transpose_conflict_totals("xor", 1024, 2048) == (g["xor_store_conflicts"], 0)
+
+
+def test_transpose_conflicts_large_closed_form():
+    # every warp store of the naive layout hits one bank 32 times: 31 extra
+    st, _ = sb.transpose_conflict_totals("naive", 16384, 32768)
+    assert st == (16384 * 32768 // 32) * 31 == 520093696
+
+
+def test_wavefront_rules():
+    # 32 lanes reading 32 consecutive words: 1 wavefront
+    assert sb.wavefronts([4 * t for t in range(32)], 4) == 1
+    # all lanes reading the same word: broadcast, 1 wavefront
+    assert sb.wavefronts([0] * 32, 4) == 1
+    # stride 2 words: 2-way conflict
+    assert sb.wavefronts([8 * t for t in range(32)], 4) == 2
+    # 16-byte accesses: 4 phases of 8 lanes, contiguous -> 4 wavefronts, 0 conflicts
+    assert sb.wavefronts([16 * t for t in range(32)], 16) == 4
+    assert sb.conflicts([16 * t for t in range(32)], 16) == 0
+    # 8-byte accesses: 2 phases
+    assert sb.wavefronts([8 * t for t in range(32)], 8) == 2
+
+
+@pytest.mark.parametrize("fn", ["xor", "tma"])
+def test_swizzle_properties(fn):
+    """The page's three properties of a swizzle map: one-to-one, ranges kept,
+    and two rows never put the same logical column in the same physical one."""
+    rows, cols = (32, 32) if fn == "xor" else (8, 64)
+
+    def phys(r, c):
+        if fn == "xor":
+            return r, sb.xor_offset(r, c, cols) - r * cols
+        return sb.tma_swizzle_128b(r, c, cols, 2)
+
+    images = {phys(r, c) for r in range(rows) for c in range(cols)}
+    assert len(images) == rows * cols
+    assert all(0 <= y < rows and 0 <= x < cols for y, x in images)
+    for c in range(cols):
+        xs = [phys(r, c)[1] for r in range(rows)]
+        if fn == "xor":
+            assert len(set(xs)) == rows
+        else:  # chunk granularity: 8 rows of one atom land in 8 distinct chunks
+            assert len({x // 8 for x in xs}) == rows
+
+
+def test_tma_swizzle_equals_cute_swizzle():
+    # Swizzle<3,3,3> on fp16 element offsets and Swizzle<3,4,3> on byte
+    # offsets describe the same 128-byte swizzle as the TMA chunk formula.
+    for y in range(16):
+        for x in range(64):
+            yy, xs = sb.tma_swizzle_128b(y, x, 64, 2)
+            assert yy * 64 + xs == sb.cute_swizzle(y * 64 + x, 3, 3, 3)
+            assert 2 * (yy * 64 + xs) == sb.cute_swizzle(2 * (y * 64 + x), 3, 4, 3)
+    # 4-byte elements: 32 per 128-byte row, chunk = 4 elements
+    for y in range(8):
+        for x in range(32):
+            yy, xs = sb.tma_swizzle_128b(y, x, 32, 4)
+            assert 4 * (yy * 32 + xs) == sb.cute_swizzle(4 * (y * 32 + x), 3, 4, 3)
+
+
+def test_staged_epilogue_store_conflicts():
+    # 128-byte rows, lane t writes 16 bytes of row t: without the swizzle the
+    # 8 lanes of a phase hit the same 4 banks (8 wavefronts per phase, 28
+    # extra over the 4 phases); with it every phase is conflict free.
+    assert sb.staged_row_store_conflicts(128, swizzled=False) == [28] * 8
+    assert sb.staged_row_store_conflicts(128, swizzled=True) == [0] * 8
+
+
+def test_padding_breaks_16b_alignment():
+    # the page's caveat: in int[32][33], row 1 starts at byte 132, not 16-aligned
+    assert (sb.padded_offset(1, 0, 32) * 4) % 16 != 0

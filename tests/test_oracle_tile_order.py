@@ -1,0 +1,158 @@
+"""Pins of the tile-order oracle against the pages' tables, closed forms and
+hand-derived cases (CPU only)."""
+import random
+
+import pytest
+
+from conftest import read_lines, read_table
+from oracle import tile_order as to
+
+
+@pytest.mark.parametrize("fname,order,group", [
+    ("tbs_row_major_8x8.txt", to.ROW, 1),
+    ("tbs_panel_g4_8x8.txt", to.PANEL, 4),
+    ("tbs_morton_8x8.txt", to.MORTON, 1),
+    ("tbs_xor_8x8.txt", to.XOR, 1),
+])
+def test_8x8_tables(fname, order, group):
+    assert to.id_table(order, 8, 8, group) == read_table(fname)
+
+
+def test_col_major_is_transposed_row_major():
+    # closed form: tile (m, n) is reached by id n*gm + m
+    for gm, gn in [(8, 8), (3, 5), (5, 3), (1, 7)]:
+        t = to.id_table(to.COL, gm, gn)
+        assert t == [[n * gm + m for n in range(gn)] for m in range(gm)]
+    row = read_table("tbs_row_major_8x8.txt")
+    assert to.id_table(to.COL, 8, 8) == [list(r) for r in zip(*row)]
+
+
+def test_group_major_table_equals_panel():
+    assert to.id_table(to.PANEL, 4, 4, 2) == read_table("cps_group_major_4x4_g2.txt")
+
+
+def test_serpentine_table():
+    assert to.id_table(to.SERPENTINE, 4, 4, 2) == read_table("cps_serpentine_4x4_s2.txt")
+
+
+def test_panel_degenerate_groups():
+    # G = 1 walks rows (row-major); G >= gm is one band walked down columns.
+    for gm, gn in [(8, 8), (6, 10), (5, 3)]:
+        assert to.tile_sequence(to.PANEL, gm, gn, 1) == to.tile_sequence(to.ROW, gm, gn)
+        for g in (gm, gm + 3):
+            assert to.tile_sequence(to.PANEL, gm, gn, g) == to.tile_sequence(to.COL, gm, gn)
+
+
+def test_panel_ragged_last_band_by_hand():
+    # 5 x 3 grid, G = 2: bands of rows {0,1}, {2,3} and the 1-row tail {4}.
+    assert to.id_table(to.PANEL, 5, 3, 2) == [
+        [0, 2, 4], [1, 3, 5], [6, 8, 10], [7, 9, 11], [12, 13, 14]]
+
+
+def test_serpentine_degenerate_and_ragged():
+    for gm, gn in [(4, 4), (3, 7), (6, 2)]:
+        # one strip as wide as the grid: row-major
+        assert to.tile_sequence(to.SERPENTINE, gm, gn, gn) == to.tile_sequence(to.ROW, gm, gn)
+        # strips one tile wide: columns walked alternately down and up
+        assert to.id_table(to.SERPENTINE, gm, gn, 1) == [
+            [n * gm + (m if n % 2 == 0 else gm - 1 - m) for n in range(gn)]
+            for m in range(gm)]
+    # 3 x 5 grid, S = 2: strips {0,1} down, {2,3} up, tail strip {4} down
+    assert to.id_table(to.SERPENTINE, 3, 5, 2) == [
+        [0, 1, 10, 11, 12], [2, 3, 8, 9, 13], [4, 5, 6, 7, 14]]
+
+
+def test_morton_xor_bijective_on_square_powers_of_two():
+    # the first page: both are bijective for power-of-two (square) grids
+    for e in range(0, 7):
+        g = 1 << e
+        assert to.is_bijective(to.MORTON, g, g)
+        assert to.is_bijective(to.XOR, g, g)
+
+
+def test_morton_not_bijective_by_hand():
+    # 3 x 3: id 5 has bits 0b101 -> m = 0b11 = 3 -> 3 mod 3 = 0, n = 0: tile
+    # (0, 0) again, already taken by id 0.
+    assert to.morton(5, 3, 3) == (0, 0) == to.morton(0, 3, 3)
+    assert not to.is_bijective(to.MORTON, 3, 3)
+
+
+def test_xor_not_bijective_by_hand():
+    # 2 x 4 grid: id 0 -> x=0,y=0 -> (0,0); id 2 -> x=2,y=0 -> (2 mod 2, 0) = (0,0)
+    assert to.xor_swizzle(0, 2, 4) == to.xor_swizzle(2, 2, 4) == (0, 0)
+    assert not to.is_bijective(to.XOR, 2, 4)
+
+
+def test_panel_and_serpentine_always_bijective():
+    rnd = random.Random(1)
+    for _ in range(60):
+        gm, gn, g = rnd.randint(1, 23), rnd.randint(1, 23), rnd.randint(1, 9)
+        assert to.is_bijective(to.PANEL, gm, gn, g)
+        assert to.is_bijective(to.SERPENTINE, gm, gn, g)
+        assert to.is_bijective(to.ROW, gm, gn)
+        assert to.is_bijective(to.COL, gm, gn)
+
+
+def _three_cluster_fixture():
+    lines = read_lines("cps_three_clusters.txt")
+    owner, work, seq, cta = [], {}, {}, []
+    mode = None
+    for ln in lines:
+        if ln[0] == "owner":
+            mode = "owner"
+        elif ln[0] == "work":
+            work[int(ln[1])] = [int(v) for v in ln[2:]]
+        elif ln[0] == "seq":
+            v = [int(x) for x in ln[2:]]
+            seq[int(ln[1])] = list(zip(v[0::2], v[1::2]))
+        elif ln[0] == "cta":
+            cta.append([int(x) for x in ln[1:]])
+        elif mode == "owner":
+            owner.append([int(x) for x in ln])
+    return owner, work, seq, cta
+
+
+def test_three_cluster_distribution():
+    owner, work, seq, _ = _three_cluster_fixture()
+    seqs = to.cluster_sequences(4, 4, 3, to.PANEL, 2)
+    for c in range(3):
+        assert [w for w, _, _ in seqs[c]] == work[c]
+        assert [(m, n) for _, m, n in seqs[c]] == seq[c]
+        for _, m, n in seqs[c]:
+            assert owner[m][n] == c
+
+
+def test_scheduler_state_machine():
+    s = to.ClusterSchedule(4, 4, 3, to.PANEL, 2)
+    s.init(2)
+    assert (s.work_idx, s.tile_count, s.m_idx, s.n_idx) == (2, 0, 0, 1)
+    s.next_tile()
+    assert (s.work_idx, s.tile_count, s.m_idx, s.n_idx) == (5, 1, 1, 2)
+    s.next_tile_stride(100)
+    assert not s.valid() and s.tile_count == 2
+
+
+def test_cta_split_example():
+    *_, cta = _three_cluster_fixture()
+    for m_idx, n_idx, rank, cm, cn in cta:
+        assert to.cta_tile(m_idx, n_idx, rank, 2, 1) == (cm, cn)
+
+
+def test_persistent_trace_closed_forms():
+    gm, gn = 6, 5
+    for order, g in [(to.ROW, 1), (to.PANEL, 4), (to.SERPENTINE, 2)]:
+        ids = {mn: p for p, mn in enumerate(to.tile_sequence(order, gm, gn, g))}
+        # non-persistent: program p takes tile id p, once
+        tr = to.persistent_trace(order, gm, gn, g, gm * gn)
+        assert tr == {mn: (p, 0) for mn, p in ids.items()}
+        # persistent with P programs: id p runs on program p mod P at step p div P
+        P = 7
+        tr = to.persistent_trace(order, gm, gn, g, P)
+        assert tr == {mn: (p % P, p // P) for mn, p in ids.items()}
+    # 2-CTA clusters on a 6 x 5 CTA grid = 3 x 5 cluster grid, 4 clusters
+    cids = {mn: w for w, mn in enumerate(to.tile_sequence(to.PANEL, 3, 5, 2))}
+    tr = to.persistent_trace(to.PANEL, 6, 5, 2, 8, cluster_m=2)
+    assert len(tr) == 30
+    for (cm, n), (prog, it) in tr.items():
+        w = cids[(cm // 2, n)]
+        assert prog == 2 * (w % 4) + cm % 2 and it == w // 4
