@@ -1,0 +1,173 @@
+/*
+ * swz.h -- C ABI of libswz.so: thread-block-swizzled GEMM, tile maps and a
+ * shared-memory-swizzled transpose for NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (cited by page title and section):
+ *   [TBS] Lei Mao, "CUDA Thread Block Swizzle" -- tile orders (sections
+ *         "Linear Swizzle", "Grouped 2D Panel Swizzle", "Morton / Z-order
+ *         Swizzle", "Bitwise XOR Swizzle") and the benchmark's masked tiled
+ *         GEMM C = A*B with persistent / non-persistent launch.
+ *   [SBC] WHC, "CUDA Swizzle & bank conflict" -- section "Matrix Transpose"
+ *         (naive, padded and XOR-swizzled shared-memory tiles) and section
+ *         "Hopper TMA 的 swizzling" (the 128-byte swizzle the GEMM's operand
+ *         staging uses).
+ *   [CPS] TVM TIRx docs, "ClusterPersistentScheduler2D" -- group-major and
+ *         serpentine orders, work_idx = cluster_id + i * num_clusters, and
+ *         the cluster-tile -> CTA-tile split of "Example 2: 2SM GEMM".
+ *
+ * Conventions for every call:
+ *   - Device pointers are caller-owned global memory on the current device;
+ *     the library never allocates, frees or retains them.  Host pointers are
+ *     named h_* and are only read or written during the call.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; no call synchronises except
+ *     swz_check_status.
+ *   - Every call returns SWZ_OK (0) or a negative swz_status.  Arguments are
+ *     validated before anything is enqueued; on error nothing is enqueued.
+ *     No exception crosses the ABI.  Calls are thread-safe; the only
+ *     library-global state is the per-device status word read by
+ *     swz_check_status and the last CUDA error code.
+ */
+#ifndef SWZ_H_
+#define SWZ_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes -------------------------------------------------------- */
+enum swz_status {
+  SWZ_OK = 0,
+  SWZ_EINVAL = -1,         /* null pointer, bad size, bad enum, misalignment */
+  SWZ_ENOTBIJECTIVE = -2,  /* Morton/XOR order not a permutation of this grid */
+  SWZ_EARCH = -3,          /* current device is not sm_103 (GB300)            */
+  SWZ_ECUDA = -4,          /* a CUDA runtime call failed: swz_last_cuda_error */
+  SWZ_ETIMEOUT = -5,       /* a bounded device wait expired (swz_check_status)*/
+  SWZ_EUNSUPPORTED = -6    /* valid arguments, configuration not provided     */
+};
+
+/* ---- tile orders ([TBS] mode ids 0..4; 5 added for [CPS] serpentine) ----- */
+enum swz_order {
+  SWZ_ROW = 0,        /* m = id / gn, n = id % gn                              */
+  SWZ_COL = 1,        /* m = id % gm, n = id / gm                              */
+  SWZ_PANEL = 2,      /* grouped 2D panel, G rows per band (= [CPS] group-major)*/
+  SWZ_MORTON = 3,     /* bit 2i of id -> bit i of m, bit 2i+1 -> bit i of n    */
+  SWZ_XOR = 4,        /* m = ((id % gn) ^ (id / gn)) % gm, n = (id / gn) % gn  */
+  SWZ_SERPENTINE = 5  /* strips of S columns, rows walked down / up alternately*/
+};
+
+enum swz_dtype { SWZ_F16 = 0, SWZ_BF16 = 1 };
+
+/* shared-memory tile layouts of the transpose ([SBC] "Matrix Transpose") */
+enum swz_smem_layout {
+  SWZ_SMEM_NAIVE = 0,   /* tile[32][32], element (r,c) at r*32 + c            */
+  SWZ_SMEM_PADDED = 1,  /* tile[32][33], element (r,c) at r*33 + c            */
+  SWZ_SMEM_XOR = 2      /* tile[32][32], element (r,c) at r*32 + (c ^ r)      */
+};
+
+/*
+ * swz_tile_map -- [TBS] tile-order functions, [CPS] serpentine.
+ * For every program id p in [0, grid_m*grid_n) writes d_m[p], d_n[p]: the
+ * output tile (row, column) that `order` maps p to, computed on the device by
+ * the same function the GEMM's scheduler calls.  `group` is G for SWZ_PANEL
+ * and S for SWZ_SERPENTINE (>= 1), ignored otherwise.  d_m, d_n: device int32
+ * arrays of grid_m*grid_n entries.  Morton/XOR maps are written even when not
+ * bijective (the map is well defined; only the GEMM refuses them).
+ * Errors: SWZ_EINVAL (grid <= 0, grid_m*grid_n > 2^31-1, group < 1 where
+ * used, null arrays, unknown order), SWZ_EARCH, SWZ_ECUDA.
+ */
+int swz_tile_map(int order, int grid_m, int grid_n, int group,
+                 int32_t* d_m, int32_t* d_n, void* stream);
+
+/* Host-side check: 1 if `order` visits each of the grid_m x grid_n tiles
+ * exactly once, 0 if not, SWZ_EINVAL on bad arguments. */
+int swz_is_bijective(int order, int grid_m, int grid_n, int group);
+
+/*
+ * swz_gemm -- [TBS] benchmark GEMM: C = A * B with FP32 accumulation.
+ * A: M x K, B: K x N, both row-major fp16 on the device; C: M x N row-major
+ * FP32 (written, never read).  Output tiles are 128 x 256 (128 x 128 when
+ * N <= 128), visited in `order` (group = G or S as in swz_tile_map).
+ * persistent = 0: one CTA per output tile, tile = order(blockIdx.x) ([TBS]
+ * non-persistent launch); persistent = 1: min(tiles, resident CTAs) CTAs,
+ * CTA b takes tile ids b, b + P, b + 2P, ... ([TBS] persistent loop, [CPS]
+ * work_idx striding).  Ragged M, N, K are handled (TMA zero-fill on loads,
+ * clipped stores).  K = 0 writes zeros; M = 0 or N = 0 is a no-op.
+ * Requirements: A, B 16-byte aligned; C 16-byte aligned; K % 8 == 0,
+ * N % 8 == 0; M, N, K < 2^31.  Errors: SWZ_EINVAL, SWZ_ENOTBIJECTIVE (Morton
+ * or XOR on a grid they do not permute), SWZ_EARCH, SWZ_ECUDA.
+ */
+int swz_gemm(const void* A, const void* B, float* C, int M, int N, int K,
+             int order, int group, int persistent, void* stream);
+
+/* Options of swz_gemm_ex (zero-initialise, then set what you need). */
+typedef struct swz_gemm_opts {
+  int dtype;         /* SWZ_F16 (default) or SWZ_BF16; A and B share it      */
+  int tile_n;        /* 128 or 256; 0 = automatic as in swz_gemm             */
+  int cta_pair;      /* 1: 2-CTA clusters, tcgen05 cta_group::2, cluster tile
+                        256 x tile_n (tile_n must be 256; each CTA owns
+                        128 x 256 of C) -- [CPS] Example 2; 0: single CTA    */
+  int num_programs;  /* persistent only: CTAs to launch (a multiple of 2 with
+                        cta_pair); 0 = resident capacity, capped at the tile
+                        count                                                */
+  int32_t* d_trace;  /* optional device array, 2 int32 per CTA tile, indexed
+                        (cta_m * tiles_n + cta_n): {program (blockIdx.x),
+                        iteration of that program's tile loop}               */
+  uint32_t debug_flags; /* SWZ_DEBUG_*; 0 in normal use                      */
+  uint32_t timeout_ms;  /* bound of every device wait; 0 = 2000 ms           */
+} swz_gemm_opts;
+
+/* debug_flags: withhold the first operand load so that the consumer's
+ * bounded wait expires; the kernel then records SWZ_ETIMEOUT for
+ * swz_check_status and exits cleanly (tests of the timeout path only). */
+#define SWZ_DEBUG_SKIP_FIRST_LOAD 1u
+
+/* swz_gemm with explicit tile shape, dtype, 2-CTA mode, program count, trace
+ * and wait bound.  opts may be NULL (= swz_gemm).  Extra errors:
+ * SWZ_EUNSUPPORTED for tile_n not in {0,128,256} or cta_pair with tile_n
+ * != 256. */
+int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N, int K,
+                int order, int group, int persistent,
+                const swz_gemm_opts* opts, void* stream);
+
+/* Grid and launch the GEMM would use, without launching: tiles_m, tiles_n
+ * (CTA tiles), sched_m, sched_n (scheduler grid: cluster tiles in 2-CTA mode)
+ * and programs (CTAs launched).  Any out pointer may be NULL. */
+int swz_gemm_plan(int M, int N, int K, int persistent,
+                  const swz_gemm_opts* opts, int* tiles_m, int* tiles_n,
+                  int* sched_m, int* sched_n, int* programs);
+
+/*
+ * swz_transpose -- [SBC] "Matrix Transpose": out[j][i] = in[i][j] for an
+ * M x N matrix of 32-bit words (out is N x M, row-major), staged through a
+ * 32 x 32 shared-memory tile in `layout` (swz_smem_layout).  The result is
+ * bit-identical for all layouts; they differ in shared-memory bank conflicts
+ * (naive: 31 per warp store; padded and XOR: none).  Any M, N >= 0 (ragged
+ * edges clipped; 0 = no-op), M, N <= 2^31-1 with M*N < 2^62 and M/32 < 65536
+ * tiles along M.  in, out: device, 4-byte aligned, must not overlap.
+ * Errors: SWZ_EINVAL, SWZ_EARCH, SWZ_ECUDA.
+ */
+int swz_transpose(const uint32_t* in, uint32_t* out, int M, int N, int layout,
+                  void* stream);
+
+/* Synchronises `stream`, then returns and clears the current device's
+ * status word: SWZ_OK, or SWZ_ETIMEOUT if a kernel's bounded wait expired
+ * since the last check. */
+int swz_check_status(void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* swz_strerror(int status);
+
+/* cudaError_t of the last failing CUDA call in this thread (0 if none). */
+int swz_last_cuda_error(void);
+
+/* Properties of the current device the scheduler uses: SM count, L2 bytes,
+ * compute capability.  Out pointers may be NULL. */
+int swz_device_info(int* num_sms, int* l2_bytes, int* cc_major, int* cc_minor);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SWZ_H_ */

@@ -1,0 +1,218 @@
+"""Python binding of libswz.so (include/swz.h): argument marshalling only.
+
+Every computation runs in the library's CUDA kernels; PyTorch supplies device
+memory and streams.  There is no fallback: if the library is missing or the
+device is not sm_103, calls raise.
+
+Two layers:
+  * ``swz_*`` -- one-to-one mirrors of the C entry points (raw device
+    pointers as ints, stream as an int cudaStream_t).
+  * ``tile_map``, ``gemm``, ``transpose``, ``gemm_plan`` -- the same calls on
+    torch tensors (pointers and the current stream are taken from them).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libswz.so")
+
+# status codes and enums (include/swz.h)
+SWZ_OK, SWZ_EINVAL, SWZ_ENOTBIJECTIVE, SWZ_EARCH, SWZ_ECUDA, SWZ_ETIMEOUT, SWZ_EUNSUPPORTED = (
+    0, -1, -2, -3, -4, -5, -6)
+SWZ_ROW, SWZ_COL, SWZ_PANEL, SWZ_MORTON, SWZ_XOR, SWZ_SERPENTINE = range(6)
+SWZ_F16, SWZ_BF16 = 0, 1
+SWZ_SMEM_NAIVE, SWZ_SMEM_PADDED, SWZ_SMEM_XOR = 0, 1, 2
+SWZ_DEBUG_SKIP_FIRST_LOAD = 1
+ORDERS = {"row": SWZ_ROW, "col": SWZ_COL, "panel": SWZ_PANEL, "morton": SWZ_MORTON,
+          "xor": SWZ_XOR, "serpentine": SWZ_SERPENTINE}
+LAYOUTS = {"naive": SWZ_SMEM_NAIVE, "padded": SWZ_SMEM_PADDED, "xor": SWZ_SMEM_XOR}
+
+EXPORTS = ["swz_tile_map", "swz_is_bijective", "swz_gemm", "swz_gemm_ex", "swz_gemm_plan",
+           "swz_transpose", "swz_check_status", "swz_strerror", "swz_last_cuda_error",
+           "swz_device_info"]
+
+
+class SwzError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} (status {code}, "
+                         f"cuda error {swz_last_cuda_error()})")
+
+
+class swz_gemm_opts(ctypes.Structure):
+    _fields_ = [("dtype", ctypes.c_int), ("tile_n", ctypes.c_int), ("cta_pair", ctypes.c_int),
+                ("num_programs", ctypes.c_int), ("d_trace", ctypes.c_void_p),
+                ("debug_flags", ctypes.c_uint32), ("timeout_ms", ctypes.c_uint32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libswz.so (built by thread_block_smem_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libswz.so not built ({LIB_PATH}); run "
+                               "`python -m thread_block_smem_gb300.build` first")
+        L = ctypes.CDLL(LIB_PATH)
+        i, vp, u32 = ctypes.c_int, ctypes.c_void_p, ctypes.c_uint32
+        ip = ctypes.POINTER(ctypes.c_int)
+        L.swz_tile_map.argtypes = [i, i, i, i, vp, vp, vp]
+        L.swz_is_bijective.argtypes = [i, i, i, i]
+        L.swz_gemm.argtypes = [vp, vp, vp, i, i, i, i, i, i, vp]
+        L.swz_gemm_ex.argtypes = [vp, vp, vp, i, i, i, i, i, i, ctypes.POINTER(swz_gemm_opts), vp]
+        L.swz_gemm_plan.argtypes = [i, i, i, i, ctypes.POINTER(swz_gemm_opts), ip, ip, ip, ip, ip]
+        L.swz_transpose.argtypes = [vp, vp, i, i, i, vp]
+        L.swz_check_status.argtypes = [vp]
+        L.swz_strerror.argtypes = [i]
+        L.swz_strerror.restype = ctypes.c_char_p
+        L.swz_last_cuda_error.argtypes = []
+        L.swz_device_info.argtypes = [ip, ip, ip, ip]
+        for name in EXPORTS:
+            if name != "swz_strerror":
+                getattr(L, name).restype = ctypes.c_int
+        del u32
+        _lib = L
+    return _lib
+
+
+# ---- raw mirrors ------------------------------------------------------------
+def swz_tile_map(order, grid_m, grid_n, group, d_m, d_n, stream=0):
+    return lib().swz_tile_map(order, grid_m, grid_n, group, d_m, d_n, stream)
+
+
+def swz_is_bijective(order, grid_m, grid_n, group=1):
+    return lib().swz_is_bijective(order, grid_m, grid_n, group)
+
+
+def swz_gemm(A, B, C, M, N, K, order, group, persistent, stream=0):
+    return lib().swz_gemm(A, B, C, M, N, K, order, group, persistent, stream)
+
+
+def swz_gemm_ex(A, B, C, M, N, K, order, group, persistent, opts, stream=0):
+    return lib().swz_gemm_ex(A, B, C, M, N, K, order, group, persistent,
+                             ctypes.byref(opts) if opts is not None else None, stream)
+
+
+def swz_gemm_plan(M, N, K, persistent, opts=None):
+    out = [ctypes.c_int(0) for _ in range(5)]
+    rc = lib().swz_gemm_plan(M, N, K, persistent,
+                             ctypes.byref(opts) if opts is not None else None,
+                             *[ctypes.byref(o) for o in out])
+    return rc, tuple(o.value for o in out)
+
+
+def swz_transpose(src, dst, M, N, layout, stream=0):
+    return lib().swz_transpose(src, dst, M, N, layout, stream)
+
+
+def swz_check_status(stream=0):
+    return lib().swz_check_status(stream)
+
+
+def swz_strerror(code):
+    return lib().swz_strerror(code).decode()
+
+
+def swz_last_cuda_error():
+    return lib().swz_last_cuda_error()
+
+
+def swz_device_info():
+    v = [ctypes.c_int(0) for _ in range(4)]
+    rc = lib().swz_device_info(*[ctypes.byref(x) for x in v])
+    return rc, tuple(x.value for x in v)
+
+
+strerror = swz_strerror
+
+
+def _check(rc, what):
+    if rc != SWZ_OK:
+        raise SwzError(rc, what)
+
+
+# ---- tensor-level calls -----------------------------------------------------
+def _stream(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _order(order):
+    return ORDERS[order] if isinstance(order, str) else int(order)
+
+
+def tile_map(order, grid_m, grid_n, group=1, device="cuda", stream=None):
+    """Device-computed tile map: (m, n) int32 tensors of length grid_m*grid_n."""
+    import torch
+    m = torch.empty(grid_m * grid_n, dtype=torch.int32, device=device)
+    n = torch.empty_like(m)
+    _check(swz_tile_map(_order(order), grid_m, grid_n, group, m.data_ptr(), n.data_ptr(),
+                        _stream(stream)), "swz_tile_map")
+    return m, n
+
+
+def make_opts(dtype=SWZ_F16, tile_n=0, cta_pair=False, num_programs=0, trace=None,
+              debug_flags=0, timeout_ms=0):
+    o = swz_gemm_opts()
+    o.dtype = dtype
+    o.tile_n = tile_n
+    o.cta_pair = 1 if cta_pair else 0
+    o.num_programs = num_programs
+    o.d_trace = trace.data_ptr() if trace is not None else None
+    o.debug_flags = debug_flags
+    o.timeout_ms = timeout_ms
+    return o
+
+
+def gemm_plan(M, N, K, persistent=False, tile_n=0, cta_pair=False, num_programs=0):
+    """(tiles_m, tiles_n, sched_m, sched_n, programs) of a GEMM launch."""
+    rc, v = swz_gemm_plan(M, N, K, int(bool(persistent)),
+                          make_opts(tile_n=tile_n, cta_pair=cta_pair, num_programs=num_programs))
+    _check(rc, "swz_gemm_plan")
+    return v
+
+
+def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
+         cta_pair=False, num_programs=0, trace=None, debug_flags=0, timeout_ms=0,
+         stream=None):
+    """C = A @ B (fp32) through swz_gemm_ex.  A: M x K, B: K x N, both fp16 or
+    both bf16, row-major contiguous CUDA tensors."""
+    import torch
+    if A.dtype != B.dtype or A.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("A and B must both be fp16 or both bf16")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
+        raise ValueError("A: M x K and B: K x N expected")
+    if not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("row-major contiguous operands expected")
+    M, K = A.shape
+    N = B.shape[1]
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=A.device)
+    opts = make_opts(SWZ_BF16 if A.dtype == torch.bfloat16 else SWZ_F16, tile_n, cta_pair,
+                     num_programs, trace, debug_flags, timeout_ms)
+    _check(swz_gemm_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _order(order),
+                       group, int(bool(persistent)), opts, _stream(stream)), "swz_gemm_ex")
+    return C
+
+
+def transpose(x, layout="xor", out=None, stream=None):
+    """N x M transpose of an M x N 32-bit CUDA tensor through swz_transpose."""
+    import torch
+    if x.dim() != 2 or x.element_size() != 4 or not x.is_contiguous():
+        raise ValueError("contiguous 2-D tensor of 32-bit words expected")
+    M, N = x.shape
+    y = out if out is not None else torch.empty((N, M), dtype=x.dtype, device=x.device)
+    lay = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+    _check(swz_transpose(x.data_ptr(), y.data_ptr(), M, N, lay, _stream(stream)),
+           "swz_transpose")
+    return y
+
+
+def check_status(stream=None):
+    """Raises SwzError(SWZ_ETIMEOUT) if a bounded device wait expired."""
+    _check(swz_check_status(_stream(stream)), "swz_check_status")

@@ -1,0 +1,44 @@
+// common.h -- host-side helpers shared by the entry points of libswz.so:
+// status codes, CUDA error capture and the device-architecture check.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/swz.h"
+
+namespace swz {
+
+// cudaError_t of the last failing CUDA call made by this thread.
+int& last_cuda_error_slot();
+
+// Records a failing CUDA call and maps it to SWZ_ECUDA.
+inline int cuda_fail(cudaError_t e) {
+  last_cuda_error_slot() = static_cast<int>(e);
+  return SWZ_ECUDA;
+}
+
+#define SWZ_CUDA_TRY(expr)                       \
+  do {                                           \
+    cudaError_t swz_e_ = (expr);                 \
+    if (swz_e_ != cudaSuccess) return ::swz::cuda_fail(swz_e_); \
+  } while (0)
+
+// Current device, its SM count and whether it is sm_103 (GB300).
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int l2_bytes;
+  int cc_major, cc_minor;
+};
+
+// Fills `info` for the current device; SWZ_OK, SWZ_ECUDA or SWZ_EARCH.
+int current_device(DeviceInfo* info, bool require_sm103 = true);
+
+// True when `order` visits each tile of the gm x gn grid exactly once
+// (host-side exhaustive check over all ids).
+bool order_is_bijective(int order, uint32_t gm, uint32_t gn, uint32_t group);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+}  // namespace swz

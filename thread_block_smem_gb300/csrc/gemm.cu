@@ -1,0 +1,611 @@
+// gemm.cu -- C = A * B (fp16/bf16 in, fp32 accumulate and out) on sm_103a
+// with a selectable thread-block swizzle and a persistent tile scheduler.
+//
+// What it computes: the masked tiled GEMM of Lei Mao, "CUDA Thread Block
+// Swizzle" (benchmark section: program id -> output tile through the chosen
+// tile order, a K loop per tile, masked loads and stores, persistent launch =
+// each program takes tile ids pid, pid + P, pid + 2P, ...).  The scheduler is
+// the work-index stride of TVM TIRx "ClusterPersistentScheduler2D"
+// (work_idx = cluster_id + i * num_clusters, cluster tiles split into CTA
+// tiles as in its "Example 2: 2SM GEMM").  Operands are staged with the
+// 128-byte TMA swizzle of WHC, "CUDA Swizzle & bank conflict", section
+// "Hopper TMA 的 swizzling" (16-byte chunk index XOR row mod 8 inside each
+// 1024-byte atom), which the tensor cores read without bank conflicts.
+//
+// Design (GB300 / sm_103a):
+//   * 192 threads per CTA, one CTA per SM.  Warp 0: TMA producer.  Warp 1:
+//     TMEM allocator and (one lane) tcgen05.mma issuer.  Warps 2-5: epilogue
+//     (warp w reads TMEM lanes 32*(w%4) .. +31).
+//   * K is consumed in blocks of 64 elements (128 bytes per A row) through a
+//     ring of STAGES shared-memory stages guarded by full/empty mbarriers.
+//     A tile: 128 x 64, K-major.  B tile: 64 x BN_LOCAL, N-major (B is K x N
+//     row-major), loaded as 64-column boxes.
+//   * The accumulator lives in TMEM, double-buffered (2 x BN fp32 columns),
+//     so the epilogue of tile i overlaps the MMAs of tile i+1.
+//   * CTA pair (PAIR): 2-CTA cluster, tcgen05 cta_group::2, MMA 256 x 256.
+//     Each CTA loads its own 128 rows of A and its half (128 columns) of B;
+//     the leader issues the MMAs and its commits are multicast to both CTAs.
+//   * Every wait is bounded (globaltimer); on expiry the kernel records
+//     SWZ_ETIMEOUT in a device status word, drains what it issued, frees TMEM
+//     and returns.
+#include <mutex>
+
+#include "common.h"
+#include "ptx.cuh"
+#include "tile_order.cuh"
+
+namespace swz {
+
+__device__ unsigned int g_status_word;  // nonzero: a bounded wait expired
+
+namespace gemm {
+
+constexpr int BM = 128;        // CTA tile rows = TMEM lanes
+constexpr int BK = 64;         // K elements per stage (one 128-byte swizzle row)
+constexpr int UMMA_K = 16;     // K of one tcgen05.mma kind::f16
+constexpr int kThreads = 192;  // 6 warps
+constexpr int kSmemBudget = 200 * 1024;
+
+template <int BN, bool PAIR>
+struct Cfg {
+  static constexpr int CG = PAIR ? 2 : 1;
+  static constexpr int BN_LOCAL = PAIR ? BN / 2 : BN;  // B columns this CTA loads
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BOX_BYTES = 64 * BK * 2;      // one 64-column B box
+  static constexpr int B_BYTES = BK * BN_LOCAL * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = kSmemBudget / STAGE_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int UMMA_M = PAIR ? 256 : 128;
+  static constexpr uint32_t TX_BYTES = uint32_t(CG) * STAGE_BYTES;
+  static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1024-byte swizzle atoms");
+  static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation size");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
+// A and B format (bits 7-9, 10-12: 0 fp16, 1 bf16), A K-major (bit 15 = 0),
+// B MN-major (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(int dtype, int m, int n) {
+  return (1u << 4) | (uint32_t(dtype) << 7) | (uint32_t(dtype) << 10) | (1u << 16) |
+         (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor: start address >> 4 (bits 0-13), leading
+// byte offset >> 4 (16-29), stride byte offset >> 4 (32-45), the fixed
+// 0b001 at bits 46-48, base offset 0 (atoms are 1024-byte aligned), swizzle
+// mode 2 = 128-byte swizzle (bits 61-63).
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+struct Params {
+  float* C;
+  int M, N, K;
+  int order, group;
+  uint32_t sched_m, sched_n;  // scheduler grid (cluster tiles with PAIR)
+  uint32_t num_kb;            // ceil(K / BK)
+  uint32_t idesc;
+  int32_t* trace;
+  uint32_t debug_flags;
+  uint64_t timeout_ns;
+};
+
+struct Ctl {
+  volatile int* abort_flag;
+  uint32_t peer_abort;  // shared::cluster address of the peer's flag (PAIR)
+  uint64_t timeout_ns;
+  bool pair;
+};
+
+__device__ __noinline__ void raise_abort(const Ctl& c) {
+  atomicCAS(&g_status_word, 0u, 1u);
+  *c.abort_flag = 1;
+  if (c.pair) asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(c.peer_abort), "r"(1) : "memory");
+}
+
+// Waits for the phase of `bar` with parity `parity`; false if the kernel
+// is aborting or the bound expired (then the abort is raised).
+__device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Ctl& c) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((n & 31u) == 0) {
+      if (*c.abort_flag) return false;
+      if (ptx::global_timer_ns() - t0 > c.timeout_ns) {
+        raise_abort(c);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = ptx::global_timer_ns();
+  while (ptx::global_timer_ns() - t0 < ns) __nanosleep(1000);
+}
+
+template <int BN, bool PAIR>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ Params p) {
+  using K_ = Cfg<BN, PAIR>;
+  constexpr int CL = K_::CG;
+  constexpr int STAGES = K_::STAGES;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sA = ptx::smem_u32(smem);
+  const uint32_t sB = sA + STAGES * K_::A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * K_::STAGE_BYTES);
+  const uint32_t bar0 = ptx::smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmB);
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(full_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(tfull_bar(a), 1);
+      ptx::mbar_init(tempty_bar(a), PAIR ? 8 : 4);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc<CL>(ptx::smem_u32(tmem_slot), K_::TMEM_COLS);
+    ptx::tmem_relinquish<CL>();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if constexpr (PAIR) ptx::cluster_sync();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  Ctl ctl;
+  ctl.abort_flag = abort_flag;
+  ctl.peer_abort = PAIR ? ptx::map_to_rank(ptx::smem_u32(abort_flag), rank ^ 1u) : 0u;
+  ctl.timeout_ns = p.timeout_ns;
+  ctl.pair = PAIR;
+
+  const uint32_t units = p.sched_m * p.sched_n;
+  const uint32_t first = blockIdx.x / CL, stride = gridDim.x / CL;
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      bool skip = (p.debug_flags & SWZ_DEBUG_SKIP_FIRST_LOAD) != 0;
+      for (uint32_t w = first; w < units && !aborted; w += stride) {
+        const TileCoord t = tile_of(p.order, w, p.sched_m, p.sched_n, uint32_t(p.group));
+        const int32_t m0 = int32_t((t.m * CL + rank) * BM);
+        const int32_t n0 = int32_t(t.n * BN + rank * K_::BN_LOCAL);
+        for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait(empty_bar(stage), phase ^ 1u, ctl)) { aborted = true; break; }
+          if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), K_::TX_BYTES);
+          if (skip) {
+            skip = false;
+          } else {
+            const uint32_t fb = PAIR ? ptx::map_to_rank(full_bar(stage), 0) : full_bar(stage);
+            const int32_t k0 = int32_t(kb * BK);
+            if constexpr (PAIR) {
+              ptx::tma_load_2d_pair(sA + stage * K_::A_BYTES, &tmA, fb, k0, m0);
+#pragma unroll
+              for (int j = 0; j < K_::BN_LOCAL / 64; ++j)
+                ptx::tma_load_2d_pair(sB + stage * K_::B_BYTES + j * K_::B_BOX_BYTES, &tmB, fb,
+                                      n0 + 64 * j, k0);
+            } else {
+              ptx::tma_load_2d(sA + stage * K_::A_BYTES, &tmA, fb, k0, m0);
+#pragma unroll
+              for (int j = 0; j < K_::BN_LOCAL / 64; ++j)
+                ptx::tma_load_2d(sB + stage * K_::B_BYTES + j * K_::B_BOX_BYTES, &tmB, fb,
+                                 n0 + 64 * j, k0);
+            }
+          }
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // Tail: wait until every stage has been released, so that no MMA
+      // commit (possibly multicast from the leader) is still in flight
+      // towards this CTA's barriers when it exits.
+      for (int i = 0; i < STAGES && !aborted; ++i) {
+        if (!wait(empty_bar(stage), phase ^ 1u, ctl)) aborted = true;
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (aborted) spin_ns(50000);  // let copies already issued land
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (leader CTA) ----------------
+    if (lane == 0 && leader) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool issued = false;
+      for (uint32_t w = first; w < units && !aborted; w += stride) {
+        if (!wait(tempty_bar(acc), acc_phase ^ 1u, ctl)) { aborted = true; break; }
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait(full_bar(stage), phase, ctl)) { aborted = true; break; }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = sA + stage * K_::A_BYTES;
+          const uint32_t b_addr = sB + stage * K_::B_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // A: K-major; the 16-element K slice starts 32 bytes further
+            // into each 128-byte row; 8-row groups are 1024 bytes apart.
+            const uint64_t adesc = make_sdesc(a_addr + kk * 32, 16, 1024);
+            // B: N-major; 16 K rows of 128 bytes further; 8-row groups
+            // 1024 bytes apart along K, 64-column boxes B_BOX_BYTES apart.
+            const uint64_t bdesc = make_sdesc(b_addr + kk * 2048, K_::B_BOX_BYTES, 1024);
+            ptx::mma_f16<CL>(d, adesc, bdesc, p.idesc, (kb | uint32_t(kk)) != 0u);
+          }
+          issued = true;
+          if constexpr (PAIR) ptx::mma_commit_pair(empty_bar(stage), 0x3);
+          else ptx::mma_commit(empty_bar(stage));
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (aborted) break;
+        if constexpr (PAIR) ptx::mma_commit_pair(tfull_bar(acc), 0x3);
+        else ptx::mma_commit(tfull_bar(acc));
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      if (aborted && issued) {
+        // drain: wait (bounded) until every MMA issued so far has completed
+        if constexpr (PAIR) ptx::mma_commit_pair(drain_bar, 0x1);
+        else ptx::mma_commit(drain_bar);
+        const uint64_t t0 = ptx::global_timer_ns();
+        while (!ptx::mbar_try_wait(drain_bar, 0) && ptx::global_timer_ns() - t0 < p.timeout_ns) {
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: TMEM -> registers -> C ----------------
+    const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may access
+    uint32_t acc = 0, acc_phase = 0, it = 0;
+    for (uint32_t w = first; w < units; w += stride, ++it) {
+      const bool ok = wait(tfull_bar(acc), acc_phase, ctl);
+      if (!__all_sync(0xFFFFFFFFu, ok)) { aborted = true; break; }
+      ptx::tc_fence_after();
+      const TileCoord t = tile_of(p.order, w, p.sched_m, p.sched_n, uint32_t(p.group));
+      const uint32_t cta_m = t.m * CL + rank, cta_n = t.n;
+      const int64_t row = int64_t(cta_m) * BM + q * 32 + lane;
+      const int32_t col0 = int32_t(cta_n) * BN;
+      float* crow = p.C + row * p.N + col0;
+      const uint32_t taddr = tmem_base + ((q * 32u) << 16) + acc * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(taddr + c, r);
+        ptx::tmem_ld_wait();
+        if (row < p.M) {
+          if (col0 + c + 32 <= p.N) {
+            float4* dst = reinterpret_cast<float4*>(crow + c);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + c + j < p.N) crow[c + j] = __uint_as_float(r[j]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
+        else ptx::mbar_arrive(tempty_bar(acc));
+        if (warp == 2 && p.trace) {
+          const uint64_t idx = uint64_t(cta_m) * p.sched_n + cta_n;
+          p.trace[2 * idx] = int32_t(blockIdx.x);
+          p.trace[2 * idx + 1] = int32_t(it);
+        }
+      }
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  // ---------------- teardown ----------------
+  ptx::tc_fence_before();
+  __syncthreads();
+  if constexpr (PAIR) ptx::cluster_sync();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc<CL>(tmem_base, K_::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D row-major matrix rows x cols of 2-byte elements, box box_cols x box_rows,
+// 128-byte swizzle, out-of-bounds elements read as zero.
+static int encode_2d(CUtensorMap* map, int dtype, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cuda_fail(cudaErrorNotSupported);
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, dtype == SWZ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                        2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return SWZ_OK;
+}
+
+struct Plan {
+  int bn;
+  bool pair;
+  uint32_t tiles_m, tiles_n, sched_m, sched_n, units;
+  int programs;
+};
+
+template <int BN, bool PAIR>
+static int kernel_capacity(const DeviceInfo& dev, int* programs) {
+  using K_ = Cfg<BN, PAIR>;
+  static std::mutex mu;
+  static int cache[64] = {};
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev.device] > 0) {
+      *programs = cache[dev.device];
+      return SWZ_OK;
+    }
+  }
+  auto kern = gemm_kernel<BN, PAIR>;
+  SWZ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    K_::SMEM_BYTES));
+  int cap = 0;
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * dev.num_sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = K_::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    SWZ_CUDA_TRY(cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg));
+    cap = 2 * clusters;
+  } else {
+    int per_sm = 0;
+    SWZ_CUDA_TRY(
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, K_::SMEM_BYTES));
+    cap = per_sm * dev.num_sms;
+  }
+  if (cap <= 0) return SWZ_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  cache[dev.device] = cap;
+  *programs = cap;
+  return SWZ_OK;
+}
+
+static int capacity_for(const Plan& pl, const DeviceInfo& dev, int* cap) {
+  if (pl.pair) return kernel_capacity<256, true>(dev, cap);
+  if (pl.bn == 128) return kernel_capacity<128, false>(dev, cap);
+  return kernel_capacity<256, false>(dev, cap);
+}
+
+static int make_plan(int M, int N, int persistent, const swz_gemm_opts& o, const DeviceInfo* dev,
+                     Plan* pl) {
+  if (o.tile_n != 0 && o.tile_n != 128 && o.tile_n != 256) return SWZ_EUNSUPPORTED;
+  pl->pair = o.cta_pair != 0;
+  pl->bn = o.tile_n ? o.tile_n : (pl->pair || N > 128 ? 256 : 128);
+  if (pl->pair && pl->bn != 256) return SWZ_EUNSUPPORTED;
+  const int cl = pl->pair ? 2 : 1;
+  const uint64_t sm = (uint64_t(M) + BM * cl - 1) / (BM * cl);
+  const uint64_t sn = (uint64_t(N) + pl->bn - 1) / pl->bn;
+  if (sm * sn * cl > uint64_t(INT32_MAX)) return SWZ_EINVAL;
+  pl->sched_m = uint32_t(sm);
+  pl->sched_n = uint32_t(sn);
+  pl->tiles_m = uint32_t(sm * cl);
+  pl->tiles_n = uint32_t(sn);
+  pl->units = uint32_t(sm * sn);
+  if (o.num_programs < 0 || (o.num_programs % cl) != 0) return SWZ_EINVAL;
+  if (!persistent) {
+    pl->programs = int(pl->units) * cl;
+  } else {
+    int cap = o.num_programs;
+    if (cap == 0) {
+      if (!dev) return SWZ_EINVAL;
+      const int rc = capacity_for(*pl, *dev, &cap);
+      if (rc != SWZ_OK) return rc;
+    }
+    const uint32_t units_cap = uint32_t(cap / cl);
+    pl->programs = int(pl->units < units_cap ? pl->units : units_cap) * cl;
+  }
+  return SWZ_OK;
+}
+
+template <int BN, bool PAIR>
+static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm,
+                  cudaStream_t stream) {
+  using K_ = Cfg<BN, PAIR>;
+  static std::mutex mu;
+  static bool attr_set[64] = {};
+  auto kern = gemm_kernel<BN, PAIR>;
+  int dev = 0;
+  SWZ_CUDA_TRY(cudaGetDevice(&dev));
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev]) {
+      SWZ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        K_::SMEM_BYTES));
+      attr_set[dev] = true;
+    }
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(pl.programs));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = K_::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if constexpr (PAIR) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  SWZ_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ta, tb, prm));
+  return SWZ_OK;
+}
+
+}  // namespace gemm
+}  // namespace swz
+
+using namespace swz;
+using namespace swz::gemm;
+
+static int validate(const void* A, const void* B, const float* C, int M, int N, int K, int order,
+                    int group, const swz_gemm_opts& o) {
+  if (M < 0 || N < 0 || K < 0) return SWZ_EINVAL;
+  if (!order_is_valid(order)) return SWZ_EINVAL;
+  if (order_uses_group(order) && group < 1) return SWZ_EINVAL;
+  if (o.dtype != SWZ_F16 && o.dtype != SWZ_BF16) return SWZ_EINVAL;
+  if (M == 0 || N == 0) return SWZ_OK;
+  if (!C || !aligned16(C)) return SWZ_EINVAL;
+  if (K == 0) return SWZ_OK;
+  if (!A || !B || !aligned16(A) || !aligned16(B)) return SWZ_EINVAL;
+  if (K % 8 != 0 || N % 8 != 0) return SWZ_EINVAL;
+  return SWZ_OK;
+}
+
+extern "C" int swz_gemm_plan(int M, int N, int K, int persistent, const swz_gemm_opts* opts,
+                             int* tiles_m, int* tiles_n, int* sched_m, int* sched_n,
+                             int* programs) {
+  swz_gemm_opts o = {};
+  if (opts) o = *opts;
+  if (M <= 0 || N <= 0 || K < 0) return SWZ_EINVAL;
+  DeviceInfo dev{};
+  const bool need_dev = persistent && o.num_programs == 0;
+  if (need_dev) {
+    const int rc = current_device(&dev);
+    if (rc != SWZ_OK) return rc;
+  }
+  Plan pl{};
+  const int rc = make_plan(M, N, persistent, o, need_dev ? &dev : nullptr, &pl);
+  if (rc != SWZ_OK) return rc;
+  if (tiles_m) *tiles_m = int(pl.tiles_m);
+  if (tiles_n) *tiles_n = int(pl.tiles_n);
+  if (sched_m) *sched_m = int(pl.sched_m);
+  if (sched_n) *sched_n = int(pl.sched_n);
+  if (programs) *programs = pl.programs;
+  return SWZ_OK;
+}
+
+extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N, int K, int order,
+                           int group, int persistent, const swz_gemm_opts* opts, void* stream) {
+  swz_gemm_opts o = {};
+  if (opts) o = *opts;
+  int rc = validate(A, B, C, M, N, K, order, group, o);
+  if (rc != SWZ_OK) return rc;
+  if (M == 0 || N == 0) return SWZ_OK;
+  DeviceInfo dev{};
+  rc = current_device(&dev);
+  if (rc != SWZ_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (K == 0) {
+    SWZ_CUDA_TRY(cudaMemsetAsync(C, 0, size_t(M) * size_t(N) * sizeof(float), s));
+    return SWZ_OK;
+  }
+  Plan pl{};
+  rc = make_plan(M, N, persistent, o, &dev, &pl);
+  if (rc != SWZ_OK) return rc;
+  const uint32_t g = order_uses_group(order) ? uint32_t(group) : 1u;
+  if ((order == kMorton || order == kXor) &&
+      !order_is_bijective(order, pl.sched_m, pl.sched_n, g))
+    return SWZ_ENOTBIJECTIVE;
+
+  CUtensorMap ta, tb;
+  rc = encode_2d(&ta, o.dtype, A, uint64_t(M), uint64_t(K), BK, BM);
+  if (rc != SWZ_OK) return rc;
+  rc = encode_2d(&tb, o.dtype, B, uint64_t(K), uint64_t(N), 64, BK);
+  if (rc != SWZ_OK) return rc;
+
+  Params prm{};
+  prm.C = C;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.order = order;
+  prm.group = int(g);
+  prm.sched_m = pl.sched_m;
+  prm.sched_n = pl.sched_n;
+  prm.num_kb = uint32_t((K + BK - 1) / BK);
+  prm.idesc = make_idesc(o.dtype, pl.pair ? 256 : 128, pl.bn);
+  prm.trace = o.d_trace;
+  prm.debug_flags = o.debug_flags;
+  prm.timeout_ns = uint64_t(o.timeout_ms ? o.timeout_ms : 2000u) * 1000000ull;
+
+  if (pl.pair) return launch<256, true>(pl, ta, tb, prm, s);
+  if (pl.bn == 128) return launch<128, false>(pl, ta, tb, prm, s);
+  return launch<256, false>(pl, ta, tb, prm, s);
+}
+
+extern "C" int swz_gemm(const void* A, const void* B, float* C, int M, int N, int K, int order,
+                        int group, int persistent, void* stream) {
+  return swz_gemm_ex(A, B, C, M, N, K, order, group, persistent, nullptr, stream);
+}
+
+extern "C" int swz_check_status(void* stream) {
+  SWZ_CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  unsigned int v = 0;
+  SWZ_CUDA_TRY(cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v)));
+  if (v != 0) {
+    const unsigned int zero = 0;
+    SWZ_CUDA_TRY(cudaMemcpyToSymbol(g_status_word, &zero, sizeof(zero)));
+    return SWZ_ETIMEOUT;
+  }
+  return SWZ_OK;
+}
