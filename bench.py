@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GEMM TFLOP/s & % FP16 tensor peak per swizzle order; L2 hit rate vs model"
 WORKLOAD = dict(M=8192, N=8192, K=8192, dtype="bf16", dist="normal")
-HEADLINE = dict(order="panel", group=16, cta_pair=True, persistent=True)
+HEADLINE = dict(order="panel", group=8, cta_pair=True, persistent=True)
 SWEEP = [("row", 1), ("col", 1), ("panel", 4), ("panel", 8), ("panel", 16),
          ("serpentine", 4), ("serpentine", 8), ("serpentine", 16), ("morton", 1), ("xor", 1)]
 
@@ -43,6 +43,12 @@ SWEEP = [("row", 1), ("col", 1), ("panel", 4), ("panel", 8), ("panel", 16),
 # source whose SHA-256 prefix is recorded with it.
 TRAFFIC = {"bytes": None, "gemm_cu_sha256": None,
            "profile": "profiles/gemm_8192_bf16_pair_ncu.md"}
+
+
+# L2 hit rate (lts__t_sector_hit_rate.pct) of one cold launch per order from
+# an ncu capture of `bench.py --only sweep`; valid for the recorded kernel
+# source only.
+L2_NCU = {"gemm_cu_sha256": None, "profile": "profiles/gemm_8192_bf16_orders_l2.md"}
 
 
 def _gemm_src_hash():
@@ -114,6 +120,25 @@ class ClockSampler:
                 "sm_max_mhz": max(num(r[1]) or 0 for r in self.rows),
                 "power_w_max": max(pw) if pw else None,
                 "reasons": reasons, "samples": len(self.rows)}
+
+
+def spearman(xs, ys):
+    """Rank correlation as the first page's benchmark reports it: ranks are
+    positions after a stable ascending sort (no tie averaging), then the
+    Pearson correlation of the ranks; 0 when a rank vector is constant."""
+    def pos(v):
+        r = [0] * len(v)
+        for p, i in enumerate(sorted(range(len(v)), key=lambda i: v[i])):
+            r[i] = p
+        return r
+    if len(xs) < 2:
+        return 0.0
+    rx, ry = pos(xs), pos(ys)
+    mx, my = statistics.mean(rx), statistics.mean(ry)
+    sxy = sum((a - mx) * (b - my) for a, b in zip(rx, ry))
+    sxx = sum((a - mx) ** 2 for a in rx)
+    syy = sum((b - my) ** 2 for b in ry)
+    return sxy / (sxx * syy) ** 0.5 if sxx and syy else 0.0
 
 
 def _dist():
@@ -192,144 +217,156 @@ def run_swz(args):
     dev = torch.device("cuda", local)
     rc, (sms, l2_bytes, ccmaj, ccmin) = swz.swz_device_info()
     peaks, peak_src = _peaks()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(2 * max(l2_bytes, 64 << 20) // 4, dtype=torch.float32, device=dev)
+    do_gemm = args.only in ("all", "gemm", "sweep")
+    do_transpose = args.only in ("all", "transpose") and not args.no_transpose
 
     M, N, K = WORKLOAD["M"], WORKLOAD["N"], WORKLOAD["K"]
     flops = 2.0 * M * N * K
-    A, B = si.gemm_inputs(M, N, K, WORKLOAD["dtype"], WORKLOAD["dist"], seed=0)
-    Ad, Bd = A.to(dev), B.to(dev)
-    C = torch.empty((M, N), dtype=torch.float32, device=dev)
-    flush = torch.empty(2 * max(l2_bytes, 64 << 20) // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream()
+    line = {"metric": METRIC, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
 
-    def timed_gemm(order, group, steps, warmup, **kw):
+    if do_gemm:
+        A, B = si.gemm_inputs(M, N, K, WORKLOAD["dtype"], WORKLOAD["dist"], seed=0)
+        Ad, Bd = A.to(dev), B.to(dev)
+        C = torch.empty((M, N), dtype=torch.float32, device=dev)
+        _, (_, _, _, _, programs) = swz.swz_gemm_plan(M, N, K, 1, swz.make_opts(cta_pair=True))
+
+    def gemm_once(order, group):
+        swz.gemm(Ad, Bd, order, group, True, out=C, cta_pair=True)
+
+    def timed(fn, steps, warmup):
         for _ in range(warmup):
-            swz.gemm(Ad, Bd, order, group, kw.get("persistent", True), out=C,
-                     cta_pair=kw.get("cta_pair", True))
+            fn()
         torch.cuda.synchronize()
-        ts = []
+        ev = []
         for _ in range(steps):
             flush.fill_(1.0)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            swz.gemm(Ad, Bd, order, group, kw.get("persistent", True), out=C,
-                     cta_pair=kw.get("cta_pair", True))
+            fn()
             e1.record(stream)
-            ts.append((e0, e1))
+            ev.append((e0, e1))
         torch.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in ts]
+        return [a.elapsed_time(b) for a, b in ev]
 
     sampler = ClockSampler(local)
+    ms = None
+    orders = []
     with sampler:
-        # ---- headline: K timed steps ------------------------------------
-        if world > 1:
-            tdist.barrier()
-        torch.cuda.synchronize()
-        ms = timed_gemm(HEADLINE["order"], HEADLINE["group"], args.steps, args.warmup,
-                        cta_pair=HEADLINE["cta_pair"], persistent=HEADLINE["persistent"])
-        torch.cuda.synchronize()
-        if world > 1:
-            tdist.barrier()
+        if args.only in ("all", "gemm"):
+            # ---- headline: K timed steps ------------------------------
+            if world > 1:
+                tdist.barrier()
+            torch.cuda.synchronize()
+            ms = timed(lambda: gemm_once(HEADLINE["order"], HEADLINE["group"]),
+                       args.steps, args.warmup)
+            torch.cuda.synchronize()
+            if world > 1:
+                tdist.barrier()
+        if args.only == "sweep":
+            # one cold (L2-flushed) launch per order, for counter capture
+            for order, g in SWEEP:
+                gemm_once(order, g)
+            torch.cuda.synchronize()
+            for order, g in SWEEP:
+                t = timed(lambda: gemm_once(order, g), 1, 0)
+                orders.append({"order": order, "group": g, "ms": t[0]})
+        elif args.only == "all" and not args.no_sweep:
+            for order, g in SWEEP:
+                t = timed(lambda: gemm_once(order, g), max(5, args.steps // 4), 3)
+                med = statistics.median(t)
+                pred = swz.l2_model_hit_rate(order, g, M, N, K, 128, 256, 64, 2, l2_bytes,
+                                             programs, 2)
+                orders.append({"order": order, "group": g, "ms": med,
+                               "tflops": flops / med / 1e9,
+                               "pct_peak": 100.0 * flops / med / 1e9 / peaks["bf16_tflops"],
+                               "l2_model_hit_pct": pred,
+                               "l2_ncu_hit_pct": L2_NCU.get((order, g))
+                               if L2_NCU.get("gemm_cu_sha256") == _gemm_src_hash() else None})
+    clocks = sampler.summary()
+
+    if ms is not None:
         ms_step = statistics.mean(ms)
         if world > 1:
             t = torch.tensor([ms_step], device=dev)
             tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
             ms_step = t.item()
-        # ---- order sweep ------------------------------------------------
-        orders = []
-        if not args.no_sweep:
-            for order, g in SWEEP:
-                try:
-                    t = timed_gemm(order, g, max(5, args.steps // 4), 3)
-                except swz.SwzError as e:
-                    orders.append({"order": order, "group": g, "error": str(e)})
-                    continue
-                med = statistics.median(t)
-                orders.append({"order": order, "group": g, "ms": med,
-                               "tflops": flops / med / 1e9,
-                               "pct_peak": 100.0 * flops / med / 1e9 / peaks["bf16_tflops"]})
-
-    clocks = sampler.summary()
-    value_dev = world * flops / ms_step / 1e9  # TFLOP/s, all ranks
+        achieved = flops / statistics.mean(ms) / 1e9
+        traffic = TRAFFIC["bytes"] if TRAFFIC["gemm_cu_sha256"] == _gemm_src_hash() else None
+        line.update({
+            "value": world * flops / ms_step / 1e9, "ms_per_step": ms_step,
+            "config": {"workload": "gemm 8192x8192x8192 bf16 N(0,1) -> fp32, 2-CTA clusters "
+                                   "256x256, cluster-persistent",
+                       "order": HEADLINE["order"], "group": HEADLINE["group"],
+                       "programs": programs,
+                       "l2": "flushed before every timed step (write of 2x L2)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "device": {"sms": sms, "l2_bytes": l2_bytes, "cc": f"{ccmaj}.{ccmin}"}},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                         "traffic": traffic, "peak_source": f"bf16 burst, of {peak_src}"},
+            "gpu_launches": args.steps,
+        })
+    line["clocks"] = clocks
+    if orders:
+        line["orders"] = orders
+        good = [o for o in orders if "tflops" in o]
+        if len(good) > 1:
+            line["spearman_l2_model_vs_tflops"] = spearman(
+                [o["l2_model_hit_pct"] for o in good], [o["tflops"] for o in good])
 
     # ---- end to end through the public API from pinned host buffers --------
-    hA, hB = A.pin_memory(), B.pin_memory()
-    hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
-    e2e_ms = []
-    for i in range(3 + 5):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        Ad.copy_(hA, non_blocking=True)
-        Bd.copy_(hB, non_blocking=True)
-        swz.gemm(Ad, Bd, HEADLINE["order"], HEADLINE["group"], True, out=C, cta_pair=True)
-        hC.copy_(C, non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if i >= 3:
-            e2e_ms.append(e0.elapsed_time(e1))
-    e2e = {"value": world * flops / statistics.mean(e2e_ms) / 1e9, "unit": "TFLOP/s",
-           "h2d_bytes_per_step": hA.numel() * 2 + hB.numel() * 2,
-           "d2h_bytes_per_step": hC.numel() * 4}
-    # the result is checked against a few oracle-free invariants only here;
-    # parity lives in the tests
-    assert torch.isfinite(hC[:4]).all()
+    if args.only == "all":
+        hA, hB = A.pin_memory(), B.pin_memory()
+        hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
+        e2e_ms = []
+        for i in range(3 + 5):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            Ad.copy_(hA, non_blocking=True)
+            Bd.copy_(hB, non_blocking=True)
+            gemm_once(HEADLINE["order"], HEADLINE["group"])
+            hC.copy_(C, non_blocking=True)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                e2e_ms.append(e0.elapsed_time(e1))
+        line["e2e"] = {"value": world * flops / statistics.mean(e2e_ms) / 1e9, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": hA.numel() * 2 + hB.numel() * 2,
+                       "d2h_bytes_per_step": hC.numel() * 4}
+        del hA, hB, hC
+    if do_gemm:
+        del A, B, Ad, Bd, C
 
     # ---- transpose (HBM-bound) ---------------------------------------------
-    transpose = {}
-    if not args.no_transpose:
-        del A, B, hA, hB, hC
-        tm, tn = 16384, 32768
-        x = torch.empty((tm, tn), dtype=torch.int32, device=dev).random_()
-        y = torch.empty((tn, tm), dtype=torch.int32, device=dev)
-        for lay in ("naive", "padded", "xor"):
-            for _ in range(3):
-                swz.transpose(x, lay, out=y)
-            ts = []
-            for _ in range(10):
-                flush.fill_(1.0)
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                swz.transpose(x, lay, out=y)
-                e1.record(stream)
-                ts.append((e0, e1))
-            torch.cuda.synchronize()
-            med = statistics.median(a.elapsed_time(b) for a, b in ts)
-            gbs = 2.0 * tm * tn * 4 / med / 1e6
-            transpose[lay] = {"ms": med, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"]}
-        del x, y
+    if do_transpose:
+        tr = {}
+        sizes = [(16384, 32768)] if args.only == "all" else [(1024, 2048), (16384, 32768)]
+        for tm, tn in sizes:
+            x = torch.empty((tm, tn), dtype=torch.int32, device=dev).random_()
+            y = torch.empty((tn, tm), dtype=torch.int32, device=dev)
+            for lay in ("naive", "padded", "xor"):
+                t = timed(lambda: swz.transpose(x, lay, out=y), 10 if args.only == "all" else 1,
+                          3 if args.only == "all" else 1)
+                med = statistics.median(t)
+                gbs = 2.0 * tm * tn * 4 / med / 1e6
+                tr[f"{lay} {tm}x{tn}"] = {"ms": med, "GB/s": gbs,
+                                          "frac_hbm": gbs / peaks["hbm_gbs"]}
+            del x, y
+        line["transpose"] = tr
 
     if rank != 0:
         if world > 1:
             tdist.destroy_process_group()
         return
-
-    achieved = flops / statistics.mean(ms) / 1e9
-    traffic = TRAFFIC["bytes"] if TRAFFIC["gemm_cu_sha256"] == _gemm_src_hash() else None
-    line = {
-        "metric": METRIC, "value": value_dev, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": "gemm 8192x8192x8192 bf16 N(0,1) -> fp32, 2-CTA clusters "
-                               "256x256, cluster-persistent",
-                   "order": HEADLINE["order"], "group": HEADLINE["group"],
-                   "l2": "flushed before every timed step (write of 2x L2)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "device": {"sms": sms, "l2_bytes": l2_bytes, "cc": f"{ccmaj}.{ccmin}"}},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                     "traffic": traffic, "peak_source": f"bf16 burst, of {peak_src}"},
-        "e2e": e2e,
-        "gpu_launches": args.steps,
-        "clocks": clocks,
-        "orders": orders,
-        "transpose": transpose,
-    }
     if world > 1:
         tdist.destroy_process_group()
-    if world == 1 and not args.no_cpu:
+    if world == 1 and not args.no_cpu and args.only == "all":
         line["cpu_baseline"] = cpu_baseline(M, N, K, WORKLOAD["dtype"], WORKLOAD["dist"])
     print(json.dumps(line), flush=True)
 
@@ -343,6 +380,9 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-transpose", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose"], default="all",
+                    help="gemm: headline steps only; sweep: one cold launch per order; "
+                         "transpose: the transposes only (profiling modes)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -152,6 +152,23 @@ int swz_gemm_plan(int M, int N, int K, int persistent,
 int swz_transpose(const uint32_t* in, uint32_t* out, int M, int N, int layout,
                   void* stream);
 
+/*
+ * swz_l2_model -- [TBS] benchmark, offline L2 model (host only, no GPU).
+ * Replays the tile order's operand-tile trace through a byte-budget LRU
+ * cache: the L2 holds whole tiles (A: tile_m x tile_k, B: tile_k x tile_n
+ * elements of elem_bytes), a hit refreshes a tile, a miss inserts it and then
+ * evicts least-recently-used tiles while more than l2_bytes are held and more
+ * than one tile is held.  Program ids run in waves of `concurrency` CTA
+ * tiles; within a wave, for every K step, each tile touches A(m, k) then
+ * B(k, n).  cluster_m > 1 runs the order on cluster tiles of
+ * cluster_m x 1 CTA tiles (the [CPS] Example 2 split), each cluster tile
+ * contributing its CTA tiles in rank order.  Writes the hit and miss counts;
+ * hit rate = hits / (hits + misses).  Errors: SWZ_EINVAL.
+ */
+int swz_l2_model(int order, int group, int M, int N, int K, int tile_m, int tile_n,
+                 int tile_k, int elem_bytes, int64_t l2_bytes, int concurrency,
+                 int cluster_m, int64_t* h_hits, int64_t* h_misses);
+
 /* Synchronises `stream`, then returns and clears the current device's
  * status word: SWZ_OK, or SWZ_ETIMEOUT if a kernel's bounded wait expired
  * since the last check. */

@@ -31,7 +31,7 @@ LAYOUTS = {"naive": SWZ_SMEM_NAIVE, "padded": SWZ_SMEM_PADDED, "xor": SWZ_SMEM_X
 
 EXPORTS = ["swz_tile_map", "swz_is_bijective", "swz_gemm", "swz_gemm_ex", "swz_gemm_plan",
            "swz_transpose", "swz_check_status", "swz_strerror", "swz_last_cuda_error",
-           "swz_device_info"]
+           "swz_device_info", "swz_l2_model"]
 
 
 class SwzError(RuntimeError):
@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
         L.swz_strerror.restype = ctypes.c_char_p
         L.swz_last_cuda_error.argtypes = []
         L.swz_device_info.argtypes = [ip, ip, ip, ip]
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        L.swz_l2_model.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.c_int64, i, i, i64p, i64p]
         for name in EXPORTS:
             if name != "swz_strerror":
                 getattr(L, name).restype = ctypes.c_int
@@ -125,6 +127,23 @@ def swz_device_info():
     v = [ctypes.c_int(0) for _ in range(4)]
     rc = lib().swz_device_info(*[ctypes.byref(x) for x in v])
     return rc, tuple(x.value for x in v)
+
+
+def swz_l2_model(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_bytes,
+                 concurrency, cluster_m=1):
+    h, m = ctypes.c_int64(0), ctypes.c_int64(0)
+    rc = lib().swz_l2_model(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes,
+                            l2_bytes, concurrency, cluster_m, ctypes.byref(h), ctypes.byref(m))
+    return rc, h.value, m.value
+
+
+def l2_model_hit_rate(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_bytes,
+                      concurrency, cluster_m=1):
+    """Predicted L2 hit rate (percent) of the offline tile-trace model."""
+    rc, h, m = swz_l2_model(_order(order), group, M, N, K, tile_m, tile_n, tile_k, elem_bytes,
+                            l2_bytes, concurrency, cluster_m)
+    _check(rc, "swz_l2_model")
+    return 100.0 * h / (h + m) if h + m else 0.0
 
 
 strerror = swz_strerror

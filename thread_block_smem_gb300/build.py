@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 SRC_DIR = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libswz.so")
-SOURCES = ["capi.cu", "transpose.cu", "gemm.cu"]
+SOURCES = ["capi.cu", "transpose.cu", "gemm.cu", "l2_model.cpp"]
 HEADERS = ["common.h", "ptx.cuh", "tile_order.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -54,7 +54,7 @@ def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True) 
         common += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *common, "-c", os.path.join(SRC_DIR, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
