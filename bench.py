@@ -141,6 +141,19 @@ def spearman(xs, ys):
     return sxy / (sxx * syy) ** 0.5 if sxx and syy else 0.0
 
 
+def max_over_ranks(value, device=None):
+    """Max of a float over all ranks of the initialised process group (the
+    identity without one).  Used for the per-step time: the slowest replica
+    sets the job's time."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -290,11 +303,7 @@ def run_swz(args):
     clocks = sampler.summary()
 
     if ms is not None:
-        ms_step = statistics.mean(ms)
-        if world > 1:
-            t = torch.tensor([ms_step], device=dev)
-            tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-            ms_step = t.item()
+        ms_step = max_over_ranks(statistics.mean(ms), dev)
         achieved = flops / statistics.mean(ms) / 1e9
         traffic = TRAFFIC["bytes"] if TRAFFIC["gemm_cu_sha256"] == _gemm_src_hash() else None
         line.update({

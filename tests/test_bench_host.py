@@ -1,0 +1,72 @@
+"""Host-side checks of bench.py: the multi-rank aggregation on two gloo ranks,
+the reference arm's JSON line under a 2-rank launch, and the rank statistic."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+from conftest import ROOT
+
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _worker(rank, world, port, out):
+    import torch.distributed as tdist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    tdist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench.max_over_ranks(1.5 + rank * 2.25)
+        tdist.barrier()
+        out.put((rank, got))
+    finally:
+        tdist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=10) for _ in range(2))
+    assert res == {0: 3.75, 1: 3.75}
+
+
+def test_max_over_ranks_without_group():
+    assert bench.max_over_ranks(2.5) == 2.5
+
+
+def test_spearman_matches_page_convention():
+    assert bench.spearman([1, 2, 3, 4], [4, 3, 2, 1]) == pytest.approx(-1.0)
+    assert bench.spearman([5, 5, 5], [1, 2, 3]) == pytest.approx(1.0)
+    assert bench.spearman([1.0], [2.0]) == 0.0
+
+
+@pytest.mark.slow
+def test_reference_arm_two_ranks_prints_one_line():
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    port = 29600 + os.getpid() % 1000
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                        "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                        "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, env=env, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 1
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0

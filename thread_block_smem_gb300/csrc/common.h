@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/swz.h"
+#include "swz.h"
 
 namespace swz {
 

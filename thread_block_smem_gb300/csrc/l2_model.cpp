@@ -16,7 +16,7 @@
 #include <utility>
 #include <vector>
 
-#include "../../include/swz.h"
+#include "swz.h"
 #include "tile_order.cuh"
 
 namespace {
