@@ -117,6 +117,15 @@ typedef struct swz_gemm_opts {
                         iteration of that program's tile loop}               */
   uint32_t debug_flags; /* SWZ_DEBUG_*; 0 in normal use                      */
   uint32_t timeout_ms;  /* bound of every device wait; 0 = 2000 ms           */
+  int stream_k;      /* persistent only: 1 = share the last, partial wave of
+                        tiles among all programs by splitting those tiles'
+                        K iterations into equal contiguous ranges (Stream-K);
+                        needs d_workspace of swz_gemm_workspace_size bytes   */
+  void* d_workspace; /* device scratch for stream_k: partial accumulators and
+                        per-piece flags.  Zero-fill it once before its first
+                        use; the library keeps it consistent afterwards.
+                        Launches sharing a workspace must not overlap.       */
+  uint64_t workspace_bytes; /* size of d_workspace                           */
 } swz_gemm_opts;
 
 /* debug_flags: withhold the first operand load so that the consumer's
@@ -124,13 +133,24 @@ typedef struct swz_gemm_opts {
  * swz_check_status and exits cleanly (tests of the timeout path only). */
 #define SWZ_DEBUG_SKIP_FIRST_LOAD 1u
 
-/* swz_gemm with explicit tile shape, dtype, 2-CTA mode, program count, trace
- * and wait bound.  opts may be NULL (= swz_gemm).  Extra errors:
- * SWZ_EUNSUPPORTED for tile_n not in {0,128,256} or cta_pair with tile_n
- * != 256. */
+/* swz_gemm with explicit tile shape, dtype, 2-CTA mode, program count, trace,
+ * wait bound and Stream-K tail.  opts may be NULL (= swz_gemm).  Extra
+ * errors: SWZ_EUNSUPPORTED for tile_n not in {0,128,256}, cta_pair with
+ * tile_n != 256, or stream_k with more programs than can be resident at
+ * once (its pieces wait on one another); SWZ_EINVAL for stream_k without
+ * persistent or with a missing, misaligned (256 B) or too small workspace.
+ * In Stream-K mode the trace records, for a split tile, the program that
+ * wrote it. */
 int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N, int K,
                 int order, int group, int persistent,
                 const swz_gemm_opts* opts, void* stream);
+
+/* Bytes of d_workspace a launch with these arguments needs (0 when
+ * stream_k is off, the launch is not persistent or the tiles divide evenly
+ * among the programs).  Needs the device when persistent and num_programs is
+ * 0 (resident capacity). */
+int swz_gemm_workspace_size(int M, int N, int K, int persistent,
+                            const swz_gemm_opts* opts, uint64_t* h_bytes);
 
 /* Grid and launch the GEMM would use, without launching: tiles_m, tiles_n
  * (CTA tiles), sched_m, sched_n (scheduler grid: cluster tiles in 2-CTA mode)

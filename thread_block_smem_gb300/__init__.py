@@ -31,7 +31,7 @@ LAYOUTS = {"naive": SWZ_SMEM_NAIVE, "padded": SWZ_SMEM_PADDED, "xor": SWZ_SMEM_X
 
 EXPORTS = ["swz_tile_map", "swz_is_bijective", "swz_gemm", "swz_gemm_ex", "swz_gemm_plan",
            "swz_transpose", "swz_check_status", "swz_strerror", "swz_last_cuda_error",
-           "swz_device_info", "swz_l2_model"]
+           "swz_device_info", "swz_l2_model", "swz_gemm_workspace_size"]
 
 
 class SwzError(RuntimeError):
@@ -44,7 +44,9 @@ class SwzError(RuntimeError):
 class swz_gemm_opts(ctypes.Structure):
     _fields_ = [("dtype", ctypes.c_int), ("tile_n", ctypes.c_int), ("cta_pair", ctypes.c_int),
                 ("num_programs", ctypes.c_int), ("d_trace", ctypes.c_void_p),
-                ("debug_flags", ctypes.c_uint32), ("timeout_ms", ctypes.c_uint32)]
+                ("debug_flags", ctypes.c_uint32), ("timeout_ms", ctypes.c_uint32),
+                ("stream_k", ctypes.c_int), ("d_workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_uint64)]
 
 
 _lib = None
@@ -73,6 +75,8 @@ def lib() -> ctypes.CDLL:
         L.swz_device_info.argtypes = [ip, ip, ip, ip]
         i64p = ctypes.POINTER(ctypes.c_int64)
         L.swz_l2_model.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.c_int64, i, i, i64p, i64p]
+        L.swz_gemm_workspace_size.argtypes = [i, i, i, i, ctypes.POINTER(swz_gemm_opts),
+                                              ctypes.POINTER(ctypes.c_uint64)]
         for name in EXPORTS:
             if name != "swz_strerror":
                 getattr(L, name).restype = ctypes.c_int
@@ -105,6 +109,14 @@ def swz_gemm_plan(M, N, K, persistent, opts=None):
                              ctypes.byref(opts) if opts is not None else None,
                              *[ctypes.byref(o) for o in out])
     return rc, tuple(o.value for o in out)
+
+
+def swz_gemm_workspace_size(M, N, K, persistent, opts=None):
+    b = ctypes.c_uint64(0)
+    rc = lib().swz_gemm_workspace_size(M, N, K, persistent,
+                                       ctypes.byref(opts) if opts is not None else None,
+                                       ctypes.byref(b))
+    return rc, b.value
 
 
 def swz_transpose(src, dst, M, N, layout, stream=0):
@@ -177,8 +189,12 @@ def tile_map(order, grid_m, grid_n, group=1, device="cuda", stream=None):
 
 
 def make_opts(dtype=SWZ_F16, tile_n=0, cta_pair=False, num_programs=0, trace=None,
-              debug_flags=0, timeout_ms=0):
+              debug_flags=0, timeout_ms=0, stream_k=False, workspace=None):
     o = swz_gemm_opts()
+    o.stream_k = 1 if stream_k else 0
+    if workspace is not None:
+        o.d_workspace = workspace.data_ptr()
+        o.workspace_bytes = workspace.numel() * workspace.element_size()
     o.dtype = dtype
     o.tile_n = tile_n
     o.cta_pair = 1 if cta_pair else 0
@@ -197,11 +213,22 @@ def gemm_plan(M, N, K, persistent=False, tile_n=0, cta_pair=False, num_programs=
     return v
 
 
+def workspace_size(M, N, K, persistent=True, tile_n=0, cta_pair=False, num_programs=0,
+                   stream_k=True):
+    """Bytes of workspace a Stream-K launch of this shape needs (0 if none)."""
+    rc, b = swz_gemm_workspace_size(M, N, K, int(bool(persistent)),
+                                    make_opts(tile_n=tile_n, cta_pair=cta_pair,
+                                              num_programs=num_programs, stream_k=stream_k))
+    _check(rc, "swz_gemm_workspace_size")
+    return b
+
+
 def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
          cta_pair=False, num_programs=0, trace=None, debug_flags=0, timeout_ms=0,
-         stream=None):
+         stream_k=False, workspace=None, stream=None):
     """C = A @ B (fp32) through swz_gemm_ex.  A: M x K, B: K x N, both fp16 or
-    both bf16, row-major contiguous CUDA tensors."""
+    both bf16, row-major contiguous CUDA tensors.  With stream_k, `workspace`
+    is a zero-initialised CUDA tensor of at least workspace_size(...) bytes."""
     import torch
     if A.dtype != B.dtype or A.dtype not in (torch.float16, torch.bfloat16):
         raise TypeError("A and B must both be fp16 or both bf16")
@@ -213,7 +240,7 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
     N = B.shape[1]
     C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=A.device)
     opts = make_opts(SWZ_BF16 if A.dtype == torch.bfloat16 else SWZ_F16, tile_n, cta_pair,
-                     num_programs, trace, debug_flags, timeout_ms)
+                     num_programs, trace, debug_flags, timeout_ms, stream_k, workspace)
     _check(swz_gemm_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _order(order),
                        group, int(bool(persistent)), opts, _stream(stream)), "swz_gemm_ex")
     return C

@@ -28,6 +28,7 @@
 //   * Every wait is bounded (globaltimer); on expiry the kernel records
 //     SWZ_ETIMEOUT in a device status word, drains what it issued, frees TMEM
 //     and returns.
+#include <atomic>
 #include <mutex>
 
 #include "common.h"
@@ -92,6 +93,70 @@ struct Params {
   int32_t* trace;
   uint32_t debug_flags;
   uint64_t timeout_ns;
+  // Stream-K tail (persistent launches only; 0 = whole tiles everywhere)
+  uint32_t stream_k;
+  uint32_t epoch;      // value a finished partial's flag takes in this launch
+  uint32_t* sk_flags;  // [cluster][rank][lane quarter]
+  float4* sk_ws;       // [cluster][rank][BN/4 column groups][128 rows] float4
+};
+
+enum ItemKind : int { kWhole = 0, kFirst = 1, kPartial = 2 };
+
+// The work of one cluster.  Scheduler units (output tiles, cluster tiles in a
+// pair) are the tile order applied to work index w; whole tiles are dealt out
+// statically, w = cluster, cluster + P, ... (the persistent loop of the first
+// page, work_idx striding of the cluster scheduler).  With stream_k, only the
+// first floor(U/P)*P units go out whole; the K iterations of the R = U mod P
+// tail units are laid end to end (R*kb iterations) and split into P
+// contiguous ranges, one per cluster, so the last wave is shared by every
+// cluster instead of running on R of them.  A range is shorter than one tile
+// (R < P), so it holds at most two pieces: a piece that starts inside a tile
+// (a partial, written to the workspace) and a piece that starts a tile (its
+// first piece: the cluster owning it adds the other pieces and writes C).
+struct Schedule {
+  uint32_t c, P, U, kb;
+  uint32_t dp_end;  // units below this are whole tiles
+  uint32_t n_dp;    // whole tiles of this cluster
+  uint64_t I;       // tail iterations
+  uint64_t s, e;    // this cluster's tail range [s, e)
+
+  __device__ __forceinline__ void init(uint32_t c_, uint32_t P_, uint32_t U_, uint32_t kb_,
+                                       bool sk) {
+    c = c_;
+    P = P_;
+    U = U_;
+    kb = kb_;
+    const uint32_t R = sk ? U % P : 0u;
+    dp_end = U - R;
+    n_dp = c < dp_end ? (dp_end - c + P - 1) / P : 0u;
+    I = uint64_t(R) * kb;
+    s = range_start(c);
+    e = range_start(c + 1);
+  }
+  __device__ __forceinline__ uint64_t range_start(uint32_t cc) const { return I * cc / P; }
+  // The i-th piece of work: unit, K-block range [k0, k1), kind.
+  __device__ __forceinline__ bool item(uint32_t i, uint32_t& unit, uint32_t& k0, uint32_t& k1,
+                                       int& kind) const {
+    if (i < n_dp) {
+      unit = c + i * P;
+      k0 = 0;
+      k1 = kb;
+      kind = kWhole;
+      return true;
+    }
+    i -= n_dp;
+    if (s >= e) return false;
+    const uint64_t t = s / kb + i;
+    const uint64_t t0 = t * kb;
+    if (t0 >= e) return false;
+    const uint32_t a = s > t0 ? uint32_t(s - t0) : 0u;
+    const uint32_t b = e < t0 + kb ? uint32_t(e - t0) : kb;
+    unit = dp_end + uint32_t(t);
+    k0 = a;
+    k1 = b;
+    kind = a > 0 ? kPartial : (b == kb ? kWhole : kFirst);
+    return true;
+  }
 };
 
 struct Ctl {
@@ -120,6 +185,23 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Ctl& c
         raise_abort(c);
         return false;
       }
+    }
+  }
+}
+
+// Waits until the 32-bit flag at `flag` (global) equals `value`, with the
+// same bound and abort rules as wait().
+__device__ __noinline__ bool wait_flag(const uint32_t* flag, uint32_t value, const Ctl& c) {
+  const uint64_t t0 = ptx::global_timer_ns();
+  for (uint32_t n = 0;; ++n) {
+    if (ptx::ld_acquire_gpu(flag) == value) return true;
+    if ((n & 15u) == 15u) {
+      if (*c.abort_flag) return false;
+      if (ptx::global_timer_ns() - t0 > c.timeout_ns) {
+        raise_abort(c);
+        return false;
+      }
+      __nanosleep(64);
     }
   }
 }
@@ -188,7 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   ctl.pair = PAIR;
 
   const uint32_t units = p.sched_m * p.sched_n;
-  const uint32_t first = blockIdx.x / CL, stride = gridDim.x / CL;
+  Schedule sch;
+  sch.init(blockIdx.x / CL, gridDim.x / CL, units, p.num_kb, p.stream_k != 0);
   bool aborted = false;
 
   if (warp == 0) {
@@ -196,11 +279,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool skip = (p.debug_flags & SWZ_DEBUG_SKIP_FIRST_LOAD) != 0;
-      for (uint32_t w = first; w < units && !aborted; w += stride) {
+      uint32_t w, kbeg, kend;
+      int kind;
+      for (uint32_t i = 0; !aborted && sch.item(i, w, kbeg, kend, kind); ++i) {
         const TileCoord t = tile_of(p.order, w, p.sched_m, p.sched_n, uint32_t(p.group));
         const int32_t m0 = int32_t((t.m * CL + rank) * BM);
         const int32_t n0 = int32_t(t.n * BN + rank * K_::BN_LOCAL);
-        for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+        for (uint32_t kb = kbeg; kb < kend; ++kb) {
           if (!wait(empty_bar(stage), phase ^ 1u, ctl)) { aborted = true; break; }
           if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), K_::TX_BYTES);
           if (skip) {
@@ -240,11 +325,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && leader) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued = false;
-      for (uint32_t w = first; w < units && !aborted; w += stride) {
+      uint32_t w, kbeg, kend;
+      int kind;
+      for (uint32_t i = 0; !aborted && sch.item(i, w, kbeg, kend, kind); ++i) {
         if (!wait(tempty_bar(acc), acc_phase ^ 1u, ctl)) { aborted = true; break; }
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
-        for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+        for (uint32_t kb = kbeg; kb < kend; ++kb) {
           if (!wait(full_bar(stage), phase, ctl)) { aborted = true; break; }
           ptx::tc_fence_after();
           const uint32_t a_addr = sA + stage * K_::A_BYTES;
@@ -257,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // B: N-major; 16 K rows of 128 bytes further; 8-row groups
             // 1024 bytes apart along K, 64-column boxes B_BOX_BYTES apart.
             const uint64_t bdesc = make_sdesc(b_addr + kk * 2048, K_::B_BOX_BYTES, 1024);
-            ptx::mma_f16<CL>(d, adesc, bdesc, p.idesc, (kb | uint32_t(kk)) != 0u);
+            ptx::mma_f16<CL>(d, adesc, bdesc, p.idesc, (kb != kbeg || kk != 0) ? 1u : 0u);
           }
           issued = true;
           if constexpr (PAIR) ptx::mma_commit_pair(empty_bar(stage), 0x3);
@@ -282,46 +369,113 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------- epilogue: TMEM -> registers -> C ----------------
-    const uint32_t q = warp & 3u;  // TMEM lane quarter this warp may access
-    uint32_t acc = 0, acc_phase = 0, it = 0;
-    for (uint32_t w = first; w < units; w += stride, ++it) {
+    // Warp w owns TMEM lanes (rows) 32*(w%4) .. +31.  A partial piece goes to
+    // this cluster's workspace slot and is published per warp with a release
+    // flag; the owner of the tile's first piece waits, warp by warp, for the
+    // matching warps of the later pieces and adds them in K order.
+    const uint32_t q = warp & 3u;
+    const uint32_t row_local = q * 32u + lane;
+    uint32_t acc = 0, acc_phase = 0;
+    uint32_t w, kbeg, kend;
+    int kind;
+    for (uint32_t i = 0; sch.item(i, w, kbeg, kend, kind); ++i) {
       const bool ok = wait(tfull_bar(acc), acc_phase, ctl);
       if (!__all_sync(0xFFFFFFFFu, ok)) { aborted = true; break; }
       ptx::tc_fence_after();
       const TileCoord t = tile_of(p.order, w, p.sched_m, p.sched_n, uint32_t(p.group));
       const uint32_t cta_m = t.m * CL + rank, cta_n = t.n;
-      const int64_t row = int64_t(cta_m) * BM + q * 32 + lane;
-      const int32_t col0 = int32_t(cta_n) * BN;
-      float* crow = p.C + row * p.N + col0;
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + acc * BN;
+      if (kind == kPartial) {
+        float4* slot = p.sk_ws + size_t(sch.c * CL + rank) * (BN / 4) * BM;
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t r[32];
-        ptx::tmem_ld_32x32b_x32(taddr + c, r);
-        ptx::tmem_ld_wait();
-        if (row < p.M) {
-          if (col0 + c + 32 <= p.N) {
-            float4* dst = reinterpret_cast<float4*>(crow + c);
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c, r);
+          ptx::tmem_ld_wait();
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-          } else {
+          for (int v = 0; v < 8; ++v)
+            __stcg(slot + size_t(c / 4 + v) * BM + row_local,
+                   make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                               __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+        }
+        ptx::tc_fence_before();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
+          else ptx::mbar_arrive(tempty_bar(acc));
+          ptx::st_release_gpu(p.sk_flags + (sch.c * CL + rank) * 4u + q, p.epoch);
+        }
+      } else {
+        // owner of a tile's first piece: the later pieces come from clusters
+        // c+1, c+2, ... whose (non-empty) ranges start inside this tile
+        const uint64_t tile_end =
+            kind == kFirst ? uint64_t(w - sch.dp_end + 1) * sch.kb : uint64_t(0);
+        if (kind == kFirst) {
+          bool got = true;
+          if (lane == 0) {
+            for (uint32_t cc = sch.c + 1; cc < sch.P; ++cc) {
+              const uint64_t sc = sch.range_start(cc);
+              if (sc >= tile_end) break;
+              if (sc >= sch.range_start(cc + 1)) continue;  // empty range
+              if (!wait_flag(p.sk_flags + (cc * CL + rank) * 4u + q, p.epoch, ctl)) {
+                got = false;
+                break;
+              }
+            }
+          }
+          got = __shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) != 0;
+          if (!got) { aborted = true; break; }
+          __threadfence();
+        }
+        const int64_t row = int64_t(cta_m) * BM + row_local;
+        const int32_t col0 = int32_t(cta_n) * BN;
+        float* crow = p.C + row * p.N + col0;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c, r);
+          ptx::tmem_ld_wait();
+          float f[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col0 + c + j < p.N) crow[c + j] = __uint_as_float(r[j]);
+          for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
+          for (uint32_t cc = sch.c + 1; kind == kFirst && cc < sch.P; ++cc) {
+            const uint64_t sc = sch.range_start(cc);
+            if (sc >= tile_end) break;
+            if (sc >= sch.range_start(cc + 1)) continue;
+            const float4* slot = p.sk_ws + size_t(cc * CL + rank) * (BN / 4) * BM;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const float4 x = __ldcg(slot + size_t(c / 4 + v) * BM + row_local);
+              f[4 * v] += x.x;
+              f[4 * v + 1] += x.y;
+              f[4 * v + 2] += x.z;
+              f[4 * v + 3] += x.w;
+            }
+          }
+          if (row < p.M) {
+            if (col0 + c + 32 <= p.N) {
+              float4* dst = reinterpret_cast<float4*>(crow + c);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[v] = make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + c + j < p.N) crow[c + j] = f[j];
+            }
           }
         }
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
-        else ptx::mbar_arrive(tempty_bar(acc));
-        if (warp == 2 && p.trace) {
-          const uint64_t idx = uint64_t(cta_m) * p.sched_n + cta_n;
-          p.trace[2 * idx] = int32_t(blockIdx.x);
-          p.trace[2 * idx + 1] = int32_t(it);
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
+          else ptx::mbar_arrive(tempty_bar(acc));
+          if (warp == 2 && p.trace) {
+            const uint64_t idx = uint64_t(cta_m) * p.sched_n + cta_n;
+            p.trace[2 * idx] = int32_t(blockIdx.x);
+            p.trace[2 * idx + 1] = int32_t(i);
+          }
         }
       }
       acc ^= 1u;
@@ -466,6 +620,24 @@ static int make_plan(int M, int N, int persistent, const swz_gemm_opts& o, const
   return SWZ_OK;
 }
 
+// Stream-K workspace: flags [clusters][CL][4] uint32 (256-byte aligned
+// block), then partial accumulators [clusters][CL][BN/4][128] float4.
+struct SkLayout {
+  bool active;
+  uint64_t flags_bytes, data_bytes;
+};
+
+static SkLayout sk_layout(const Plan& pl, int persistent, const swz_gemm_opts& o) {
+  SkLayout L{false, 0, 0};
+  const uint32_t cl = pl.pair ? 2u : 1u;
+  const uint32_t clusters = uint32_t(pl.programs) / cl;
+  if (!o.stream_k || !persistent || clusters == 0 || pl.units % clusters == 0) return L;
+  L.active = true;
+  L.flags_bytes = (uint64_t(clusters) * cl * 4u * 4u + 255u) & ~uint64_t(255);
+  L.data_bytes = uint64_t(clusters) * cl * BM * uint64_t(pl.bn) * 4u;
+  return L;
+}
+
 template <int BN, bool PAIR>
 static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm,
                   cudaStream_t stream) {
@@ -544,6 +716,27 @@ extern "C" int swz_gemm_plan(int M, int N, int K, int persistent, const swz_gemm
   return SWZ_OK;
 }
 
+extern "C" int swz_gemm_workspace_size(int M, int N, int K, int persistent,
+                                       const swz_gemm_opts* opts, uint64_t* bytes) {
+  swz_gemm_opts o = {};
+  if (opts) o = *opts;
+  if (!bytes || M < 0 || N < 0 || K < 0) return SWZ_EINVAL;
+  *bytes = 0;
+  if (M == 0 || N == 0 || K == 0 || !o.stream_k || !persistent) return SWZ_OK;
+  DeviceInfo dev{};
+  const bool need_dev = o.num_programs == 0;
+  if (need_dev) {
+    const int rc = current_device(&dev);
+    if (rc != SWZ_OK) return rc;
+  }
+  Plan pl{};
+  const int rc = make_plan(M, N, persistent, o, need_dev ? &dev : nullptr, &pl);
+  if (rc != SWZ_OK) return rc;
+  const SkLayout L = sk_layout(pl, persistent, o);
+  *bytes = L.active ? L.flags_bytes + L.data_bytes : 0;
+  return SWZ_OK;
+}
+
 extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N, int K, int order,
                            int group, int persistent, const swz_gemm_opts* opts, void* stream) {
   swz_gemm_opts o = {};
@@ -587,6 +780,28 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   prm.trace = o.d_trace;
   prm.debug_flags = o.debug_flags;
   prm.timeout_ns = uint64_t(o.timeout_ms ? o.timeout_ms : 2000u) * 1000000ull;
+
+  if (o.stream_k) {
+    if (!persistent) return SWZ_EINVAL;
+    const SkLayout L = sk_layout(pl, persistent, o);
+    if (L.active) {
+      // pieces of one tile wait on one another: every program must be resident
+      int cap = 0;
+      rc = capacity_for(pl, dev, &cap);
+      if (rc != SWZ_OK) return rc;
+      if (pl.programs > cap) return SWZ_EUNSUPPORTED;
+      const uintptr_t ws = reinterpret_cast<uintptr_t>(o.d_workspace);
+      if (!ws || (ws & 255u) || o.workspace_bytes < L.flags_bytes + L.data_bytes)
+        return SWZ_EINVAL;
+      static std::atomic<uint32_t> epoch{0};
+      uint32_t e = epoch.fetch_add(1) + 1;
+      if (e == 0) e = epoch.fetch_add(1) + 1;
+      prm.stream_k = 1;
+      prm.epoch = e;
+      prm.sk_flags = reinterpret_cast<uint32_t*>(ws);
+      prm.sk_ws = reinterpret_cast<float4*>(ws + L.flags_bytes);
+    }
+  }
 
   if (pl.pair) return launch<256, true>(pl, ta, tb, prm, s);
   if (pl.bn == 128) return launch<128, false>(pl, ta, tb, prm, s);
