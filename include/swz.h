@@ -45,7 +45,9 @@ enum swz_status {
   SWZ_EARCH = -3,          /* current device is not sm_103 (GB300)            */
   SWZ_ECUDA = -4,          /* a CUDA runtime call failed: swz_last_cuda_error */
   SWZ_ETIMEOUT = -5,       /* a bounded device wait expired (swz_check_status)*/
-  SWZ_EUNSUPPORTED = -6    /* valid arguments, configuration not provided     */
+  SWZ_EUNSUPPORTED = -6,   /* valid arguments, configuration not provided     */
+  SWZ_ESCRATCH = -7        /* launch needs more than the library's built-in
+                              scratch area (swz_gemm_streamk_noalloc)        */
 };
 
 /* ---- tile orders ([TBS] mode ids 0..4; 5 added for [CPS] serpentine) ----- */
@@ -188,6 +190,45 @@ int swz_transpose(const uint32_t* in, uint32_t* out, int M, int N, int layout,
 int swz_l2_model(int order, int group, int M, int N, int K, int tile_m, int tile_n,
                  int tile_k, int elem_bytes, int64_t l2_bytes, int concurrency,
                  int cluster_m, int64_t* h_hits, int64_t* h_misses);
+
+/*
+ * swz_gemm_streamk_noalloc -- Stream-K GEMM for callers that cannot allocate
+ * device memory.  No source page has a counterpart; this is a library
+ * convenience.
+ *
+ * Who needs it: callers that are handed only their input and output buffers
+ * and have no way to get device scratch -- plugin hosts that own every
+ * allocation, services running under a fixed memory budget whose allocator
+ * belongs to someone else, and loops that must not call cudaMalloc because
+ * it synchronises the device.  swz_gemm_ex with stream_k needs a
+ * caller-provided workspace; this entry point instead uses a scratch area
+ * built into the library: a statically sized device array of
+ * SWZ_NOALLOC_SCRATCH_BYTES (24 MiB) that every GPU which loads the library
+ * holds until the process exits.
+ *
+ * Computes exactly what swz_gemm_ex computes with persistent = 1, stream_k =
+ * 1 and the same opts (dtype, tile_n, cta_pair, num_programs, d_trace,
+ * timeout_ms; opts->stream_k, d_workspace and workspace_bytes are ignored;
+ * opts may be NULL).  A, B, C as in swz_gemm.
+ *
+ * Set-up: the first call on each device looks up the device address of the
+ * scratch area (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  The call allocates and frees
+ * nothing.  It clears the part of the scratch area that must start at zero
+ * (the per-piece flags) on `stream` before the launch.
+ *
+ * All calls on a device share the one scratch area, which keeps the last
+ * call's contents: calls whose work overlaps on the GPU (different streams,
+ * or host threads racing on one device) race on it and must be serialised
+ * by the caller.
+ *
+ * Errors: as swz_gemm_ex, plus SWZ_ESCRATCH when the launch needs more than
+ * SWZ_NOALLOC_SCRATCH_BYTES of scratch (see swz_gemm_workspace_size).
+ */
+#define SWZ_NOALLOC_SCRATCH_BYTES (24u * 1024u * 1024u)
+int swz_gemm_streamk_noalloc(const void* A, const void* B, float* C, int M, int N, int K,
+                             int order, int group, const swz_gemm_opts* opts,
+                             void* stream);
 
 /* Synchronises `stream`, then returns and clears the current device's
  * status word: SWZ_OK, or SWZ_ETIMEOUT if a kernel's bounded wait expired

@@ -21,6 +21,8 @@ LIB_PATH = os.path.join(_HERE, "_build", "libswz.so")
 # status codes and enums (include/swz.h)
 SWZ_OK, SWZ_EINVAL, SWZ_ENOTBIJECTIVE, SWZ_EARCH, SWZ_ECUDA, SWZ_ETIMEOUT, SWZ_EUNSUPPORTED = (
     0, -1, -2, -3, -4, -5, -6)
+SWZ_ESCRATCH = -7
+SWZ_NOALLOC_SCRATCH_BYTES = 24 * 1024 * 1024
 SWZ_ROW, SWZ_COL, SWZ_PANEL, SWZ_MORTON, SWZ_XOR, SWZ_SERPENTINE = range(6)
 SWZ_F16, SWZ_BF16 = 0, 1
 SWZ_SMEM_NAIVE, SWZ_SMEM_PADDED, SWZ_SMEM_XOR = 0, 1, 2
@@ -31,7 +33,8 @@ LAYOUTS = {"naive": SWZ_SMEM_NAIVE, "padded": SWZ_SMEM_PADDED, "xor": SWZ_SMEM_X
 
 EXPORTS = ["swz_tile_map", "swz_is_bijective", "swz_gemm", "swz_gemm_ex", "swz_gemm_plan",
            "swz_transpose", "swz_check_status", "swz_strerror", "swz_last_cuda_error",
-           "swz_device_info", "swz_l2_model", "swz_gemm_workspace_size"]
+           "swz_device_info", "swz_l2_model", "swz_gemm_workspace_size",
+           "swz_gemm_streamk_noalloc"]
 
 
 class SwzError(RuntimeError):
@@ -77,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.swz_l2_model.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.c_int64, i, i, i64p, i64p]
         L.swz_gemm_workspace_size.argtypes = [i, i, i, i, ctypes.POINTER(swz_gemm_opts),
                                               ctypes.POINTER(ctypes.c_uint64)]
+        L.swz_gemm_streamk_noalloc.argtypes = [vp, vp, vp, i, i, i, i, i,
+                                               ctypes.POINTER(swz_gemm_opts), vp]
         for name in EXPORTS:
             if name != "swz_strerror":
                 getattr(L, name).restype = ctypes.c_int
@@ -117,6 +122,14 @@ def swz_gemm_workspace_size(M, N, K, persistent, opts=None):
                                        ctypes.byref(opts) if opts is not None else None,
                                        ctypes.byref(b))
     return rc, b.value
+
+
+def swz_gemm_streamk_noalloc(A, B, C, M, N, K, order, group, opts=None, stream=0):
+    """Stream-K GEMM without a caller workspace (the library's built-in
+    scratch area; see include/swz.h for who needs it and its limits)."""
+    return lib().swz_gemm_streamk_noalloc(A, B, C, M, N, K, order, group,
+                                          ctypes.byref(opts) if opts is not None else None,
+                                          stream)
 
 
 def swz_transpose(src, dst, M, N, layout, stream=0):

@@ -84,6 +84,7 @@ extern "C" const char* swz_strerror(int status) {
     case SWZ_ECUDA: return "CUDA runtime call failed (see swz_last_cuda_error)";
     case SWZ_ETIMEOUT: return "a bounded device wait expired";
     case SWZ_EUNSUPPORTED: return "configuration not supported";
+    case SWZ_ESCRATCH: return "launch needs more scratch than the built-in scratch area holds";
     default: return "unknown status";
   }
 }

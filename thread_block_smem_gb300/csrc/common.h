@@ -38,6 +38,11 @@ int current_device(DeviceInfo* info, bool require_sm103 = true);
 // (host-side exhaustive check over all ids).
 bool order_is_bijective(int order, uint32_t gm, uint32_t gn, uint32_t group);
 
+// Stream-K workspace split of a launch: bytes of the flag block at the front
+// and total bytes (both 0 when the launch needs no workspace).
+int gemm_sk_workspace_split(int M, int N, int K, int persistent, const swz_gemm_opts& o,
+                            uint64_t* flag_bytes, uint64_t* total_bytes);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 

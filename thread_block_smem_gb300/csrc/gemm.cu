@@ -716,6 +716,29 @@ extern "C" int swz_gemm_plan(int M, int N, int K, int persistent, const swz_gemm
   return SWZ_OK;
 }
 
+namespace swz {
+int gemm_sk_workspace_split(int M, int N, int K, int persistent, const swz_gemm_opts& o,
+                            uint64_t* flag_bytes, uint64_t* total_bytes) {
+  *flag_bytes = *total_bytes = 0;
+  if (M <= 0 || N <= 0 || K <= 0 || !o.stream_k || !persistent) return SWZ_OK;
+  DeviceInfo dev{};
+  const bool need_dev = o.num_programs == 0;
+  if (need_dev) {
+    const int rc = current_device(&dev);
+    if (rc != SWZ_OK) return rc;
+  }
+  Plan pl{};
+  const int rc = make_plan(M, N, persistent, o, need_dev ? &dev : nullptr, &pl);
+  if (rc != SWZ_OK) return rc;
+  const SkLayout L = sk_layout(pl, persistent, o);
+  if (L.active) {
+    *flag_bytes = L.flags_bytes;
+    *total_bytes = L.flags_bytes + L.data_bytes;
+  }
+  return SWZ_OK;
+}
+}  // namespace swz
+
 extern "C" int swz_gemm_workspace_size(int M, int N, int K, int persistent,
                                        const swz_gemm_opts* opts, uint64_t* bytes) {
   swz_gemm_opts o = {};
