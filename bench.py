@@ -33,8 +33,21 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GEMM TFLOP/s & % FP16 tensor peak per swizzle order; L2 hit rate vs model"
-WORKLOAD = dict(M=8192, N=8192, K=8192, dtype="bf16", dist="normal")
-HEADLINE = dict(order="panel", group=8, cta_pair=True, persistent=True)
+# The configurations of the specification.  The default (timed headline) is
+# the 8192^3 bf16 CTA-pair one; the others are selectable with --workload.
+WORKLOADS = {
+    "gemm8192_bf16_pair": dict(M=8192, N=8192, K=8192, dtype="bf16", dist="normal",
+                               cfg=dict(cta_pair=True), tile=(128, 256), cluster_m=2),
+    "gemm4096_fp16": dict(M=4096, N=4096, K=4096, dtype="fp16", dist="uniform",
+                          cfg=dict(tile_n=256), tile=(128, 256), cluster_m=1),
+    "gemm4096_fp16_pair": dict(M=4096, N=4096, K=4096, dtype="fp16", dist="uniform",
+                               cfg=dict(cta_pair=True), tile=(128, 256), cluster_m=2),
+    "gemm6144x10240x4096_fp16": dict(M=6144, N=10240, K=4096, dtype="fp16", dist="uniform",
+                                     cfg=dict(tile_n=128), tile=(128, 128), cluster_m=1),
+    "gemm1024x1024x512_fp16": dict(M=1024, N=1024, K=512, dtype="fp16", dist="uniform",
+                                   cfg=dict(tile_n=128), tile=(128, 128), cluster_m=1),
+}
+HEADLINE = dict(order="panel", group=8, persistent=True)
 SWEEP = [("row", 1), ("col", 1), ("panel", 4), ("panel", 8), ("panel", 16),
          ("serpentine", 4), ("serpentine", 8), ("serpentine", 16), ("morton", 1), ("xor", 1)]
 
@@ -186,10 +199,11 @@ def run_reference(args):
     rank, world, _ = _dist()
     if rank != 0:
         return
-    M, N, K = WORKLOAD["M"], WORKLOAD["N"], WORKLOAD["K"]
+    wl = WORKLOADS[args.workload]
+    M, N, K = wl["M"], wl["N"], wl["K"]
     import synth_inputs as si
     from oracle import ref
-    A, B = si.gemm_inputs(M, N, K, WORKLOAD["dtype"], WORKLOAD["dist"], seed=0)
+    A, B = si.gemm_inputs(M, N, K, wl["dtype"], wl["dist"], seed=0)
     a64, b64 = A.double(), B.double()
     rows = 8  # one step = an 8-row slab of C (about a second of host work)
     for _ in range(args.warmup):
@@ -205,7 +219,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "gemm 8192x8192x8192 bf16 N(0,1) -> fp32",
+            "config": {"workload": f"{args.workload}: gemm {M}x{N}x{K} {wl['dtype']} -> fp32",
                        "note": "CPU oracle, FP64; each step computes 8 rows of C"},
             "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": ref.num_threads(),
                              "kind": "oracle", "sample": f"{rows} rows of C per step"},
@@ -235,20 +249,31 @@ def run_swz(args):
     do_gemm = args.only in ("all", "gemm", "sweep")
     do_transpose = args.only in ("all", "transpose") and not args.no_transpose
 
-    M, N, K = WORKLOAD["M"], WORKLOAD["N"], WORKLOAD["K"]
+    wl = WORKLOADS[args.workload]
+    M, N, K = wl["M"], wl["N"], wl["K"]
+    cfg = dict(wl["cfg"])
+    persistent = not args.non_persistent
     flops = 2.0 * M * N * K
     line = {"metric": METRIC, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
+            "vs_baseline": None, "dtype": wl["dtype"], "data": "synthetic"}
+    head_order = args.order or HEADLINE["order"]
+    head_group = args.group or HEADLINE["group"]
 
     if do_gemm:
-        A, B = si.gemm_inputs(M, N, K, WORKLOAD["dtype"], WORKLOAD["dist"], seed=0)
+        A, B = si.gemm_inputs(M, N, K, wl["dtype"], wl["dist"], seed=0)
         Ad, Bd = A.to(dev), B.to(dev)
         C = torch.empty((M, N), dtype=torch.float32, device=dev)
-        _, (_, _, _, _, programs) = swz.swz_gemm_plan(M, N, K, 1, swz.make_opts(cta_pair=True))
+        _, (_, _, _, _, programs) = swz.swz_gemm_plan(M, N, K, int(persistent),
+                                                      swz.make_opts(**cfg))
+        ws = None
+        if args.stream_k:
+            nws = swz.workspace_size(M, N, K, persistent, **cfg)
+            ws = torch.zeros(max(nws, 256), dtype=torch.uint8, device=dev)
 
     def gemm_once(order, group):
-        swz.gemm(Ad, Bd, order, group, True, out=C, cta_pair=True)
+        swz.gemm(Ad, Bd, order, group, persistent, out=C, stream_k=args.stream_k,
+                 workspace=ws, **cfg)
 
     def timed(fn, steps, warmup):
         for _ in range(warmup):
@@ -275,8 +300,7 @@ def run_swz(args):
             if world > 1:
                 tdist.barrier()
             torch.cuda.synchronize()
-            ms = timed(lambda: gemm_once(HEADLINE["order"], HEADLINE["group"]),
-                       args.steps, args.warmup)
+            ms = timed(lambda: gemm_once(head_order, head_group), args.steps, args.warmup)
             torch.cuda.synchronize()
             if world > 1:
                 tdist.barrier()
@@ -292,8 +316,8 @@ def run_swz(args):
             for order, g in SWEEP:
                 t = timed(lambda: gemm_once(order, g), max(5, args.steps // 4), 3)
                 med = statistics.median(t)
-                pred = swz.l2_model_hit_rate(order, g, M, N, K, 128, 256, 64, 2, l2_bytes,
-                                             programs, 2)
+                pred = swz.l2_model_hit_rate(order, g, M, N, K, wl["tile"][0], wl["tile"][1], 64,
+                                             2, l2_bytes, programs, wl["cluster_m"])
                 orders.append({"order": order, "group": g, "ms": med,
                                "tflops": flops / med / 1e9,
                                "pct_peak": 100.0 * flops / med / 1e9 / peaks["bf16_tflops"],
@@ -308,9 +332,13 @@ def run_swz(args):
         traffic = TRAFFIC["bytes"] if TRAFFIC["gemm_cu_sha256"] == _gemm_src_hash() else None
         line.update({
             "value": world * flops / ms_step / 1e9, "ms_per_step": ms_step,
-            "config": {"workload": "gemm 8192x8192x8192 bf16 N(0,1) -> fp32, 2-CTA clusters "
-                                   "256x256, cluster-persistent",
-                       "order": HEADLINE["order"], "group": HEADLINE["group"],
+            "config": {"workload": f"{args.workload}: gemm {M}x{N}x{K} {wl['dtype']} "
+                                   f"{'N(0,1)' if wl['dist'] == 'normal' else 'U[-1,1)'} -> fp32, "
+                                   + ("2-CTA clusters 256x256" if cfg.get("cta_pair") else
+                                      f"1-CTA tiles 128x{cfg.get('tile_n')}")
+                                   + (", persistent" if persistent else ", one CTA per tile")
+                                   + (", Stream-K tail" if args.stream_k else ""),
+                       "order": head_order, "group": head_group,
                        "programs": programs,
                        "l2": "flushed before every timed step (write of 2x L2)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -339,7 +367,7 @@ def run_swz(args):
             e0.record(stream)
             Ad.copy_(hA, non_blocking=True)
             Bd.copy_(hB, non_blocking=True)
-            gemm_once(HEADLINE["order"], HEADLINE["group"])
+            gemm_once(head_order, head_group)
             hC.copy_(C, non_blocking=True)
             e1.record(stream)
             torch.cuda.synchronize()
@@ -376,7 +404,7 @@ def run_swz(args):
     if world > 1:
         tdist.destroy_process_group()
     if world == 1 and not args.no_cpu and args.only == "all":
-        line["cpu_baseline"] = cpu_baseline(M, N, K, WORKLOAD["dtype"], WORKLOAD["dist"])
+        line["cpu_baseline"] = cpu_baseline(M, N, K, wl["dtype"], wl["dist"])
     print(json.dumps(line), flush=True)
 
 
@@ -389,6 +417,12 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-transpose", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gemm8192_bf16_pair")
+    ap.add_argument("--order", choices=["row", "col", "panel", "morton", "xor", "serpentine"],
+                    default=None, help="headline tile order (default panel)")
+    ap.add_argument("--group", type=int, default=None, help="G or S of the headline order")
+    ap.add_argument("--stream-k", action="store_true", help="Stream-K tail (persistent only)")
+    ap.add_argument("--non-persistent", action="store_true", help="one CTA (pair) per tile")
     ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose"], default="all",
                     help="gemm: headline steps only; sweep: one cold launch per order; "
                          "transpose: the transposes only (profiling modes)")

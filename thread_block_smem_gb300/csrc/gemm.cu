@@ -59,8 +59,12 @@ struct Cfg {
   static constexpr int TMEM_COLS = 2 * BN;
   static constexpr int UMMA_M = PAIR ? 256 : 128;
   static constexpr uint32_t TX_BYTES = uint32_t(CG) * STAGE_BYTES;
+  // epilogue staging: per epilogue warp two 32 x 32 fp32 boxes (128-byte
+  // rows, 128-byte swizzle), written from registers and stored by TMA
+  static constexpr int STG_BOX_BYTES = 32 * 32 * 4;
+  static constexpr int STG_BYTES = 4 * 2 * STG_BOX_BYTES;
   static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
-  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + BAR_BYTES;
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1024-byte swizzle atoms");
   static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation size");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -214,7 +218,7 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
 template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ Params p) {
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Params p) {
   using K_ = Cfg<BN, PAIR>;
   constexpr int CL = K_::CG;
   constexpr int STAGES = K_::STAGES;
@@ -224,7 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(1023));
   const uint32_t sA = ptx::smem_u32(smem);
   const uint32_t sB = sA + STAGES * K_::A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * K_::STAGE_BYTES);
+  const uint32_t sStg = sA + STAGES * K_::STAGE_BYTES;  // 1024-byte aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * K_::STAGE_BYTES + K_::STG_BYTES);
   const uint32_t bar0 = ptx::smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -241,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     ptx::prefetch_tensormap(&tmA);
     ptx::prefetch_tensormap(&tmB);
+    ptx::prefetch_tensormap(&tmC);
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1);
       ptx::mbar_init(empty_bar(s), 1);
@@ -428,9 +434,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!got) { aborted = true; break; }
           __threadfence();
         }
-        const int64_t row = int64_t(cta_m) * BM + row_local;
+        // C tile rows of this warp: (cta_m*128 + q*32) .. +31.  Each 32-column
+        // chunk goes registers -> staging box (row r at r*128 bytes, its 16-byte
+        // piece j at slot j ^ (r mod 8): the 8 lanes of each 16-byte phase hit
+        // 8 different bank groups) -> TMA store (full 128-byte lines; parts
+        // beyond M or N are clipped by the tensor map).
+        const int32_t row0 = int32_t(cta_m * BM + q * 32u);
         const int32_t col0 = int32_t(cta_n) * BN;
-        float* crow = p.C + row * p.N + col0;
+        const uint32_t stg_warp = sStg + (warp - 2u) * 2u * K_::STG_BOX_BYTES;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t r[32];
@@ -453,17 +464,22 @@ __global__ void __launch_bounds__(kThreads, 1)
               f[4 * v + 3] += x.w;
             }
           }
-          if (row < p.M) {
-            if (col0 + c + 32 <= p.N) {
-              float4* dst = reinterpret_cast<float4*>(crow + c);
+          const uint32_t box = stg_warp + uint32_t((c / 32) & 1) * K_::STG_BOX_BYTES;
+          // the store that last read this box (two chunks ago) must be done
+          if (lane == 0) ptx::bulk_wait_group_read<1>();
+          __syncwarp();
 #pragma unroll
-              for (int v = 0; v < 8; ++v)
-                dst[v] = make_float4(f[4 * v], f[4 * v + 1], f[4 * v + 2], f[4 * v + 3]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (col0 + c + j < p.N) crow[c + j] = f[j];
-            }
+          for (int v = 0; v < 8; ++v) {
+            const uint32_t dst = box + lane * 128u + ((uint32_t(v) ^ (lane & 7u)) << 4);
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(f[4 * v]),
+                         "f"(f[4 * v + 1]), "f"(f[4 * v + 2]), "f"(f[4 * v + 3])
+                         : "memory");
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&tmC, box, col0 + c, row0);
+            ptx::bulk_commit_group();
           }
         }
         ptx::tc_fence_before();
@@ -484,6 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---------------- teardown ----------------
+  if (warp >= 2 && lane == 0) ptx::bulk_wait_group<0>();  // C stores complete
   ptx::tc_fence_before();
   __syncthreads();
   if constexpr (PAIR) ptx::cluster_sync();
@@ -513,18 +530,24 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D row-major matrix rows x cols of 2-byte elements, box box_cols x box_rows,
-// 128-byte swizzle, out-of-bounds elements read as zero.
+// element type of a tensor map: the operands' fp16 / bf16, or fp32 for C
+constexpr int kMapF32 = 100;
+
+// 2-D row-major matrix rows x cols, box box_cols x box_rows, 128-byte swizzle;
+// out-of-bounds elements read as zero and are not written by stores.
 static int encode_2d(CUtensorMap* map, int dtype, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_cols, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cuda_fail(cudaErrorNotSupported);
+  const uint64_t esize = dtype == kMapF32 ? 4 : 2;
   const cuuint64_t dims[2] = {cols, rows};
-  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint64_t strides[1] = {cols * esize};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(map, dtype == SWZ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+  const CUtensorMapDataType t = dtype == kMapF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                : dtype == SWZ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUresult r = fn(map, t,
                         2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -639,8 +662,8 @@ static SkLayout sk_layout(const Plan& pl, int persistent, const swz_gemm_opts& o
 }
 
 template <int BN, bool PAIR>
-static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, const Params& prm,
-                  cudaStream_t stream) {
+static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
+                  const CUtensorMap& tc, const Params& prm, cudaStream_t stream) {
   using K_ = Cfg<BN, PAIR>;
   static std::mutex mu;
   static bool attr_set[64] = {};
@@ -669,7 +692,7 @@ static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  SWZ_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ta, tb, prm));
+  SWZ_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, prm));
   return SWZ_OK;
 }
 
@@ -783,10 +806,12 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
       !order_is_bijective(order, pl.sched_m, pl.sched_n, g))
     return SWZ_ENOTBIJECTIVE;
 
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   rc = encode_2d(&ta, o.dtype, A, uint64_t(M), uint64_t(K), BK, BM);
   if (rc != SWZ_OK) return rc;
   rc = encode_2d(&tb, o.dtype, B, uint64_t(K), uint64_t(N), 64, BK);
+  if (rc != SWZ_OK) return rc;
+  rc = encode_2d(&tc, kMapF32, C, uint64_t(M), uint64_t(N), 32, 32);
   if (rc != SWZ_OK) return rc;
 
   Params prm{};
@@ -826,9 +851,9 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
     }
   }
 
-  if (pl.pair) return launch<256, true>(pl, ta, tb, prm, s);
-  if (pl.bn == 128) return launch<128, false>(pl, ta, tb, prm, s);
-  return launch<256, false>(pl, ta, tb, prm, s);
+  if (pl.pair) return launch<256, true>(pl, ta, tb, tc, prm, s);
+  if (pl.bn == 128) return launch<128, false>(pl, ta, tb, tc, prm, s);
+  return launch<256, false>(pl, ta, tb, tc, prm, s);
 }
 
 extern "C" int swz_gemm(const void* A, const void* B, float* C, int M, int N, int K, int order,
