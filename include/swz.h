@@ -147,6 +147,30 @@ int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N, int K,
                 int order, int group, int persistent,
                 const swz_gemm_opts* opts, void* stream);
 
+/*
+ * swz_gemm_host -- the [TBS] GEMM from host memory: C = A * B with A, B read
+ * from host buffers and C written to a host buffer, the copies overlapped
+ * with the computation.  B (K x N) is copied to d_B first; A and C are cut
+ * into `slabs` row slabs (0 = 4; at most 64; slab heights are multiples of
+ * 256 rows): slab i of A is copied in on an input stream, multiplied on
+ * `stream` by swz_gemm_ex (persistent = 1, opts as given, order/group within
+ * the slab), and slab i of C copied out on an output stream while later
+ * slabs proceed.  The call is asynchronous like the others: when `stream`
+ * reaches the point after the call, C is in h_C.
+ * h_A (M x K), h_B (K x N): host, fp16/bf16 per opts->dtype; h_C (M x N,
+ * fp32): host.  Pinned (page-locked) host buffers are needed for the copies
+ * to overlap.  d_A, d_B, d_C: caller-owned device buffers of the full sizes,
+ * 16-byte aligned; their contents are overwritten.  The library keeps two
+ * streams and some events per device for this call (no device memory); calls
+ * are serialised while they enqueue.  Host-side argument and configuration
+ * checks (including Morton/XOR bijectivity on every slab grid) happen before
+ * anything is enqueued; a CUDA failure part-way returns SWZ_ECUDA with the
+ * earlier copies already enqueued.  Errors: as swz_gemm_ex.
+ */
+int swz_gemm_host(const void* h_A, const void* h_B, float* h_C, int M, int N, int K,
+                  int order, int group, const swz_gemm_opts* opts, void* d_A, void* d_B,
+                  float* d_C, int slabs, void* stream);
+
 /* Bytes of d_workspace a launch with these arguments needs (0 when
  * stream_k is off, the launch is not persistent or the tiles divide evenly
  * among the programs).  Needs the device when persistent and num_programs is

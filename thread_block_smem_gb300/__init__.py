@@ -34,7 +34,7 @@ LAYOUTS = {"naive": SWZ_SMEM_NAIVE, "padded": SWZ_SMEM_PADDED, "xor": SWZ_SMEM_X
 EXPORTS = ["swz_tile_map", "swz_is_bijective", "swz_gemm", "swz_gemm_ex", "swz_gemm_plan",
            "swz_transpose", "swz_check_status", "swz_strerror", "swz_last_cuda_error",
            "swz_device_info", "swz_l2_model", "swz_gemm_workspace_size",
-           "swz_gemm_streamk_noalloc"]
+           "swz_gemm_streamk_noalloc", "swz_gemm_host"]
 
 
 class SwzError(RuntimeError):
@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
                                               ctypes.POINTER(ctypes.c_uint64)]
         L.swz_gemm_streamk_noalloc.argtypes = [vp, vp, vp, i, i, i, i, i,
                                                ctypes.POINTER(swz_gemm_opts), vp]
+        L.swz_gemm_host.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.POINTER(swz_gemm_opts),
+                                    vp, vp, vp, i, vp]
         for name in EXPORTS:
             if name != "swz_strerror":
                 getattr(L, name).restype = ctypes.c_int
@@ -130,6 +132,12 @@ def swz_gemm_streamk_noalloc(A, B, C, M, N, K, order, group, opts=None, stream=0
     return lib().swz_gemm_streamk_noalloc(A, B, C, M, N, K, order, group,
                                           ctypes.byref(opts) if opts is not None else None,
                                           stream)
+
+
+def swz_gemm_host(hA, hB, hC, M, N, K, order, group, opts, dA, dB, dC, slabs=0, stream=0):
+    return lib().swz_gemm_host(hA, hB, hC, M, N, K, order, group,
+                               ctypes.byref(opts) if opts is not None else None,
+                               dA, dB, dC, slabs, stream)
 
 
 def swz_transpose(src, dst, M, N, layout, stream=0):
@@ -257,6 +265,28 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
     _check(swz_gemm_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _order(order),
                        group, int(bool(persistent)), opts, _stream(stream)), "swz_gemm_ex")
     return C
+
+
+def gemm_host(hA, hB, hC, dA, dB, dC, order="panel", group=8, *, tile_n=0, cta_pair=False,
+              num_programs=0, stream_k=False, workspace=None, slabs=0, stream=None):
+    """C = A @ B from host tensors through swz_gemm_host.  hA (M x K), hB
+    (K x N): CPU fp16/bf16 tensors (pinned for overlap); hC: CPU fp32 M x N;
+    dA, dB, dC: CUDA tensors of the same shapes used as staging.  Asynchronous
+    on `stream`; synchronise before reading hC."""
+    import torch
+    M, K = hA.shape
+    N = hB.shape[1]
+    for t, dev in ((hA, False), (hB, False), (hC, False), (dA, True), (dB, True), (dC, True)):
+        if t.is_cuda != dev or not t.is_contiguous():
+            raise ValueError("host tensors on the CPU, staging tensors on the GPU, contiguous")
+    if hA.dtype != hB.dtype or hA.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("A and B must both be fp16 or both bf16")
+    opts = make_opts(SWZ_BF16 if hA.dtype == torch.bfloat16 else SWZ_F16, tile_n, cta_pair,
+                     num_programs, None, 0, 0, stream_k, workspace)
+    _check(swz_gemm_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K, _order(order),
+                         group, opts, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), slabs,
+                         _stream(stream)), "swz_gemm_host")
+    return hC
 
 
 def transpose(x, layout="xor", out=None, stream=None):
