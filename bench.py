@@ -251,6 +251,7 @@ def run_swz(args):
     flush = torch.empty(2 * max(l2_bytes, 64 << 20) // 4, dtype=torch.float32, device=dev)
     do_gemm = args.only in ("all", "gemm", "sweep")
     do_transpose = args.only in ("all", "transpose") and not args.no_transpose
+    do_mma_sync = args.only in ("all", "mma_sync") and not args.no_mma_sync
 
     wl = WORKLOADS[args.workload]
     M, N, K = wl["M"], wl["N"], wl["K"]
@@ -401,6 +402,22 @@ def run_swz(args):
             del x, y
         line["transpose"] = tr
 
+    # ---- ldmatrix / mma.sync path: operand layout vs bank conflicts ---------
+    if do_mma_sync:
+        mm = 4096
+        Am, Bm = si.gemm_inputs(mm, mm, mm, "fp16", "uniform", seed=0)
+        Am, Bm = Am.to(dev), Bm.to(dev)
+        Cm = torch.empty((mm, mm), dtype=torch.float32, device=dev)
+        res = {}
+        for name in ("naive", "padded", "swizzle64", "swizzle128"):
+            fn = lambda: swz.gemm_mma_sync(Am, Bm, name, "panel", 8, out=Cm)
+            t = timed(fn, 10 if args.only == "all" else 1, 3 if args.only == "all" else 1)
+            med = statistics.median(t)
+            res[name] = {"ms": med, "tflops": 2.0 * mm ** 3 / med / 1e9,
+                         "layout": list(swz.SMEM_LAYOUTS[name])}
+        line["mma_sync_4096_fp16"] = res
+        del Am, Bm, Cm
+
     if rank != 0:
         if world > 1:
             tdist.destroy_process_group()
@@ -428,7 +445,9 @@ def main():
     ap.add_argument("--stream-k", action="store_true", help="Stream-K tail (persistent only)")
     ap.add_argument("--non-persistent", action="store_true", help="one CTA (pair) per tile")
     ap.add_argument("--e2e-slabs", type=int, default=8, help="row slabs of the host pipeline")
-    ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose"], default="all",
+    ap.add_argument("--no-mma-sync", action="store_true")
+    ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose", "mma_sync"],
+                    default="all",
                     help="gemm: headline steps only; sweep: one cold launch per order; "
                          "transpose: the transposes only (profiling modes)")
     args = ap.parse_args()

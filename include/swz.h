@@ -186,6 +186,28 @@ int swz_gemm_plan(int M, int N, int K, int persistent,
                   int* sched_m, int* sched_n, int* programs);
 
 /*
+ * swz_gemm_mma_sync -- [TBS] GEMM C = A * B (as swz_gemm: A M x K, B K x N
+ * row-major fp16/bf16 per `dtype`, C M x N fp32) on the warp-level tensor-core
+ * path: cp.async into shared memory, ldmatrix fragments, mma.sync m16n8k16,
+ * 128 x 128 x 64 CTA tiles, one CTA per tile in `order` (group as in
+ * swz_gemm).  The operand tiles' shared-memory layout is chosen by
+ * (vec, per_phase, max_phase, pad): element (r, c) of a tile with rows of W
+ * elements sits at r*(W + pad) + ((c/vec) ^ ((r/per_phase) % max_phase))*vec
+ * + c % vec -- [SBC] "Triton - Shared Layout swizzling" plus "Padding";
+ * (8,1,1,0) is the plain layout, (8,1,8,0) the 128-byte swizzle
+ * (Swizzle<3,3,3>, [SBC] "swizzle in CUTLASS"), (8,2,4,0) a 64-byte-style
+ * swizzle, (8,1,1,8) 16-byte padding.  Results are identical for every
+ * layout; ldmatrix bank conflicts ([SBC] "MMA Bank Conflict") are not.
+ * Requirements: vec, per_phase, max_phase powers of two, vec a multiple of
+ * 8, max_phase * vec <= 64, pad in {0, 8, ..., 64}; K % 8 == 0, N % 8 == 0;
+ * A, B 16-byte and C 8-byte aligned.  K = 0 writes zeros.  Errors:
+ * SWZ_EINVAL, SWZ_ENOTBIJECTIVE, SWZ_EARCH, SWZ_ECUDA.
+ */
+int swz_gemm_mma_sync(const void* A, const void* B, float* C, int M, int N, int K,
+                      int dtype, int vec, int per_phase, int max_phase, int pad,
+                      int order, int group, void* stream);
+
+/*
  * swz_transpose -- [SBC] "Matrix Transpose": out[j][i] = in[i][j] for an
  * M x N matrix of 32-bit words (out is N x M, row-major), staged through a
  * 32 x 32 shared-memory tile in `layout` (swz_smem_layout).  The result is

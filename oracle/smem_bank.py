@@ -161,3 +161,63 @@ def staged_row_store_conflicts(row_bytes, swizzled):
             addrs.append(t * row_bytes + jj * 16)
         out.append(conflicts(addrs, 16))
     return out
+
+
+# ----------------------------------------------------------------------------
+# ldmatrix / cp.async operand staging ("MMA Bank Conflict", "swizzle in
+# CUTLASS", "Triton - Shared Layout swizzling")
+# ----------------------------------------------------------------------------
+def staged_offset(r, c, width, vec, per_phase, max_phase, pad):
+    """Element offset of logical (r, c) in a tile with rows of `width`
+    elements plus `pad` elements of padding, under the Triton-style swizzle
+    (vec, perPhase, maxPhase); max_phase = 1 is the plain row-major tile."""
+    return r * (width + pad) + triton_source_column(r, c, vec, per_phase, max_phase)
+
+
+def ldmatrix_x4_addresses(r0, c0, width, layout, elem_bytes=2, trans_b=False):
+    """Byte addresses the 32 lanes of one ldmatrix.x4 supply for the 16 x 16
+    block at (r0, c0): lane l names row (l mod 8) of 8 x 8 matrix l div 8.
+    For the A operand (row-major M x K tile) matrix q covers rows
+    r0 + 8*(q mod 2) and columns c0 + 8*(q div 2); for the B operand loaded
+    with .trans (K x N tile, N contiguous) matrix q covers k rows
+    r0 + 8*(q mod 2) and n columns c0 + 8*(q div 2) as well."""
+    vec, per_phase, max_phase, pad = layout
+    out = []
+    for lane in range(32):
+        q, i = lane // 8, lane % 8
+        r = r0 + i + 8 * (q % 2)
+        c = c0 + 8 * (q // 2)
+        out.append(staged_offset(r, c, width, vec, per_phase, max_phase, pad) * elem_bytes)
+    return out
+
+
+def ldmatrix_conflicts_per_k_step(layout_a, layout_b, warp_m0, warp_n0, bk_step,
+                                  width_a, width_b):
+    """Bank conflicts of one warp's fragment loads for one 16-deep K step of
+    the mma.sync GEMM: four ldmatrix.x4 over A rows warp_m0 .. +63 and two
+    ldmatrix.x4.trans over B columns warp_n0 .. +31."""
+    total = 0
+    for mt in range(4):
+        total += conflicts(ldmatrix_x4_addresses(warp_m0 + 16 * mt, bk_step, width_a,
+                                                 layout_a), 16)
+    for nt in range(2):
+        total += conflicts(ldmatrix_x4_addresses(bk_step, warp_n0 + 16 * nt, width_b,
+                                                 layout_b), 16)
+    return total
+
+
+def cp_async_tile_conflicts(rows, width, layout, threads=256):
+    """Bank conflicts of the 16-byte cp.async writes that fill one tile of
+    `rows` x `width` halves: chunk t (row t div (width/8), 8-element column
+    group t mod (width/8)) is written by thread t mod threads; each warp
+    instruction writes 32 consecutive chunks."""
+    per_row = width // 8
+    chunks = rows * per_row
+    total = 0
+    for base in range(0, chunks, 32):
+        addrs = []
+        for t in range(base, min(base + 32, chunks)):
+            r, g = divmod(t, per_row)
+            addrs.append(staged_offset(r, 8 * g, width, *layout) * 2)
+        total += conflicts(addrs, 16)
+    return total

@@ -110,3 +110,37 @@ def test_staged_epilogue_store_conflicts():
 def test_padding_breaks_16b_alignment():
     # the page's caveat: in int[32][33], row 1 starts at byte 132, not 16-aligned
     assert (sb.padded_offset(1, 0, 32) * 4) % 16 != 0
+
+
+def test_ldmatrix_conflict_model():
+    # Rows 128 bytes apart (64 fp16 elements) share one bank group: the 8
+    # lanes of an ldmatrix phase that name 8 consecutive rows at one column
+    # chunk serialise 8-fold -> 7 extra wavefronts per phase, 28 per x4.
+    naive, pad, swz128, swz64 = (8, 1, 1, 0), (8, 1, 1, 8), (8, 1, 8, 0), (8, 2, 4, 0)
+    assert sb.conflicts(sb.ldmatrix_x4_addresses(0, 0, 64, naive), 16) == 28
+    assert sb.conflicts(sb.ldmatrix_x4_addresses(0, 0, 128, naive), 16) == 28
+    # 16 bytes of padding shift each row by 4 banks: conflict free
+    assert sb.conflicts(sb.ldmatrix_x4_addresses(16, 8, 64, pad), 16) == 0
+    # chunk XOR row (mod 8) puts the 8 rows of a phase into 8 bank groups
+    for r0, c0 in [(0, 0), (16, 16), (48, 48)]:
+        assert sb.conflicts(sb.ldmatrix_x4_addresses(r0, c0, 64, swz128), 16) == 0
+    # two rows per phase value: pairs of rows collide -> 2-way, 4 per x4
+    assert sb.conflicts(sb.ldmatrix_x4_addresses(0, 0, 64, swz64), 16) == 4
+    # the Swizzle<3,3,3> formula of the CUTLASS section equals the (8,1,8)
+    # Triton layout on 64-element rows
+    for r in range(16):
+        for c in range(64):
+            assert sb.staged_offset(r, c, 64, *swz128) == sb.cute_swizzle(r * 64 + c, 3, 3, 3)
+
+
+def test_mma_sync_kernel_conflict_totals():
+    # per CTA and 64-deep K block (8 warps x 4 steps x 6 ldmatrix.x4)
+    lays = {"naive": (8, 1, 1, 0), "padded": (8, 1, 1, 8), "swz128": (8, 1, 8, 0),
+            "swz64": (8, 2, 4, 0)}
+    want = {"naive": 8 * 4 * 6 * 28, "padded": 0, "swz128": 0, "swz64": 8 * 4 * 6 * 4}
+    for name, lay in lays.items():
+        got = sum(sb.ldmatrix_conflicts_per_k_step(lay, lay, wm * 64, wn * 32, ks * 16, 64, 128)
+                  for wm in range(2) for wn in range(4) for ks in range(4))
+        assert got == want[name], name
+        assert sb.cp_async_tile_conflicts(128, 64, lay) == 0
+        assert sb.cp_async_tile_conflicts(64, 128, lay) == 0

@@ -34,7 +34,7 @@ LAYOUTS = {"naive": SWZ_SMEM_NAIVE, "padded": SWZ_SMEM_PADDED, "xor": SWZ_SMEM_X
 EXPORTS = ["swz_tile_map", "swz_is_bijective", "swz_gemm", "swz_gemm_ex", "swz_gemm_plan",
            "swz_transpose", "swz_check_status", "swz_strerror", "swz_last_cuda_error",
            "swz_device_info", "swz_l2_model", "swz_gemm_workspace_size",
-           "swz_gemm_streamk_noalloc", "swz_gemm_host"]
+           "swz_gemm_streamk_noalloc", "swz_gemm_host", "swz_gemm_mma_sync"]
 
 
 class SwzError(RuntimeError):
@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
                                                ctypes.POINTER(swz_gemm_opts), vp]
         L.swz_gemm_host.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.POINTER(swz_gemm_opts),
                                     vp, vp, vp, i, vp]
+        L.swz_gemm_mma_sync.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, i, i, vp]
         for name in EXPORTS:
             if name != "swz_strerror":
                 getattr(L, name).restype = ctypes.c_int
@@ -138,6 +139,33 @@ def swz_gemm_host(hA, hB, hC, M, N, K, order, group, opts, dA, dB, dC, slabs=0, 
     return lib().swz_gemm_host(hA, hB, hC, M, N, K, order, group,
                                ctypes.byref(opts) if opts is not None else None,
                                dA, dB, dC, slabs, stream)
+
+
+def swz_gemm_mma_sync(A, B, C, M, N, K, dtype, vec, per_phase, max_phase, pad, order, group,
+                      stream=0):
+    return lib().swz_gemm_mma_sync(A, B, C, M, N, K, dtype, vec, per_phase, max_phase, pad,
+                                   order, group, stream)
+
+
+# named operand layouts of swz_gemm_mma_sync: (vec, per_phase, max_phase, pad)
+SMEM_LAYOUTS = {"naive": (8, 1, 1, 0), "padded": (8, 1, 1, 8), "swizzle128": (8, 1, 8, 0),
+                "swizzle64": (8, 2, 4, 0)}
+
+
+def gemm_mma_sync(A, B, layout="swizzle128", order="panel", group=8, out=None, stream=None):
+    """C = A @ B through swz_gemm_mma_sync with the given operand layout (a
+    name of SMEM_LAYOUTS or a (vec, per_phase, max_phase, pad) tuple)."""
+    import torch
+    if A.dtype != B.dtype or A.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError("A and B must both be fp16 or both bf16")
+    M, K = A.shape
+    N = B.shape[1]
+    C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=A.device)
+    lay = SMEM_LAYOUTS[layout] if isinstance(layout, str) else tuple(layout)
+    _check(swz_gemm_mma_sync(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                             SWZ_BF16 if A.dtype == torch.bfloat16 else SWZ_F16, *lay,
+                             _order(order), group, _stream(stream)), "swz_gemm_mma_sync")
+    return C
 
 
 def swz_transpose(src, dst, M, N, layout, stream=0):
