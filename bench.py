@@ -47,7 +47,7 @@ WORKLOADS = {
     "gemm1024x1024x512_fp16": dict(M=1024, N=1024, K=512, dtype="fp16", dist="uniform",
                                    cfg=dict(tile_n=128), tile=(128, 128), cluster_m=1),
 }
-HEADLINE = dict(order="panel", group=8, persistent=True)
+HEADLINE = dict(order="serpentine", group=8, persistent=True)
 SWEEP = [("row", 1), ("col", 1), ("panel", 4), ("panel", 8), ("panel", 16),
          ("serpentine", 4), ("serpentine", 8), ("serpentine", 16), ("morton", 1), ("xor", 1)]
 

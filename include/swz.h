@@ -128,6 +128,12 @@ typedef struct swz_gemm_opts {
                         use; the library keeps it consistent afterwards.
                         Launches sharing a workspace must not overlap.       */
   uint64_t workspace_bytes; /* size of d_workspace                           */
+  int split_tail;    /* persistent only, not with stream_k: when the R tiles
+                        left for the last wave number at most half the
+                        programs (clusters), split each into two halves of
+                        tile_n / 2 columns so that 2R programs finish the last
+                        wave in half the time; no workspace.  A split tile's
+                        trace entry records one of its two halves.           */
 } swz_gemm_opts;
 
 /* debug_flags: withhold the first operand load so that the consumer's

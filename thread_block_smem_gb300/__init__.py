@@ -49,7 +49,7 @@ class swz_gemm_opts(ctypes.Structure):
                 ("num_programs", ctypes.c_int), ("d_trace", ctypes.c_void_p),
                 ("debug_flags", ctypes.c_uint32), ("timeout_ms", ctypes.c_uint32),
                 ("stream_k", ctypes.c_int), ("d_workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_uint64)]
+                ("workspace_bytes", ctypes.c_uint64), ("split_tail", ctypes.c_int)]
 
 
 _lib = None
@@ -238,8 +238,9 @@ def tile_map(order, grid_m, grid_n, group=1, device="cuda", stream=None):
 
 
 def make_opts(dtype=SWZ_F16, tile_n=0, cta_pair=False, num_programs=0, trace=None,
-              debug_flags=0, timeout_ms=0, stream_k=False, workspace=None):
+              debug_flags=0, timeout_ms=0, stream_k=False, workspace=None, split_tail=False):
     o = swz_gemm_opts()
+    o.split_tail = 1 if split_tail else 0
     o.stream_k = 1 if stream_k else 0
     if workspace is not None:
         o.d_workspace = workspace.data_ptr()
@@ -274,7 +275,7 @@ def workspace_size(M, N, K, persistent=True, tile_n=0, cta_pair=False, num_progr
 
 def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
          cta_pair=False, num_programs=0, trace=None, debug_flags=0, timeout_ms=0,
-         stream_k=False, workspace=None, stream=None):
+         stream_k=False, workspace=None, split_tail=False, stream=None):
     """C = A @ B (fp32) through swz_gemm_ex.  A: M x K, B: K x N, both fp16 or
     both bf16, row-major contiguous CUDA tensors.  With stream_k, `workspace`
     is a zero-initialised CUDA tensor of at least workspace_size(...) bytes."""
@@ -289,14 +290,16 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
     N = B.shape[1]
     C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=A.device)
     opts = make_opts(SWZ_BF16 if A.dtype == torch.bfloat16 else SWZ_F16, tile_n, cta_pair,
-                     num_programs, trace, debug_flags, timeout_ms, stream_k, workspace)
+                     num_programs, trace, debug_flags, timeout_ms, stream_k, workspace,
+                     split_tail)
     _check(swz_gemm_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _order(order),
                        group, int(bool(persistent)), opts, _stream(stream)), "swz_gemm_ex")
     return C
 
 
 def gemm_host(hA, hB, hC, dA, dB, dC, order="panel", group=8, *, tile_n=0, cta_pair=False,
-              num_programs=0, stream_k=False, workspace=None, slabs=0, stream=None):
+              num_programs=0, stream_k=False, workspace=None, split_tail=False, slabs=0,
+              stream=None):
     """C = A @ B from host tensors through swz_gemm_host.  hA (M x K), hB
     (K x N): CPU fp16/bf16 tensors (pinned for overlap); hC: CPU fp32 M x N;
     dA, dB, dC: CUDA tensors of the same shapes used as staging.  Asynchronous
@@ -310,7 +313,7 @@ def gemm_host(hA, hB, hC, dA, dB, dC, order="panel", group=8, *, tile_n=0, cta_p
     if hA.dtype != hB.dtype or hA.dtype not in (torch.float16, torch.bfloat16):
         raise TypeError("A and B must both be fp16 or both bf16")
     opts = make_opts(SWZ_BF16 if hA.dtype == torch.bfloat16 else SWZ_F16, tile_n, cta_pair,
-                     num_programs, None, 0, 0, stream_k, workspace)
+                     num_programs, None, 0, 0, stream_k, workspace, split_tail)
     _check(swz_gemm_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K, _order(order),
                          group, opts, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), slabs,
                          _stream(stream)), "swz_gemm_host")

@@ -93,11 +93,14 @@ struct Params {
   int order, group;
   uint32_t sched_m, sched_n;  // scheduler grid (cluster tiles with PAIR)
   uint32_t num_kb;            // ceil(K / BK)
-  uint32_t idesc;
+  uint32_t idesc;       // full-width MMA (N = BN)
+  uint32_t idesc_half;  // half-width MMA (N = BN/2) for split tail tiles
+  uint32_t b3d;         // B's share of a full-width tile in one 3-D box (N % 64 == 0)
   int32_t* trace;
   uint32_t debug_flags;
   uint64_t timeout_ns;
-  // Stream-K tail (persistent launches only; 0 = whole tiles everywhere)
+  // tail policies (persistent launches only; both 0 = whole tiles everywhere)
+  uint32_t split_tail;  // halve the N width of the tiles of the last wave
   uint32_t stream_k;
   uint32_t epoch;      // value a finished partial's flag takes in this launch
   uint32_t* sk_flags;  // [cluster][rank][lane quarter]
@@ -117,30 +120,41 @@ enum ItemKind : int { kWhole = 0, kFirst = 1, kPartial = 2 };
 // (R < P), so it holds at most two pieces: a piece that starts inside a tile
 // (a partial, written to the workspace) and a piece that starts a tile (its
 // first piece: the cluster owning it adds the other pieces and writes C).
+// With split_tail, when the R = U mod P tail units would leave most clusters
+// idle in the last wave and 2R <= P, each tail unit is cut into two halves of
+// N width BN/2 (left half, right half) and cluster h takes half-unit h: the
+// last wave then runs on 2R clusters for half as long, with no data exchanged
+// between clusters.
 struct Schedule {
   uint32_t c, P, U, kb;
   uint32_t dp_end;  // units below this are whole tiles
   uint32_t n_dp;    // whole tiles of this cluster
-  uint64_t I;       // tail iterations
-  uint64_t s, e;    // this cluster's tail range [s, e)
+  uint32_t n_half;  // 1 if this cluster takes a half-width tail tile
+  uint64_t I;       // Stream-K tail iterations
+  uint64_t s, e;    // this cluster's Stream-K tail range [s, e)
 
   __device__ __forceinline__ void init(uint32_t c_, uint32_t P_, uint32_t U_, uint32_t kb_,
-                                       bool sk) {
+                                       bool sk, bool split) {
     c = c_;
     P = P_;
     U = U_;
     kb = kb_;
-    const uint32_t R = sk ? U % P : 0u;
+    uint32_t R = U % P;
+    const bool halves = !sk && split && R > 0 && 2 * R <= P;
+    if (!sk && !halves) R = 0;
     dp_end = U - R;
     n_dp = c < dp_end ? (dp_end - c + P - 1) / P : 0u;
-    I = uint64_t(R) * kb;
+    n_half = halves && c < 2 * R ? 1u : 0u;
+    I = sk ? uint64_t(R) * kb : 0u;
     s = range_start(c);
     e = range_start(c + 1);
   }
   __device__ __forceinline__ uint64_t range_start(uint32_t cc) const { return I * cc / P; }
-  // The i-th piece of work: unit, K-block range [k0, k1), kind.
+  // The i-th piece of work: unit, K-block range [k0, k1), kind, and which
+  // half of the N width (-1: the whole width).
   __device__ __forceinline__ bool item(uint32_t i, uint32_t& unit, uint32_t& k0, uint32_t& k1,
-                                       int& kind) const {
+                                       int& kind, int& half) const {
+    half = -1;
     if (i < n_dp) {
       unit = c + i * P;
       k0 = 0;
@@ -149,6 +163,15 @@ struct Schedule {
       return true;
     }
     i -= n_dp;
+    if (n_half) {
+      if (i != 0) return false;
+      unit = dp_end + c / 2;
+      half = int(c & 1u);
+      k0 = 0;
+      k1 = kb;
+      kind = kWhole;
+      return true;
+    }
     if (s >= e) return false;
     const uint64_t t = s / kb + i;
     const uint64_t t0 = t * kb;
@@ -218,7 +241,8 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
 template <int BN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Params p) {
+                const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmC,
+                const __grid_constant__ Params p) {
   using K_ = Cfg<BN, PAIR>;
   constexpr int CL = K_::CG;
   constexpr int STAGES = K_::STAGES;
@@ -246,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     ptx::prefetch_tensormap(&tmA);
     ptx::prefetch_tensormap(&tmB);
+    if (p.b3d) ptx::prefetch_tensormap(&tmB3);
     ptx::prefetch_tensormap(&tmC);
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1);
@@ -277,7 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t units = p.sched_m * p.sched_n;
   Schedule sch;
-  sch.init(blockIdx.x / CL, gridDim.x / CL, units, p.num_kb, p.stream_k != 0);
+  sch.init(blockIdx.x / CL, gridDim.x / CL, units, p.num_kb, p.stream_k != 0,
+           p.split_tail != 0);
   bool aborted = false;
 
   if (warp == 0) {
@@ -286,31 +312,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       bool skip = (p.debug_flags & SWZ_DEBUG_SKIP_FIRST_LOAD) != 0;
       uint32_t w, kbeg, kend;
-      int kind;
-      for (uint32_t i = 0; !aborted && sch.item(i, w, kbeg, kend, kind); ++i) {
+      int kind, half;
+      for (uint32_t i = 0; !aborted && sch.item(i, w, kbeg, kend, kind, half); ++i) {
         const TileCoord t = tile_of(p.order, w, p.sched_m, p.sched_n, uint32_t(p.group));
         const int32_t m0 = int32_t((t.m * CL + rank) * BM);
-        const int32_t n0 = int32_t(t.n * BN + rank * K_::BN_LOCAL);
+        // B columns this CTA loads: its share of the tile (or of one half)
+        const int local = half < 0 ? K_::BN_LOCAL : K_::BN_LOCAL / 2;
+        const int32_t n0 = int32_t(t.n * BN + (half < 0 ? 0 : half * (BN / 2)) + rank * local);
+        const int boxes = local / 64;
+        const uint32_t tx = uint32_t(CL) * uint32_t(K_::A_BYTES + boxes * K_::B_BOX_BYTES);
         for (uint32_t kb = kbeg; kb < kend; ++kb) {
           if (!wait(empty_bar(stage), phase ^ 1u, ctl)) { aborted = true; break; }
-          if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), K_::TX_BYTES);
+          if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), tx);
           if (skip) {
             skip = false;
           } else {
             const uint32_t fb = PAIR ? ptx::map_to_rank(full_bar(stage), 0) : full_bar(stage);
             const int32_t k0 = int32_t(kb * BK);
+            // B: one 3-D box (64 columns x 64 K rows x `boxes` column
+            // groups) when the map allows it, else one 2-D box per group;
+            // the shared-memory layout is the same either way
+            const bool one_box = p.b3d && half < 0;
             if constexpr (PAIR) {
               ptx::tma_load_2d_pair(sA + stage * K_::A_BYTES, &tmA, fb, k0, m0);
-#pragma unroll
-              for (int j = 0; j < K_::BN_LOCAL / 64; ++j)
-                ptx::tma_load_2d_pair(sB + stage * K_::B_BYTES + j * K_::B_BOX_BYTES, &tmB, fb,
-                                      n0 + 64 * j, k0);
+              if (one_box)
+                ptx::tma_load_3d_pair(sB + stage * K_::B_BYTES, &tmB3, fb, 0, k0, n0 / 64);
+              else
+                for (int j = 0; j < boxes; ++j)
+                  ptx::tma_load_2d_pair(sB + stage * K_::B_BYTES + j * K_::B_BOX_BYTES, &tmB,
+                                        fb, n0 + 64 * j, k0);
             } else {
               ptx::tma_load_2d(sA + stage * K_::A_BYTES, &tmA, fb, k0, m0);
-#pragma unroll
-              for (int j = 0; j < K_::BN_LOCAL / 64; ++j)
-                ptx::tma_load_2d(sB + stage * K_::B_BYTES + j * K_::B_BOX_BYTES, &tmB, fb,
-                                 n0 + 64 * j, k0);
+              if (one_box)
+                ptx::tma_load_3d(sB + stage * K_::B_BYTES, &tmB3, fb, 0, k0, n0 / 64);
+              else
+                for (int j = 0; j < boxes; ++j)
+                  ptx::tma_load_2d(sB + stage * K_::B_BYTES + j * K_::B_BOX_BYTES, &tmB, fb,
+                                   n0 + 64 * j, k0);
             }
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -332,26 +370,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued = false;
       uint32_t w, kbeg, kend;
-      int kind;
-      for (uint32_t i = 0; !aborted && sch.item(i, w, kbeg, kend, kind); ++i) {
+      int kind, half;
+      for (uint32_t i = 0; !aborted && sch.item(i, w, kbeg, kend, kind, half); ++i) {
         if (!wait(tempty_bar(acc), acc_phase ^ 1u, ctl)) { aborted = true; break; }
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
+        const uint32_t idesc = half < 0 ? p.idesc : p.idesc_half;
         for (uint32_t kb = kbeg; kb < kend; ++kb) {
           if (!wait(full_bar(stage), phase, ctl)) { aborted = true; break; }
           ptx::tc_fence_after();
           const uint32_t a_addr = sA + stage * K_::A_BYTES;
           const uint32_t b_addr = sB + stage * K_::B_BYTES;
+          // A: K-major; each 16-element K slice starts 32 bytes further into
+          // each 128-byte row (+2 in the descriptor's address field); 8-row
+          // groups are 1024 bytes apart.  B: N-major; each slice is 16 K rows
+          // of 128 bytes further (+128); 8-row groups 1024 bytes apart along
+          // K, 64-column boxes B_BOX_BYTES apart along N.  The address field
+          // cannot carry: shared addresses are below 2^18 bytes.
+          const uint64_t adesc = make_sdesc(a_addr, 16, 1024);
+          const uint64_t bdesc = make_sdesc(b_addr, K_::B_BOX_BYTES, 1024);
+          ptx::mma_f16<CL>(d, adesc, bdesc, idesc, kb != kbeg ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            // A: K-major; the 16-element K slice starts 32 bytes further
-            // into each 128-byte row; 8-row groups are 1024 bytes apart.
-            const uint64_t adesc = make_sdesc(a_addr + kk * 32, 16, 1024);
-            // B: N-major; 16 K rows of 128 bytes further; 8-row groups
-            // 1024 bytes apart along K, 64-column boxes B_BOX_BYTES apart.
-            const uint64_t bdesc = make_sdesc(b_addr + kk * 2048, K_::B_BOX_BYTES, 1024);
-            ptx::mma_f16<CL>(d, adesc, bdesc, p.idesc, (kb != kbeg || kk != 0) ? 1u : 0u);
-          }
+          for (int kk = 1; kk < BK / UMMA_K; ++kk)
+            ptx::mma_f16<CL>(d, adesc + uint64_t(2 * kk), bdesc + uint64_t(128 * kk), idesc, 1u);
           issued = true;
           if constexpr (PAIR) ptx::mma_commit_pair(empty_bar(stage), 0x3);
           else ptx::mma_commit(empty_bar(stage));
@@ -383,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t row_local = q * 32u + lane;
     uint32_t acc = 0, acc_phase = 0;
     uint32_t w, kbeg, kend;
-    int kind;
-    for (uint32_t i = 0; sch.item(i, w, kbeg, kend, kind); ++i) {
+    int kind, half;
+    for (uint32_t i = 0; sch.item(i, w, kbeg, kend, kind, half); ++i) {
       const bool ok = wait(tfull_bar(acc), acc_phase, ctl);
       if (!__all_sync(0xFFFFFFFFu, ok)) { aborted = true; break; }
       ptx::tc_fence_after();
@@ -440,10 +481,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 8 different bank groups) -> TMA store (full 128-byte lines; parts
         // beyond M or N are clipped by the tensor map).
         const int32_t row0 = int32_t(cta_m * BM + q * 32u);
-        const int32_t col0 = int32_t(cta_n) * BN;
+        const int width = half < 0 ? BN : BN / 2;
+        const int32_t col0 = int32_t(cta_n) * BN + (half < 0 ? 0 : half * (BN / 2));
         const uint32_t stg_warp = sStg + (warp - 2u) * 2u * K_::STG_BOX_BYTES;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 0; c < width; c += 32) {
           uint32_t r[32];
           ptx::tmem_ld_32x32b_x32(taddr + c, r);
           ptx::tmem_ld_wait();
@@ -551,6 +593,26 @@ static int encode_2d(CUtensorMap* map, int dtype, const void* base, uint64_t row
                         2, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return SWZ_OK;
+}
+
+// B (K x N row-major, N % 64 == 0) seen as a 3-D tensor (64 columns, K rows,
+// N/64 column groups); box 64 x 64 x `groups`, 128-byte swizzle.  In shared
+// memory the box is `groups` consecutive 64 x 64 blocks, as the 2-D boxes.
+static int encode_b_groups(CUtensorMap* map, int dtype, const void* base, uint64_t K, uint64_t N,
+                           uint32_t groups) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cuda_fail(cudaErrorNotSupported);
+  const cuuint64_t dims[3] = {64, K, N / 64};
+  const cuuint64_t strides[2] = {N * 2, 128};
+  const cuuint32_t box[3] = {64, uint32_t(BK), groups};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r =
+      fn(map, dtype == SWZ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+         3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
   return SWZ_OK;
 }
@@ -663,7 +725,8 @@ static SkLayout sk_layout(const Plan& pl, int persistent, const swz_gemm_opts& o
 
 template <int BN, bool PAIR>
 static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
-                  const CUtensorMap& tc, const Params& prm, cudaStream_t stream) {
+                  const CUtensorMap& tb3, const CUtensorMap& tc, const Params& prm,
+                  cudaStream_t stream) {
   using K_ = Cfg<BN, PAIR>;
   static std::mutex mu;
   static bool attr_set[64] = {};
@@ -692,7 +755,7 @@ static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  SWZ_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, prm));
+  SWZ_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ta, tb, tb3, tc, prm));
   return SWZ_OK;
 }
 
@@ -806,11 +869,21 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
       !order_is_bijective(order, pl.sched_m, pl.sched_n, g))
     return SWZ_ENOTBIJECTIVE;
 
-  CUtensorMap ta, tb, tc;
+  CUtensorMap ta, tb, tb3, tc;
   rc = encode_2d(&ta, o.dtype, A, uint64_t(M), uint64_t(K), BK, BM);
   if (rc != SWZ_OK) return rc;
   rc = encode_2d(&tb, o.dtype, B, uint64_t(K), uint64_t(N), 64, BK);
   if (rc != SWZ_OK) return rc;
+  // B as (64 columns, K rows, N/64 column groups): a CTA's whole share of a
+  // tile in one box.  Only when N % 64 == 0: a partial last group would read
+  // the next row's elements instead of zeros.
+  const bool b3d = (N % 64) == 0;
+  tb3 = tb;
+  if (b3d) {
+    rc = encode_b_groups(&tb3, o.dtype, B, uint64_t(K), uint64_t(N),
+                         uint32_t((pl.pair ? pl.bn / 2 : pl.bn) / 64));
+    if (rc != SWZ_OK) return rc;
+  }
   rc = encode_2d(&tc, kMapF32, C, uint64_t(M), uint64_t(N), 32, 32);
   if (rc != SWZ_OK) return rc;
 
@@ -825,6 +898,11 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   prm.sched_n = pl.sched_n;
   prm.num_kb = uint32_t((K + BK - 1) / BK);
   prm.idesc = make_idesc(o.dtype, pl.pair ? 256 : 128, pl.bn);
+  prm.idesc_half = make_idesc(o.dtype, pl.pair ? 256 : 128, pl.bn / 2);
+  if (o.split_tail) {
+    if (!persistent || o.stream_k) return SWZ_EINVAL;
+    prm.split_tail = 1;
+  }
   prm.trace = o.d_trace;
   prm.debug_flags = o.debug_flags;
   prm.timeout_ns = uint64_t(o.timeout_ms ? o.timeout_ms : 2000u) * 1000000ull;
@@ -851,9 +929,10 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
     }
   }
 
-  if (pl.pair) return launch<256, true>(pl, ta, tb, tc, prm, s);
-  if (pl.bn == 128) return launch<128, false>(pl, ta, tb, tc, prm, s);
-  return launch<256, false>(pl, ta, tb, tc, prm, s);
+  prm.b3d = b3d ? 1u : 0u;
+  if (pl.pair) return launch<256, true>(pl, ta, tb, tb3, tc, prm, s);
+  if (pl.bn == 128) return launch<128, false>(pl, ta, tb, tb3, tc, prm, s);
+  return launch<256, false>(pl, ta, tb, tb3, tc, prm, s);
 }
 
 extern "C" int swz_gemm(const void* A, const void* B, float* C, int M, int N, int K, int order,
