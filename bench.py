@@ -54,17 +54,17 @@ SWEEP = [("row", 1), ("col", 1), ("panel", 4), ("panel", 8), ("panel", 16),
 # DRAM traffic of one launch of the headline GEMM from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
 # source whose SHA-256 prefix is recorded with it.
-TRAFFIC = {"bytes": 1339318528, "gemm_cu_sha256": "354b9f06b2a7b4da",
+TRAFFIC = {"bytes": 1300055552, "gemm_cu_sha256": "232fb2601831c892",
            "profile": "profiles/gemm_8192_bf16_pair_ncu.md"}
 
 
 # L2 hit rate (lts__t_sector_hit_rate.pct) of one cold launch per order from
 # an ncu capture of `bench.py --only sweep`; valid for the recorded kernel
 # source only.
-L2_NCU = {"gemm_cu_sha256": "354b9f06b2a7b4da", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
-          ("row", 1): 63.06, ("col", 1): 63.66, ("panel", 4): 66.60, ("panel", 8): 73.91,
-          ("panel", 16): 69.36, ("serpentine", 4): 73.28, ("serpentine", 8): 74.08,
-          ("serpentine", 16): 71.73, ("morton", 1): 68.97, ("xor", 1): 62.94}
+L2_NCU = {"gemm_cu_sha256": "232fb2601831c892", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
+          ("row", 1): 62.31, ("col", 1): 62.13, ("panel", 4): 69.04, ("panel", 8): 73.54,
+          ("panel", 16): 67.61, ("serpentine", 4): 70.93, ("serpentine", 8): 73.66,
+          ("serpentine", 16): 69.57, ("morton", 1): 69.16, ("xor", 1): 63.01}
 
 
 def _gemm_src_hash():
