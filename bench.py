@@ -402,6 +402,22 @@ def run_swz(args):
             del x, y
         line["transpose"] = tr
 
+    # ---- TF32 path (fp32 inputs, B stored N x K), 8192^3 ---------------------
+    if args.only == "all" and not args.no_tf32:
+        g = torch.Generator().manual_seed(0)
+        A32 = (torch.rand((M, K), generator=g) * 2 - 1).to(dev)
+        Bt32 = (torch.rand((N, K), generator=g) * 2 - 1).to(dev)
+        C32 = torch.empty((M, N), dtype=torch.float32, device=dev)
+        t = timed(lambda: swz.gemm(A32, Bt32, head_order, head_group, True, out=C32,
+                                   b_transposed=True, cta_pair=True), 10, 3)
+        med = statistics.median(t)
+        # the recipe's nominal dense ratio tf32 / bf16 = 1.1 / 2.25 PFLOP/s
+        peak_tf32 = peaks["bf16_tflops"] * 1.1 / 2.25
+        line["tf32_8192"] = {"ms": med, "tflops": flops / med / 1e9,
+                             "peak": peak_tf32, "frac": flops / med / 1e9 / peak_tf32,
+                             "peak_source": "measured bf16 x nominal 1.1/2.25"}
+        del A32, Bt32, C32
+
     # ---- ldmatrix / mma.sync path: operand layout vs bank conflicts ---------
     if do_mma_sync:
         mm = 4096
@@ -446,6 +462,7 @@ def main():
     ap.add_argument("--non-persistent", action="store_true", help="one CTA (pair) per tile")
     ap.add_argument("--e2e-slabs", type=int, default=8, help="row slabs of the host pipeline")
     ap.add_argument("--no-mma-sync", action="store_true")
+    ap.add_argument("--no-tf32", action="store_true")
     ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose", "mma_sync"],
                     default="all",
                     help="gemm: headline steps only; sweep: one cold launch per order; "

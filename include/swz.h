@@ -60,7 +60,13 @@ enum swz_order {
   SWZ_SERPENTINE = 5  /* strips of S columns, rows walked down / up alternately*/
 };
 
-enum swz_dtype { SWZ_F16 = 0, SWZ_BF16 = 1 };
+/* operand types: fp16, bf16, or fp32 multiplied as TF32 (the first page's
+ * --dtype fp32 runs the same kernel with TF32 tensor cores) */
+enum swz_dtype { SWZ_F16 = 0, SWZ_BF16 = 1, SWZ_TF32 = 2 };
+
+/* storage of B: K x N row-major (the pages' B) or N x K row-major (B
+ * transposed, K contiguous) */
+enum swz_b_layout { SWZ_B_KN = 0, SWZ_B_NK = 1 };
 
 /* shared-memory tile layouts of the transpose ([SBC] "Matrix Transpose") */
 enum swz_smem_layout {
@@ -97,8 +103,10 @@ int swz_is_bijective(int order, int grid_m, int grid_n, int group);
  * CTA b takes tile ids b, b + P, b + 2P, ... ([TBS] persistent loop, [CPS]
  * work_idx striding).  Ragged M, N, K are handled (TMA zero-fill on loads,
  * clipped stores).  K = 0 writes zeros; M = 0 or N = 0 is a no-op.
- * Requirements: A, B 16-byte aligned; C 16-byte aligned; K % 8 == 0,
- * N % 8 == 0; M, N, K < 2^31.  Errors: SWZ_EINVAL, SWZ_ENOTBIJECTIVE (Morton
+ * Requirements: A, B 16-byte aligned; C 16-byte aligned; rows of A (and of
+ * B in either layout) a multiple of 16 bytes (K % 8 == 0 for fp16/bf16,
+ * K % 4 == 0 for TF32; N % 8 == 0 for B as K x N); N % 4 == 0; M, N, K <
+ * 2^31.  Errors: SWZ_EINVAL, SWZ_ENOTBIJECTIVE (Morton
  * or XOR on a grid they do not permute), SWZ_EARCH, SWZ_ECUDA.
  */
 int swz_gemm(const void* A, const void* B, float* C, int M, int N, int K,
@@ -106,7 +114,8 @@ int swz_gemm(const void* A, const void* B, float* C, int M, int N, int K,
 
 /* Options of swz_gemm_ex (zero-initialise, then set what you need). */
 typedef struct swz_gemm_opts {
-  int dtype;         /* SWZ_F16 (default) or SWZ_BF16; A and B share it      */
+  int dtype;         /* SWZ_F16 (default), SWZ_BF16 or SWZ_TF32 (fp32 A and B,
+                        multiplied as TF32; needs b_layout = SWZ_B_NK)        */
   int tile_n;        /* 128 or 256; 0 = automatic as in swz_gemm             */
   int cta_pair;      /* 1: 2-CTA clusters, tcgen05 cta_group::2, cluster tile
                         256 x tile_n (tile_n must be 256; each CTA owns
@@ -128,6 +137,8 @@ typedef struct swz_gemm_opts {
                         use; the library keeps it consistent afterwards.
                         Launches sharing a workspace must not overlap.       */
   uint64_t workspace_bytes; /* size of d_workspace                           */
+  int b_layout;      /* SWZ_B_KN (default): B is K x N row-major; SWZ_B_NK: B
+                        is stored transposed, N x K row-major (K contiguous)  */
   int split_tail;    /* persistent only, not with stream_k: when the R tiles
                         left for the last wave number at most half the
                         programs (clusters), split each into two halves of

@@ -24,7 +24,8 @@ SWZ_OK, SWZ_EINVAL, SWZ_ENOTBIJECTIVE, SWZ_EARCH, SWZ_ECUDA, SWZ_ETIMEOUT, SWZ_E
 SWZ_ESCRATCH = -7
 SWZ_NOALLOC_SCRATCH_BYTES = 24 * 1024 * 1024
 SWZ_ROW, SWZ_COL, SWZ_PANEL, SWZ_MORTON, SWZ_XOR, SWZ_SERPENTINE = range(6)
-SWZ_F16, SWZ_BF16 = 0, 1
+SWZ_F16, SWZ_BF16, SWZ_TF32 = 0, 1, 2
+SWZ_B_KN, SWZ_B_NK = 0, 1
 SWZ_SMEM_NAIVE, SWZ_SMEM_PADDED, SWZ_SMEM_XOR = 0, 1, 2
 SWZ_DEBUG_SKIP_FIRST_LOAD = 1
 ORDERS = {"row": SWZ_ROW, "col": SWZ_COL, "panel": SWZ_PANEL, "morton": SWZ_MORTON,
@@ -49,7 +50,8 @@ class swz_gemm_opts(ctypes.Structure):
                 ("num_programs", ctypes.c_int), ("d_trace", ctypes.c_void_p),
                 ("debug_flags", ctypes.c_uint32), ("timeout_ms", ctypes.c_uint32),
                 ("stream_k", ctypes.c_int), ("d_workspace", ctypes.c_void_p),
-                ("workspace_bytes", ctypes.c_uint64), ("split_tail", ctypes.c_int)]
+                ("workspace_bytes", ctypes.c_uint64), ("b_layout", ctypes.c_int),
+                ("split_tail", ctypes.c_int)]
 
 
 _lib = None
@@ -238,8 +240,10 @@ def tile_map(order, grid_m, grid_n, group=1, device="cuda", stream=None):
 
 
 def make_opts(dtype=SWZ_F16, tile_n=0, cta_pair=False, num_programs=0, trace=None,
-              debug_flags=0, timeout_ms=0, stream_k=False, workspace=None, split_tail=False):
+              debug_flags=0, timeout_ms=0, stream_k=False, workspace=None, split_tail=False,
+              b_layout=SWZ_B_KN):
     o = swz_gemm_opts()
+    o.b_layout = b_layout
     o.split_tail = 1 if split_tail else 0
     o.stream_k = 1 if stream_k else 0
     if workspace is not None:
@@ -273,25 +277,41 @@ def workspace_size(M, N, K, persistent=True, tile_n=0, cta_pair=False, num_progr
     return b
 
 
+def _dtype_code(t):
+    import torch
+    codes = {torch.float16: SWZ_F16, torch.bfloat16: SWZ_BF16, torch.float32: SWZ_TF32}
+    if t not in codes:
+        raise TypeError("A and B must be fp16, bf16 or fp32 (TF32)")
+    return codes[t]
+
+
 def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
          cta_pair=False, num_programs=0, trace=None, debug_flags=0, timeout_ms=0,
-         stream_k=False, workspace=None, split_tail=False, stream=None):
-    """C = A @ B (fp32) through swz_gemm_ex.  A: M x K, B: K x N, both fp16 or
-    both bf16, row-major contiguous CUDA tensors.  With stream_k, `workspace`
-    is a zero-initialised CUDA tensor of at least workspace_size(...) bytes."""
+         stream_k=False, workspace=None, split_tail=False, b_transposed=False, stream=None):
+    """C = A @ B (fp32) through swz_gemm_ex.  A: M x K; B: K x N, or N x K
+    when ``b_transposed`` (B stored transposed); both fp16, both bf16, or both
+    fp32 (multiplied as TF32); row-major contiguous CUDA tensors.  fp32 inputs
+    need B as N x K: a K x N fp32 B is first transposed on the device with
+    swz_transpose (one extra pass over B).  With stream_k, `workspace` is a
+    zero-initialised CUDA tensor of at least workspace_size(...) bytes."""
     import torch
-    if A.dtype != B.dtype or A.dtype not in (torch.float16, torch.bfloat16):
-        raise TypeError("A and B must both be fp16 or both bf16")
-    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[0]:
-        raise ValueError("A: M x K and B: K x N expected")
+    if A.dtype != B.dtype:
+        raise TypeError("A and B must have the same dtype")
+    code = _dtype_code(A.dtype)
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("2-D operands expected")
     if not (A.is_contiguous() and B.is_contiguous()):
         raise ValueError("row-major contiguous operands expected")
     M, K = A.shape
-    N = B.shape[1]
+    if code == SWZ_TF32 and not b_transposed:
+        B = transpose(B.view(torch.int32), "xor", stream=stream).view(torch.float32)
+        b_transposed = True
+    N = B.shape[0] if b_transposed else B.shape[1]
+    if (B.shape[1] if b_transposed else B.shape[0]) != K:
+        raise ValueError("inner dimensions differ")
     C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=A.device)
-    opts = make_opts(SWZ_BF16 if A.dtype == torch.bfloat16 else SWZ_F16, tile_n, cta_pair,
-                     num_programs, trace, debug_flags, timeout_ms, stream_k, workspace,
-                     split_tail)
+    opts = make_opts(code, tile_n, cta_pair, num_programs, trace, debug_flags, timeout_ms,
+                     stream_k, workspace, split_tail, SWZ_B_NK if b_transposed else SWZ_B_KN)
     _check(swz_gemm_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _order(order),
                        group, int(bool(persistent)), opts, _stream(stream)), "swz_gemm_ex")
     return C
@@ -299,21 +319,23 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
 
 def gemm_host(hA, hB, hC, dA, dB, dC, order="panel", group=8, *, tile_n=0, cta_pair=False,
               num_programs=0, stream_k=False, workspace=None, split_tail=False, slabs=0,
-              stream=None):
+              b_transposed=False, stream=None):
     """C = A @ B from host tensors through swz_gemm_host.  hA (M x K), hB
-    (K x N): CPU fp16/bf16 tensors (pinned for overlap); hC: CPU fp32 M x N;
+    (K x N, or N x K when ``b_transposed``; always N x K for fp32 / TF32): CPU
+    fp16/bf16/fp32 tensors (pinned for overlap); hC: CPU fp32 M x N;
     dA, dB, dC: CUDA tensors of the same shapes used as staging.  Asynchronous
     on `stream`; synchronise before reading hC."""
     import torch
     M, K = hA.shape
-    N = hB.shape[1]
+    N = hB.shape[0] if (b_transposed or hA.dtype == torch.float32) else hB.shape[1]
     for t, dev in ((hA, False), (hB, False), (hC, False), (dA, True), (dB, True), (dC, True)):
         if t.is_cuda != dev or not t.is_contiguous():
             raise ValueError("host tensors on the CPU, staging tensors on the GPU, contiguous")
-    if hA.dtype != hB.dtype or hA.dtype not in (torch.float16, torch.bfloat16):
-        raise TypeError("A and B must both be fp16 or both bf16")
-    opts = make_opts(SWZ_BF16 if hA.dtype == torch.bfloat16 else SWZ_F16, tile_n, cta_pair,
-                     num_programs, None, 0, 0, stream_k, workspace, split_tail)
+    if hA.dtype != hB.dtype:
+        raise TypeError("A and B must have the same dtype")
+    code = _dtype_code(hA.dtype)
+    opts = make_opts(code, tile_n, cta_pair, num_programs, None, 0, 0, stream_k, workspace,
+                     split_tail, SWZ_B_NK if (b_transposed or code == SWZ_TF32) else SWZ_B_KN)
     _check(swz_gemm_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K, _order(order),
                          group, opts, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), slabs,
                          _stream(stream)), "swz_gemm_host")

@@ -42,8 +42,12 @@ __device__ unsigned int g_status_word;  // nonzero: a bounded wait expired
 namespace gemm {
 
 constexpr int BM = 128;        // CTA tile rows = TMEM lanes
-constexpr int BK = 64;         // K elements per stage (one 128-byte swizzle row)
+constexpr int BK = 64;         // K elements per stage, 16-bit operands (128-byte rows)
 constexpr int UMMA_K = 16;     // K of one tcgen05.mma kind::f16
+// With 32-bit (TF32) operands a stage holds 32 K elements: the same 128-byte
+// rows, so every byte offset below is shared by both kinds.
+template <int KIND>
+constexpr int bk_elems() { return KIND == 0 ? 64 : 32; }
 constexpr int kThreads = 192;  // 6 warps
 constexpr int kSmemBudget = 200 * 1024;
 
@@ -70,12 +74,14 @@ struct Cfg {
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
-// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
-// A and B format (bits 7-9, 10-12: 0 fp16, 1 bf16), A K-major (bit 15 = 0),
-// B MN-major (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-__host__ __device__ constexpr uint32_t make_idesc(int dtype, int m, int n) {
-  return (1u << 4) | (uint32_t(dtype) << 7) | (uint32_t(dtype) << 10) | (1u << 16) |
-         (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+// Instruction descriptor of tcgen05.mma kind::f16 / kind::tf32: D fp32
+// (bits 4-5 = 1), A and B format (bits 7-9, 10-12: 0 fp16, 1 bf16, 2 tf32 --
+// the swz_dtype values), A K-major (bit 15 = 0), B MN-major (bit 16 = 1) or
+// K-major (0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+__host__ __device__ constexpr uint32_t make_idesc(int dtype, int m, int n, bool b_mn_major) {
+  return (1u << 4) | (uint32_t(dtype) << 7) | (uint32_t(dtype) << 10) |
+         (uint32_t(b_mn_major ? 1 : 0) << 16) | (uint32_t(n >> 3) << 17) |
+         (uint32_t(m >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor: start address >> 4 (bits 0-13), leading
@@ -96,6 +102,7 @@ struct Params {
   uint32_t idesc;       // full-width MMA (N = BN)
   uint32_t idesc_half;  // half-width MMA (N = BN/2) for split tail tiles
   uint32_t b3d;         // B's share of a full-width tile in one 3-D box (N % 64 == 0)
+  uint32_t b_kmajor;    // B given as N x K (K contiguous): K-major operand
   int32_t* trace;
   uint32_t debug_flags;
   uint64_t timeout_ns;
@@ -238,7 +245,7 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
   while (ptx::global_timer_ns() - t0 < ns) __nanosleep(1000);
 }
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmC,
@@ -328,14 +335,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             skip = false;
           } else {
             const uint32_t fb = PAIR ? ptx::map_to_rank(full_bar(stage), 0) : full_bar(stage);
-            const int32_t k0 = int32_t(kb * BK);
-            // B: one 3-D box (64 columns x 64 K rows x `boxes` column
-            // groups) when the map allows it, else one 2-D box per group;
-            // the shared-memory layout is the same either way
+            const int32_t k0 = int32_t(kb * bk_elems<KIND>());
+            // B, N-major (K x N given): one 3-D box (64 columns x 64 K rows x
+            // `boxes` column groups) when the map allows it, else one 2-D box
+            // per group; the shared-memory layout is the same either way.
+            // B, K-major (N x K given): one 2-D box of `local` rows of 128
+            // bytes (tmB: full width, tmB3: half width).
             const bool one_box = p.b3d && half < 0;
             if constexpr (PAIR) {
               ptx::tma_load_2d_pair(sA + stage * K_::A_BYTES, &tmA, fb, k0, m0);
-              if (one_box)
+              if (p.b_kmajor)
+                ptx::tma_load_2d_pair(sB + stage * K_::B_BYTES, half < 0 ? &tmB : &tmB3, fb, k0,
+                                      n0);
+              else if (one_box)
                 ptx::tma_load_3d_pair(sB + stage * K_::B_BYTES, &tmB3, fb, 0, k0, n0 / 64);
               else
                 for (int j = 0; j < boxes; ++j)
@@ -343,7 +355,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         fb, n0 + 64 * j, k0);
             } else {
               ptx::tma_load_2d(sA + stage * K_::A_BYTES, &tmA, fb, k0, m0);
-              if (one_box)
+              if (p.b_kmajor)
+                ptx::tma_load_2d(sB + stage * K_::B_BYTES, half < 0 ? &tmB : &tmB3, fb, k0, n0);
+              else if (one_box)
                 ptx::tma_load_3d(sB + stage * K_::B_BYTES, &tmB3, fb, 0, k0, n0 / 64);
               else
                 for (int j = 0; j < boxes; ++j)
@@ -387,12 +401,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // of 128 bytes further (+128); 8-row groups 1024 bytes apart along
           // K, 64-column boxes B_BOX_BYTES apart along N.  The address field
           // cannot carry: shared addresses are below 2^18 bytes.
+          // A K-major B (N x K given) is laid out and advanced like A.
           const uint64_t adesc = make_sdesc(a_addr, 16, 1024);
-          const uint64_t bdesc = make_sdesc(b_addr, K_::B_BOX_BYTES, 1024);
-          ptx::mma_f16<CL>(d, adesc, bdesc, idesc, kb != kbeg ? 1u : 0u);
+          const uint64_t bdesc = p.b_kmajor ? make_sdesc(b_addr, 16, 1024)
+                                            : make_sdesc(b_addr, K_::B_BOX_BYTES, 1024);
+          const uint64_t bstep = p.b_kmajor ? 2u : 128u;
+          ptx::mma<CL, KIND>(d, adesc, bdesc, idesc, kb != kbeg ? 1u : 0u);
 #pragma unroll
-          for (int kk = 1; kk < BK / UMMA_K; ++kk)
-            ptx::mma_f16<CL>(d, adesc + uint64_t(2 * kk), bdesc + uint64_t(128 * kk), idesc, 1u);
+          for (int kk = 1; kk < 4; ++kk)
+            ptx::mma<CL, KIND>(d, adesc + uint64_t(2 * kk), bdesc + bstep * uint64_t(kk), idesc,
+                               1u);
           issued = true;
           if constexpr (PAIR) ptx::mma_commit_pair(empty_bar(stage), 0x3);
           else ptx::mma_commit(empty_bar(stage));
@@ -581,12 +599,15 @@ static int encode_2d(CUtensorMap* map, int dtype, const void* base, uint64_t row
                      uint32_t box_cols, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cuda_fail(cudaErrorNotSupported);
-  const uint64_t esize = dtype == kMapF32 ? 4 : 2;
+  const uint64_t esize = (dtype == kMapF32 || dtype == SWZ_TF32) ? 4 : 2;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols * esize};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType t = dtype == kMapF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+  // TF32 operands are copied bit for bit (FLOAT32); the tensor core reads
+  // them as TF32
+  const CUtensorMapDataType t = (dtype == kMapF32 || dtype == SWZ_TF32)
+                                    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                 : dtype == SWZ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   const CUresult r = fn(map, t,
@@ -624,7 +645,7 @@ struct Plan {
   int programs;
 };
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, int KIND>
 static int kernel_capacity(const DeviceInfo& dev, int* programs) {
   using K_ = Cfg<BN, PAIR>;
   static std::mutex mu;
@@ -636,7 +657,7 @@ static int kernel_capacity(const DeviceInfo& dev, int* programs) {
       return SWZ_OK;
     }
   }
-  auto kern = gemm_kernel<BN, PAIR>;
+  auto kern = gemm_kernel<BN, PAIR, KIND>;
   SWZ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     K_::SMEM_BYTES));
   int cap = 0;
@@ -669,9 +690,11 @@ static int kernel_capacity(const DeviceInfo& dev, int* programs) {
 }
 
 static int capacity_for(const Plan& pl, const DeviceInfo& dev, int* cap) {
-  if (pl.pair) return kernel_capacity<256, true>(dev, cap);
-  if (pl.bn == 128) return kernel_capacity<128, false>(dev, cap);
-  return kernel_capacity<256, false>(dev, cap);
+  // the three configurations share their shared-memory footprint across
+  // kinds, so the f16 kernels' residency stands for both
+  if (pl.pair) return kernel_capacity<256, true, 0>(dev, cap);
+  if (pl.bn == 128) return kernel_capacity<128, false, 0>(dev, cap);
+  return kernel_capacity<256, false, 0>(dev, cap);
 }
 
 static int make_plan(int M, int N, int persistent, const swz_gemm_opts& o, const DeviceInfo* dev,
@@ -723,14 +746,14 @@ static SkLayout sk_layout(const Plan& pl, int persistent, const swz_gemm_opts& o
   return L;
 }
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, int KIND>
 static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
                   const CUtensorMap& tb3, const CUtensorMap& tc, const Params& prm,
                   cudaStream_t stream) {
   using K_ = Cfg<BN, PAIR>;
   static std::mutex mu;
   static bool attr_set[64] = {};
-  auto kern = gemm_kernel<BN, PAIR>;
+  auto kern = gemm_kernel<BN, PAIR, KIND>;
   int dev = 0;
   SWZ_CUDA_TRY(cudaGetDevice(&dev));
   {
@@ -770,12 +793,17 @@ static int validate(const void* A, const void* B, const float* C, int M, int N, 
   if (M < 0 || N < 0 || K < 0) return SWZ_EINVAL;
   if (!order_is_valid(order)) return SWZ_EINVAL;
   if (order_uses_group(order) && group < 1) return SWZ_EINVAL;
-  if (o.dtype != SWZ_F16 && o.dtype != SWZ_BF16) return SWZ_EINVAL;
+  if (o.dtype != SWZ_F16 && o.dtype != SWZ_BF16 && o.dtype != SWZ_TF32) return SWZ_EINVAL;
+  if (o.b_layout != SWZ_B_KN && o.b_layout != SWZ_B_NK) return SWZ_EINVAL;
   if (M == 0 || N == 0) return SWZ_OK;
-  if (!C || !aligned16(C)) return SWZ_EINVAL;
+  if (!C || !aligned16(C) || N % 4 != 0) return SWZ_EINVAL;
   if (K == 0) return SWZ_OK;
   if (!A || !B || !aligned16(A) || !aligned16(B)) return SWZ_EINVAL;
-  if (K % 8 != 0 || N % 8 != 0) return SWZ_EINVAL;
+  // rows of A (and of B given as N x K) and of B given as K x N must be
+  // multiples of 16 bytes for TMA
+  const int per16 = o.dtype == SWZ_TF32 ? 4 : 8;
+  if (K % per16 != 0) return SWZ_EINVAL;
+  if (o.b_layout == SWZ_B_KN && N % per16 != 0) return SWZ_EINVAL;
   return SWZ_OK;
 }
 
@@ -869,20 +897,34 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
       !order_is_bijective(order, pl.sched_m, pl.sched_n, g))
     return SWZ_ENOTBIJECTIVE;
 
+  // TF32 operands are taken K-major on both sides (B as N x K)
+  if (o.dtype == SWZ_TF32 && o.b_layout != SWZ_B_NK) return SWZ_EUNSUPPORTED;
+  const bool tf32 = o.dtype == SWZ_TF32;
+  const uint32_t bke = tf32 ? 32u : 64u;  // K elements per 128-byte stage row
+  const uint32_t local = uint32_t(pl.pair ? pl.bn / 2 : pl.bn);  // B columns per CTA
+  const bool b_kmajor = o.b_layout == SWZ_B_NK;
   CUtensorMap ta, tb, tb3, tc;
-  rc = encode_2d(&ta, o.dtype, A, uint64_t(M), uint64_t(K), BK, BM);
+  rc = encode_2d(&ta, o.dtype, A, uint64_t(M), uint64_t(K), bke, BM);
   if (rc != SWZ_OK) return rc;
-  rc = encode_2d(&tb, o.dtype, B, uint64_t(K), uint64_t(N), 64, BK);
-  if (rc != SWZ_OK) return rc;
-  // B as (64 columns, K rows, N/64 column groups): a CTA's whole share of a
-  // tile in one box.  Only when N % 64 == 0: a partial last group would read
-  // the next row's elements instead of zeros.
-  const bool b3d = (N % 64) == 0;
-  tb3 = tb;
-  if (b3d) {
-    rc = encode_b_groups(&tb3, o.dtype, B, uint64_t(K), uint64_t(N),
-                         uint32_t((pl.pair ? pl.bn / 2 : pl.bn) / 64));
+  bool b3d = false;
+  if (b_kmajor) {
+    // B given as N x K: like A, boxes of `local` (tb) or local/2 (tb3) rows
+    rc = encode_2d(&tb, o.dtype, B, uint64_t(N), uint64_t(K), bke, local);
     if (rc != SWZ_OK) return rc;
+    rc = encode_2d(&tb3, o.dtype, B, uint64_t(N), uint64_t(K), bke, local / 2);
+    if (rc != SWZ_OK) return rc;
+  } else {
+    rc = encode_2d(&tb, o.dtype, B, uint64_t(K), uint64_t(N), 64, BK);
+    if (rc != SWZ_OK) return rc;
+    // B as (64 columns, K rows, N/64 column groups): a CTA's whole share of
+    // a tile in one box.  Only when N % 64 == 0: a partial last group would
+    // read the next row's elements instead of zeros.
+    b3d = (N % 64) == 0;
+    tb3 = tb;
+    if (b3d) {
+      rc = encode_b_groups(&tb3, o.dtype, B, uint64_t(K), uint64_t(N), local / 64);
+      if (rc != SWZ_OK) return rc;
+    }
   }
   rc = encode_2d(&tc, kMapF32, C, uint64_t(M), uint64_t(N), 32, 32);
   if (rc != SWZ_OK) return rc;
@@ -896,9 +938,10 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   prm.group = int(g);
   prm.sched_m = pl.sched_m;
   prm.sched_n = pl.sched_n;
-  prm.num_kb = uint32_t((K + BK - 1) / BK);
-  prm.idesc = make_idesc(o.dtype, pl.pair ? 256 : 128, pl.bn);
-  prm.idesc_half = make_idesc(o.dtype, pl.pair ? 256 : 128, pl.bn / 2);
+  prm.num_kb = uint32_t((uint32_t(K) + bke - 1) / bke);
+  prm.idesc = make_idesc(o.dtype, pl.pair ? 256 : 128, pl.bn, !b_kmajor);
+  prm.idesc_half = make_idesc(o.dtype, pl.pair ? 256 : 128, pl.bn / 2, !b_kmajor);
+  prm.b_kmajor = b_kmajor ? 1u : 0u;
   if (o.split_tail) {
     if (!persistent || o.stream_k) return SWZ_EINVAL;
     prm.split_tail = 1;
@@ -930,9 +973,14 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   }
 
   prm.b3d = b3d ? 1u : 0u;
-  if (pl.pair) return launch<256, true>(pl, ta, tb, tb3, tc, prm, s);
-  if (pl.bn == 128) return launch<128, false>(pl, ta, tb, tb3, tc, prm, s);
-  return launch<256, false>(pl, ta, tb, tb3, tc, prm, s);
+  if (tf32) {
+    if (pl.pair) return launch<256, true, 1>(pl, ta, tb, tb3, tc, prm, s);
+    if (pl.bn == 128) return launch<128, false, 1>(pl, ta, tb, tb3, tc, prm, s);
+    return launch<256, false, 1>(pl, ta, tb, tb3, tc, prm, s);
+  }
+  if (pl.pair) return launch<256, true, 0>(pl, ta, tb, tb3, tc, prm, s);
+  if (pl.bn == 128) return launch<128, false, 0>(pl, ta, tb, tb3, tc, prm, s);
+  return launch<256, false, 0>(pl, ta, tb, tb3, tc, prm, s);
 }
 
 extern "C" int swz_gemm(const void* A, const void* B, float* C, int M, int N, int K, int order,

@@ -60,7 +60,12 @@ extern "C" int swz_gemm_host(const void* h_A, const void* h_B, float* h_C, int M
     return SWZ_EINVAL;
   swz_gemm_opts o = {};
   if (opts) o = *opts;
-  const size_t esize = 2;  // fp16 / bf16
+  if (o.dtype != SWZ_F16 && o.dtype != SWZ_BF16 && o.dtype != SWZ_TF32) return SWZ_EINVAL;
+  if (o.b_layout != SWZ_B_KN && o.b_layout != SWZ_B_NK) return SWZ_EINVAL;
+  if (o.dtype == SWZ_TF32 && o.b_layout != SWZ_B_NK) return SWZ_EUNSUPPORTED;
+  const size_t esize = o.dtype == SWZ_TF32 ? 4 : 2;  // fp32 (TF32) or fp16 / bf16
+  const int per16 = int(16 / esize);
+  if (N % 4 || (K > 0 && K % per16) || (o.b_layout == SWZ_B_KN && N % per16)) return SWZ_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   // slab rows: a multiple of 256 (one cluster tile of rows) when possible
