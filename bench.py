@@ -35,21 +35,30 @@ sys.path.insert(0, ROOT)
 METRIC = "GEMM TFLOP/s & % FP16 tensor peak per swizzle order; L2 hit rate vs model"
 # The configurations of the specification.  The default (timed headline) is
 # the 8192^3 bf16 CTA-pair one; the others are selectable with --workload.
+_ALL = [("row", 1), ("col", 1), ("panel", 2), ("panel", 4), ("panel", 8), ("panel", 16),
+        ("serpentine", 4), ("serpentine", 8), ("serpentine", 16), ("morton", 1), ("xor", 1)]
 WORKLOADS = {
+    # sweep: the orders each configuration of the specification names
     "gemm8192_bf16_pair": dict(M=8192, N=8192, K=8192, dtype="bf16", dist="normal",
-                               cfg=dict(cta_pair=True), tile=(128, 256), cluster_m=2),
+                               cfg=dict(cta_pair=True), tile=(128, 256), cluster_m=2,
+                               sweep=[o for o in _ALL if o != ("panel", 2)]),
     "gemm4096_fp16": dict(M=4096, N=4096, K=4096, dtype="fp16", dist="uniform",
-                          cfg=dict(tile_n=256), tile=(128, 256), cluster_m=1),
+                          cfg=dict(tile_n=256), tile=(128, 256), cluster_m=1, sweep=_ALL),
     "gemm4096_fp16_pair": dict(M=4096, N=4096, K=4096, dtype="fp16", dist="uniform",
-                               cfg=dict(cta_pair=True), tile=(128, 256), cluster_m=2),
+                               cfg=dict(cta_pair=True), tile=(128, 256), cluster_m=2,
+                               sweep=_ALL),
     "gemm6144x10240x4096_fp16": dict(M=6144, N=10240, K=4096, dtype="fp16", dist="uniform",
-                                     cfg=dict(tile_n=128), tile=(128, 128), cluster_m=1),
+                                     cfg=dict(tile_n=128), tile=(128, 128), cluster_m=1,
+                                     sweep=[("row", 1), ("col", 1), ("panel", 4), ("panel", 8),
+                                            ("panel", 16), ("serpentine", 4),
+                                            ("serpentine", 8), ("serpentine", 16)]),
     "gemm1024x1024x512_fp16": dict(M=1024, N=1024, K=512, dtype="fp16", dist="uniform",
-                                   cfg=dict(tile_n=128), tile=(128, 128), cluster_m=1),
+                                   cfg=dict(tile_n=128), tile=(128, 128), cluster_m=1,
+                                   sweep=[("row", 1), ("col", 1), ("panel", 4), ("morton", 1),
+                                          ("xor", 1), ("serpentine", 2)]),
 }
 HEADLINE = dict(order="serpentine", group=8, persistent=True)
-SWEEP = [("row", 1), ("col", 1), ("panel", 4), ("panel", 8), ("panel", 16),
-         ("serpentine", 4), ("serpentine", 8), ("serpentine", 16), ("morton", 1), ("xor", 1)]
+SWEEP = WORKLOADS["gemm8192_bf16_pair"]["sweep"]
 
 # DRAM traffic of one launch of the headline GEMM from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
@@ -310,15 +319,19 @@ def run_swz(args):
                 tdist.barrier()
         if args.only == "sweep":
             # one cold (L2-flushed) launch per order, for counter capture
-            for order, g in SWEEP:
+            for order, g in wl["sweep"]:
                 gemm_once(order, g)
             torch.cuda.synchronize()
-            for order, g in SWEEP:
+            for order, g in wl["sweep"]:
                 t = timed(lambda: gemm_once(order, g), 1, 0)
                 orders.append({"order": order, "group": g, "ms": t[0]})
         elif args.only == "all" and not args.no_sweep:
-            for order, g in SWEEP:
-                t = timed(lambda: gemm_once(order, g), max(5, args.steps // 4), 3)
+            for order, g in wl["sweep"]:
+                try:
+                    t = timed(lambda: gemm_once(order, g), max(5, args.steps // 4), 3)
+                except swz.SwzError as e:  # Morton / XOR on a grid they do not permute
+                    orders.append({"order": order, "group": g, "error": swz.strerror(e.code)})
+                    continue
                 med = statistics.median(t)
                 pred = swz.l2_model_hit_rate(order, g, M, N, K, wl["tile"][0], wl["tile"][1], 64,
                                              2, l2_bytes, programs, wl["cluster_m"])
@@ -327,7 +340,9 @@ def run_swz(args):
                                "pct_peak": 100.0 * flops / med / 1e9 / peaks["bf16_tflops"],
                                "l2_model_hit_pct": pred,
                                "l2_ncu_hit_pct": L2_NCU.get((order, g))
-                               if L2_NCU.get("gemm_cu_sha256") == _gemm_src_hash() else None})
+                               if (L2_NCU.get("gemm_cu_sha256") == _gemm_src_hash()
+                                   and args.workload == "gemm8192_bf16_pair"
+                                   and persistent and not args.stream_k) else None})
     clocks = sampler.summary()
 
     if ms is not None:
@@ -418,6 +433,51 @@ def run_swz(args):
                              "peak_source": "measured bf16 x nominal 1.1/2.25"}
         del A32, Bt32, C32
 
+    # ---- tensor-core rate of the library's own tcgen05 code (swz_tc_rate) ----
+    # FLOP per clock per SM from back-to-back MMAs on shared-memory operands;
+    # peaks = SMs x that x SM clock at the maximum clock, at the clock of a
+    # short run, and at the clock after about 2 s of full load.
+    if args.only in ("all", "tc_rate") and not args.no_tc_rate:
+        tc = {}
+        max_mhz = clocks.get("sm_max_mhz") or None
+        for name, dt, k_row in (("bf16", torch.bfloat16, 64), ("fp16", torch.float16, 64),
+                                ("tf32", torch.float32, 32)):
+            g = torch.Generator().manual_seed(0)
+            At = (torch.rand((128, k_row), generator=g) * 2 - 1).to(dt).to(dev)
+            Bt = (torch.rand((256, k_row), generator=g) * 2 - 1).to(dt).to(dev)
+            swz.tc_rate(At, Bt, 1024)  # warm-up
+            n_short = 16384
+            times, flop, _ = swz.tc_rate(At, Bt, n_short)
+            cyc, ns = times[:, 0].double(), times[:, 1].double()
+            fpc = float((n_short * flop / cyc).median())
+            burst_mhz = float((cyc / ns * 1e3).median())
+            rec = {"mma": f"128x256x{flop // (2 * 128 * 256)} {name}, one CTA per SM",
+                   "flop_per_clk_per_sm": fpc, "short_run_sm_mhz": burst_mhz,
+                   "peak_short_run_tflops": sms * fpc * burst_mhz / 1e6}
+            if max_mhz:
+                rec["sm_max_mhz"] = max_mhz
+                rec["peak_max_clock_tflops"] = sms * fpc * max_mhz / 1e6
+            if name != "fp16":
+                t_end = time.time() + 2.0
+                while True:
+                    times, _, _ = swz.tc_rate(At, Bt, 1 << 20)
+                    if time.time() >= t_end:
+                        break
+                cyc, ns = times[:, 0].double(), times[:, 1].double()
+                load_mhz = float((cyc / ns * 1e3).median())
+                rec["loaded_sm_mhz"] = load_mhz
+                rec["peak_loaded_tflops"] = sms * fpc * load_mhz / 1e6
+            tc[name] = rec
+            del At, Bt
+        if "roofline" in line and "peak_max_clock_tflops" in tc["bf16"]:
+            a = line["roofline"]["achieved"]
+            tc["headline_frac_of_bf16_max_clock_peak"] = a / tc["bf16"]["peak_max_clock_tflops"]
+            tc["headline_frac_of_bf16_loaded_peak"] = a / tc["bf16"]["peak_loaded_tflops"]
+        if "tf32_8192" in line:
+            line["tf32_8192"]["frac_of_tf32_loaded_peak"] = (
+                line["tf32_8192"]["tflops"] / tc["tf32"]["peak_loaded_tflops"])
+        line["tc_rate"] = tc
+
     # ---- ldmatrix / mma.sync path: operand layout vs bank conflicts ---------
     if do_mma_sync:
         mm = 4096
@@ -463,7 +523,9 @@ def main():
     ap.add_argument("--e2e-slabs", type=int, default=8, help="row slabs of the host pipeline")
     ap.add_argument("--no-mma-sync", action="store_true")
     ap.add_argument("--no-tf32", action="store_true")
-    ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose", "mma_sync"],
+    ap.add_argument("--no-tc-rate", action="store_true")
+    ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose", "mma_sync",
+                                       "tc_rate"],
                     default="all",
                     help="gemm: headline steps only; sweep: one cold launch per order; "
                          "transpose: the transposes only (profiling modes)")

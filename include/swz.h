@@ -293,6 +293,38 @@ int swz_gemm_streamk_noalloc(const void* A, const void* B, float* C, int M, int 
                              int order, int group, const swz_gemm_opts* opts,
                              void* stream);
 
+/*
+ * swz_tc_rate -- measures the dense tensor-core rate of this library's
+ * tcgen05 MMA code, for the roofline denominator.  No source page has a
+ * counterpart: the pages quote peak figures; this measures FLOP per SM clock.
+ *
+ * Launches num_ctas CTAs (0 = one per SM; at most the SM count, one CTA per
+ * SM).  Each copies A and B into shared memory (128-byte swizzle, as the
+ * GEMM stages its operands) and issues n_mma tcgen05.mma instructions of
+ * shape 128 x n x k (k = 16 for SWZ_F16 / SWZ_BF16, 8 for SWZ_TF32), the i-th
+ * on k-slice i % 4 of the operands, all accumulating into one fp32 TMEM
+ * accumulator (the first overwrites it).  One instruction is 2 * 128 * n * k
+ * FLOP; there is no global-memory traffic while it runs.
+ *   dtype   SWZ_F16, SWZ_BF16 or SWZ_TF32 (A and B of that type).
+ *   n       MMA N: 64, 128 or 256.
+ *   A       device, 128 rows x 128 bytes, row-major (64 fp16/bf16 or 32 fp32
+ *           per row): the 128 x 4k operand, K-major.
+ *   B       device, n rows x 128 bytes, row-major: B stored N x K.
+ *   n_mma   instructions per CTA, 1 .. 2^24.
+ *   d_times device, 4 * ctas uint64, written per CTA c at 4c: SM cycles from
+ *           the first issue to completion, globaltimer ns over the same span,
+ *           the SM id, and 0 (completed) or 1 (the bounded wait for
+ *           completion expired; the other fields are then not a rate).
+ *   d_D     device fp32 128 x n, or NULL: CTA 0's accumulator at the end;
+ *           with n_mma % 4 == 0 it is (n_mma / 4) * A * B^T (A, B as read
+ *           in the dtype; TF32 keeps 10 fraction bits of each fp32 operand).
+ * FLOP / clock / SM = n_mma * 2 * 128 * n * k / cycles.  Pointers 16-byte
+ * (A, B), 8-byte (d_times) and 4-byte (d_D) aligned.  Errors: SWZ_EINVAL,
+ * SWZ_EARCH, SWZ_ECUDA.
+ */
+int swz_tc_rate(int dtype, int n, const void* A, const void* B, int n_mma, int num_ctas,
+                uint64_t* d_times, float* d_D, void* stream);
+
 /* Synchronises `stream`, then returns and clears the current device's
  * status word: SWZ_OK, or SWZ_ETIMEOUT if a kernel's bounded wait expired
  * since the last check. */

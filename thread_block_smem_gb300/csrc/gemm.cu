@@ -43,7 +43,6 @@ namespace gemm {
 
 constexpr int BM = 128;        // CTA tile rows = TMEM lanes
 constexpr int BK = 64;         // K elements per stage, 16-bit operands (128-byte rows)
-constexpr int UMMA_K = 16;     // K of one tcgen05.mma kind::f16
 // With 32-bit (TF32) operands a stage holds 32 K elements: the same 128-byte
 // rows, so every byte offset below is shared by both kinds.
 template <int KIND>
