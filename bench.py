@@ -258,7 +258,7 @@ def run_swz(args):
     peaks, peak_src = _peaks()
     stream = torch.cuda.current_stream()
     flush = torch.empty(2 * max(l2_bytes, 64 << 20) // 4, dtype=torch.float32, device=dev)
-    do_gemm = args.only in ("all", "gemm", "sweep")
+    do_gemm = args.only in ("all", "gemm", "sweep", "swizzle")
     do_transpose = args.only in ("all", "transpose") and not args.no_transpose
     do_mma_sync = args.only in ("all", "mma_sync") and not args.no_mma_sync
 
@@ -284,9 +284,9 @@ def run_swz(args):
             nws = swz.workspace_size(M, N, K, persistent, **cfg)
             ws = torch.zeros(max(nws, 256), dtype=torch.uint8, device=dev)
 
-    def gemm_once(order, group):
+    def gemm_once(order, group, span=0):
         swz.gemm(Ad, Bd, order, group, persistent, out=C, stream_k=args.stream_k,
-                 workspace=ws, **cfg)
+                 workspace=ws, smem_swizzle=span, **cfg)
 
     def timed(fn, steps, warmup):
         for _ in range(warmup):
@@ -343,7 +343,21 @@ def run_swz(args):
                                if (L2_NCU.get("gemm_cu_sha256") == _gemm_src_hash()
                                    and args.workload == "gemm8192_bf16_pair"
                                    and persistent and not args.stream_k) else None})
+        # ---- operand-stage swizzle span (TMA + tensor-core layout) ---------
+        spans = []
+        if args.only == "swizzle":  # one cold launch per span, for counter capture
+            for sp in (128, 64, 32):
+                gemm_once(head_order, head_group, sp)
+            torch.cuda.synchronize()
+        elif args.only == "all" and not args.no_swizzle:
+            for sp in (128, 64, 32):
+                t = timed(lambda: gemm_once(head_order, head_group, sp), max(5, args.steps // 4),
+                          3)
+                med = statistics.median(t)
+                spans.append({"span_bytes": sp, "ms": med, "tflops": flops / med / 1e9})
     clocks = sampler.summary()
+    if spans:
+        line["smem_swizzle_spans"] = spans
 
     if ms is not None:
         ms_step = max_over_ranks(statistics.mean(ms), dev)
@@ -524,10 +538,12 @@ def main():
     ap.add_argument("--no-mma-sync", action="store_true")
     ap.add_argument("--no-tf32", action="store_true")
     ap.add_argument("--no-tc-rate", action="store_true")
+    ap.add_argument("--no-swizzle", action="store_true")
     ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose", "mma_sync",
-                                       "tc_rate"],
+                                       "tc_rate", "swizzle"],
                     default="all",
-                    help="gemm: headline steps only; sweep: one cold launch per order; "
+                    help="gemm: headline steps only; sweep / swizzle: one cold launch per "
+                         "order / operand swizzle span; "
                          "transpose: the transposes only (profiling modes)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps

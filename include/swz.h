@@ -145,6 +145,14 @@ typedef struct swz_gemm_opts {
                         tile_n / 2 columns so that 2R programs finish the last
                         wave in half the time; no workspace.  A split tile's
                         trace entry records one of its two halves.           */
+  int smem_swizzle;  /* span in bytes of the TMA / tensor-core shared-memory
+                        swizzle of the operand stages ([SBC] "Hopper TMA 的
+                        swizzling": the 16-byte chunk index of an address is
+                        XORed with the bits just above the span): 128
+                        (default when 0), 64 or 32.  Same results and stage
+                        bytes in every mode; with 64 and 32 a 128-byte row of
+                        a stage is split into 2 or 4 column groups of the
+                        span's width.  The C staging keeps the 128-byte span. */
 } swz_gemm_opts;
 
 /* debug_flags: withhold the first operand load so that the consumer's
@@ -157,7 +165,8 @@ typedef struct swz_gemm_opts {
  * errors: SWZ_EUNSUPPORTED for tile_n not in {0,128,256}, cta_pair with
  * tile_n != 256, or stream_k with more programs than can be resident at
  * once (its pieces wait on one another); SWZ_EINVAL for stream_k without
- * persistent or with a missing, misaligned (256 B) or too small workspace.
+ * persistent or with a missing, misaligned (256 B) or too small workspace,
+ * and for smem_swizzle not in {0, 32, 64, 128}.
  * In Stream-K mode the trace records, for a split tile, the program that
  * wrote it. */
 int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N, int K,

@@ -55,7 +55,6 @@ struct Cfg {
   static constexpr int CG = PAIR ? 2 : 1;
   static constexpr int BN_LOCAL = PAIR ? BN / 2 : BN;  // B columns this CTA loads
   static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BOX_BYTES = 64 * BK * 2;      // one 64-column B box
   static constexpr int B_BYTES = BK * BN_LOCAL * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = kSmemBudget / STAGE_BYTES;
@@ -85,11 +84,17 @@ __host__ __device__ constexpr uint32_t make_idesc(int dtype, int m, int n, bool 
 
 // Shared-memory matrix descriptor: start address >> 4 (bits 0-13), leading
 // byte offset >> 4 (16-29), stride byte offset >> 4 (32-45), the fixed
-// 0b001 at bits 46-48, base offset 0 (atoms are 1024-byte aligned), swizzle
-// mode 2 = 128-byte swizzle (bits 61-63).
-__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// 0b001 at bits 46-48, base offset 0 (atoms are aligned to their size), and
+// the layout type at bits 61-63: 2 = 128-byte swizzle, 4 = 64-byte, 6 =
+// 32-byte.
+__host__ __device__ constexpr uint32_t sw_layout_type(uint32_t span) {
+  return span == 128 ? 2u : span == 64 ? 4u : 6u;
+}
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                               uint32_t layout) {
   return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
-         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) |
+         (uint64_t(layout) << 61);
 }
 
 struct Params {
@@ -100,8 +105,9 @@ struct Params {
   uint32_t num_kb;            // ceil(K / BK)
   uint32_t idesc;       // full-width MMA (N = BN)
   uint32_t idesc_half;  // half-width MMA (N = BN/2) for split tail tiles
-  uint32_t b3d;         // B's share of a full-width tile in one 3-D box (N % 64 == 0)
+  uint32_t b3d;         // B's share of a full-width tile in one 3-D box (N % span == 0)
   uint32_t b_kmajor;    // B given as N x K (K contiguous): K-major operand
+  uint32_t a3d;         // A's stage in one 3-D box (span < 128 and K % span == 0)
   int32_t* trace;
   uint32_t debug_flags;
   uint64_t timeout_ns;
@@ -244,11 +250,11 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
   while (ptx::global_timer_ns() - t0 < ns) __nanosleep(1000);
 }
 
-template <int BN, bool PAIR, int KIND>
+template <int BN, bool PAIR, int KIND, int SW>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmC,
-                const __grid_constant__ Params p) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
+                const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3,
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Params p) {
   using K_ = Cfg<BN, PAIR>;
   constexpr int CL = K_::CG;
   constexpr int STAGES = K_::STAGES;
@@ -275,6 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::prefetch_tensormap(&tmA);
+    if constexpr (SW != 128) {
+      if (p.a3d) ptx::prefetch_tensormap(&tmA3);
+    }
     ptx::prefetch_tensormap(&tmB);
     if (p.b3d) ptx::prefetch_tensormap(&tmB3);
     ptx::prefetch_tensormap(&tmC);
@@ -319,14 +328,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool skip = (p.debug_flags & SWZ_DEBUG_SKIP_FIRST_LOAD) != 0;
       uint32_t w, kbeg, kend;
       int kind, half;
+      // Swizzle span sw: a stage's 128-byte rows are split into 128/sw
+      // column groups of sw bytes (xe elements), each a TMA box of its own
+      // (or one 3-D box for all of them); a group holds all rows of the
+      // operand block, so group g of a K-major block of R rows starts at
+      // g * R * sw.  B given as K x N: boxes of xn columns x BK K rows.
+      // The span is a template parameter: the 128-byte kernel carries none
+      // of the other spans' code (its issuing threads are latency-critical).
+      constexpr uint32_t sw = uint32_t(SW);
+      const int groups = int(128u / sw);
+      const int xe = int(sw) / (KIND == 0 ? 2 : 4);
+      const int xn = int(sw) / 2;
+      const uint32_t b_box_bytes = uint32_t(BK) * sw;
       for (uint32_t i = 0; !aborted && sch.item(i, w, kbeg, kend, kind, half); ++i) {
         const TileCoord t = tile_of(p.order, w, p.sched_m, p.sched_n, uint32_t(p.group));
         const int32_t m0 = int32_t((t.m * CL + rank) * BM);
         // B columns this CTA loads: its share of the tile (or of one half)
         const int local = half < 0 ? K_::BN_LOCAL : K_::BN_LOCAL / 2;
         const int32_t n0 = int32_t(t.n * BN + (half < 0 ? 0 : half * (BN / 2)) + rank * local);
-        const int boxes = local / 64;
-        const uint32_t tx = uint32_t(CL) * uint32_t(K_::A_BYTES + boxes * K_::B_BOX_BYTES);
+        const int boxes = local / xn;  // xn = 64 when sw == 128
+        const uint32_t tx = uint32_t(CL) * uint32_t(K_::A_BYTES + local * 128);
         for (uint32_t kb = kbeg; kb < kend; ++kb) {
           if (!wait(empty_bar(stage), phase ^ 1u, ctl)) { aborted = true; break; }
           if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), tx);
@@ -335,33 +356,65 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             const uint32_t fb = PAIR ? ptx::map_to_rank(full_bar(stage), 0) : full_bar(stage);
             const int32_t k0 = int32_t(kb * bk_elems<KIND>());
-            // B, N-major (K x N given): one 3-D box (64 columns x 64 K rows x
+            const uint32_t a_dst = sA + stage * K_::A_BYTES, b_dst = sB + stage * K_::B_BYTES;
+            // A: one box of 128 rows per column group, or one 3-D box
+            // (xe elements x 128 rows x groups) when the map allows it.
+            // B, N-major (K x N given): one 3-D box (xn columns x BK K rows x
             // `boxes` column groups) when the map allows it, else one 2-D box
             // per group; the shared-memory layout is the same either way.
-            // B, K-major (N x K given): one 2-D box of `local` rows of 128
-            // bytes (tmB: full width, tmB3: half width).
+            // B, K-major (N x K given): per column group one 2-D box of
+            // `local` rows (tmB: full width, tmB3: half width).
             const bool one_box = p.b3d && half < 0;
-            if constexpr (PAIR) {
-              ptx::tma_load_2d_pair(sA + stage * K_::A_BYTES, &tmA, fb, k0, m0);
+            if constexpr (SW == 128) {
+              if constexpr (PAIR) {
+                ptx::tma_load_2d_pair(a_dst, &tmA, fb, k0, m0);
+                if (p.b_kmajor)
+                  ptx::tma_load_2d_pair(b_dst, half < 0 ? &tmB : &tmB3, fb, k0, n0);
+                else if (one_box)
+                  ptx::tma_load_3d_pair(b_dst, &tmB3, fb, 0, k0, n0 / 64);
+                else
+                  for (int j = 0; j < boxes; ++j)
+                    ptx::tma_load_2d_pair(b_dst + j * (BK * 128), &tmB, fb, n0 + 64 * j, k0);
+              } else {
+                ptx::tma_load_2d(a_dst, &tmA, fb, k0, m0);
+                if (p.b_kmajor)
+                  ptx::tma_load_2d(b_dst, half < 0 ? &tmB : &tmB3, fb, k0, n0);
+                else if (one_box)
+                  ptx::tma_load_3d(b_dst, &tmB3, fb, 0, k0, n0 / 64);
+                else
+                  for (int j = 0; j < boxes; ++j)
+                    ptx::tma_load_2d(b_dst + j * (BK * 128), &tmB, fb, n0 + 64 * j, k0);
+              }
+            } else if constexpr (PAIR) {
+              if (p.a3d)
+                ptx::tma_load_3d_pair(a_dst, &tmA3, fb, 0, m0, k0 / xe);
+              else
+                for (int g = 0; g < groups; ++g)
+                  ptx::tma_load_2d_pair(a_dst + g * BM * sw, &tmA, fb, k0 + g * xe, m0);
               if (p.b_kmajor)
-                ptx::tma_load_2d_pair(sB + stage * K_::B_BYTES, half < 0 ? &tmB : &tmB3, fb, k0,
-                                      n0);
+                for (int g = 0; g < groups; ++g)
+                  ptx::tma_load_2d_pair(b_dst + g * local * sw, half < 0 ? &tmB : &tmB3, fb,
+                                        k0 + g * xe, n0);
               else if (one_box)
-                ptx::tma_load_3d_pair(sB + stage * K_::B_BYTES, &tmB3, fb, 0, k0, n0 / 64);
+                ptx::tma_load_3d_pair(b_dst, &tmB3, fb, 0, k0, n0 / xn);
               else
                 for (int j = 0; j < boxes; ++j)
-                  ptx::tma_load_2d_pair(sB + stage * K_::B_BYTES + j * K_::B_BOX_BYTES, &tmB,
-                                        fb, n0 + 64 * j, k0);
+                  ptx::tma_load_2d_pair(b_dst + j * b_box_bytes, &tmB, fb, n0 + xn * j, k0);
             } else {
-              ptx::tma_load_2d(sA + stage * K_::A_BYTES, &tmA, fb, k0, m0);
+              if (p.a3d)
+                ptx::tma_load_3d(a_dst, &tmA3, fb, 0, m0, k0 / xe);
+              else
+                for (int g = 0; g < groups; ++g)
+                  ptx::tma_load_2d(a_dst + g * BM * sw, &tmA, fb, k0 + g * xe, m0);
               if (p.b_kmajor)
-                ptx::tma_load_2d(sB + stage * K_::B_BYTES, half < 0 ? &tmB : &tmB3, fb, k0, n0);
+                for (int g = 0; g < groups; ++g)
+                  ptx::tma_load_2d(b_dst + g * local * sw, half < 0 ? &tmB : &tmB3, fb,
+                                   k0 + g * xe, n0);
               else if (one_box)
-                ptx::tma_load_3d(sB + stage * K_::B_BYTES, &tmB3, fb, 0, k0, n0 / 64);
+                ptx::tma_load_3d(b_dst, &tmB3, fb, 0, k0, n0 / xn);
               else
                 for (int j = 0; j < boxes; ++j)
-                  ptx::tma_load_2d(sB + stage * K_::B_BYTES + j * K_::B_BOX_BYTES, &tmB, fb,
-                                   n0 + 64 * j, k0);
+                  ptx::tma_load_2d(b_dst + j * b_box_bytes, &tmB, fb, n0 + xn * j, k0);
             }
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -384,32 +437,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool issued = false;
       uint32_t w, kbeg, kend;
       int kind, half;
+      // Operand layouts of a stage for swizzle span sw (see the producer).
+      // K-major block of R rows: 8-row groups 8*sw bytes apart (stride byte
+      // offset); MMA k-slice kk (32 bytes of each row) starts at column
+      // group kk*32/sw, byte (kk*32) % sw of the row: offset
+      // (kk*32/sw)*R*sw + (kk*32)%sw.  N-major B: boxes of xn columns
+      // BK*sw bytes apart along N (leading byte offset), 8 K-rows 8*sw apart
+      // (stride byte offset); slice kk starts 16 K-rows = 16*sw bytes in.
+      // Offsets are in the descriptor's 16-byte units; the address field
+      // cannot carry: shared addresses are below 2^18 bytes.
+      constexpr uint32_t sw = uint32_t(SW);
+      constexpr uint32_t lay = sw_layout_type(sw);
+      auto kmajor_off = [&](int kk, uint32_t rows) {
+        return uint64_t(((uint32_t(kk) * 32u / sw) * rows * sw + (uint32_t(kk) * 32u) % sw) >> 4);
+      };
       for (uint32_t i = 0; !aborted && sch.item(i, w, kbeg, kend, kind, half); ++i) {
         if (!wait(tempty_bar(acc), acc_phase ^ 1u, ctl)) { aborted = true; break; }
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
         const uint32_t idesc = half < 0 ? p.idesc : p.idesc_half;
+        const uint32_t b_rows = uint32_t(half < 0 ? K_::BN_LOCAL : K_::BN_LOCAL / 2);
+        uint64_t a_step[4] = {}, b_step[4] = {};
+        if constexpr (SW != 128) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            a_step[kk] = kmajor_off(kk, BM);
+            b_step[kk] = p.b_kmajor ? kmajor_off(kk, b_rows) : uint64_t((16u * sw * kk) >> 4);
+          }
+        }
         for (uint32_t kb = kbeg; kb < kend; ++kb) {
           if (!wait(full_bar(stage), phase, ctl)) { aborted = true; break; }
           ptx::tc_fence_after();
           const uint32_t a_addr = sA + stage * K_::A_BYTES;
           const uint32_t b_addr = sB + stage * K_::B_BYTES;
-          // A: K-major; each 16-element K slice starts 32 bytes further into
-          // each 128-byte row (+2 in the descriptor's address field); 8-row
-          // groups are 1024 bytes apart.  B: N-major; each slice is 16 K rows
-          // of 128 bytes further (+128); 8-row groups 1024 bytes apart along
-          // K, 64-column boxes B_BOX_BYTES apart along N.  The address field
-          // cannot carry: shared addresses are below 2^18 bytes.
-          // A K-major B (N x K given) is laid out and advanced like A.
-          const uint64_t adesc = make_sdesc(a_addr, 16, 1024);
-          const uint64_t bdesc = p.b_kmajor ? make_sdesc(b_addr, 16, 1024)
-                                            : make_sdesc(b_addr, K_::B_BOX_BYTES, 1024);
-          const uint64_t bstep = p.b_kmajor ? 2u : 128u;
-          ptx::mma<CL, KIND>(d, adesc, bdesc, idesc, kb != kbeg ? 1u : 0u);
+          if constexpr (SW == 128) {
+            const uint64_t adesc = make_sdesc(a_addr, 16, 1024, 2);
+            const uint64_t bdesc = p.b_kmajor ? make_sdesc(b_addr, 16, 1024, 2)
+                                              : make_sdesc(b_addr, BK * 128, 1024, 2);
+            const uint64_t bstep = p.b_kmajor ? 2u : 128u;
+            ptx::mma<CL, KIND>(d, adesc, bdesc, idesc, kb != kbeg ? 1u : 0u);
 #pragma unroll
-          for (int kk = 1; kk < 4; ++kk)
-            ptx::mma<CL, KIND>(d, adesc + uint64_t(2 * kk), bdesc + bstep * uint64_t(kk), idesc,
-                               1u);
+            for (int kk = 1; kk < 4; ++kk)
+              ptx::mma<CL, KIND>(d, adesc + uint64_t(2 * kk), bdesc + bstep * uint64_t(kk),
+                                 idesc, 1u);
+          } else {
+            const uint64_t adesc = make_sdesc(a_addr, 16, 8 * sw, lay);
+            const uint64_t bdesc = p.b_kmajor ? make_sdesc(b_addr, 16, 8 * sw, lay)
+                                              : make_sdesc(b_addr, BK * sw, 8 * sw, lay);
+            ptx::mma<CL, KIND>(d, adesc, bdesc, idesc, kb != kbeg ? 1u : 0u);
+#pragma unroll
+            for (int kk = 1; kk < 4; ++kk)
+              ptx::mma<CL, KIND>(d, adesc + a_step[kk], bdesc + b_step[kk], idesc, 1u);
+          }
           issued = true;
           if constexpr (PAIR) ptx::mma_commit_pair(empty_bar(stage), 0x3);
           else ptx::mma_commit(empty_bar(stage));
@@ -592,10 +671,25 @@ static EncodeTiledFn encode_fn() {
 // element type of a tensor map: the operands' fp16 / bf16, or fp32 for C
 constexpr int kMapF32 = 100;
 
-// 2-D row-major matrix rows x cols, box box_cols x box_rows, 128-byte swizzle;
-// out-of-bounds elements read as zero and are not written by stores.
+static CUtensorMapSwizzle tma_swizzle(uint32_t span) {
+  return span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+         : span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                      : CU_TENSOR_MAP_SWIZZLE_32B;
+}
+
+static CUtensorMapDataType tma_type(int dtype) {
+  // TF32 operands are copied bit for bit (FLOAT32); the tensor core reads
+  // them as TF32
+  return (dtype == kMapF32 || dtype == SWZ_TF32) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+         : dtype == SWZ_BF16                      ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+}
+
+// 2-D row-major matrix rows x cols, box box_cols x box_rows, swizzle span
+// `span` bytes (box_cols * element size must not exceed it); out-of-bounds
+// elements read as zero and are not written by stores.
 static int encode_2d(CUtensorMap* map, int dtype, const void* base, uint64_t rows, uint64_t cols,
-                     uint32_t box_cols, uint32_t box_rows) {
+                     uint32_t box_cols, uint32_t box_rows, uint32_t span = 128) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cuda_fail(cudaErrorNotSupported);
   const uint64_t esize = (dtype == kMapF32 || dtype == SWZ_TF32) ? 4 : 2;
@@ -603,36 +697,32 @@ static int encode_2d(CUtensorMap* map, int dtype, const void* base, uint64_t row
   const cuuint64_t strides[1] = {cols * esize};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  // TF32 operands are copied bit for bit (FLOAT32); the tensor core reads
-  // them as TF32
-  const CUtensorMapDataType t = (dtype == kMapF32 || dtype == SWZ_TF32)
-                                    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                : dtype == SWZ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                    : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const CUresult r = fn(map, t,
-                        2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUresult r = fn(map, tma_type(dtype), 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, tma_swizzle(span),
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
   return SWZ_OK;
 }
 
-// B (K x N row-major, N % 64 == 0) seen as a 3-D tensor (64 columns, K rows,
-// N/64 column groups); box 64 x 64 x `groups`, 128-byte swizzle.  In shared
-// memory the box is `groups` consecutive 64 x 64 blocks, as the 2-D boxes.
-static int encode_b_groups(CUtensorMap* map, int dtype, const void* base, uint64_t K, uint64_t N,
-                           uint32_t groups) {
+// A row-major rows x cols matrix (cols % gcols == 0) seen as a 3-D tensor
+// (gcols columns, rows, cols / gcols column groups); box gcols x box_rows x
+// box_groups, swizzle span `span` (= gcols * element size).  In shared
+// memory the box is box_groups consecutive box_rows x gcols blocks, the
+// layout of box_groups 2-D boxes side by side.  Only for cols % gcols == 0:
+// a partial last group would read the next row's elements instead of zeros.
+static int encode_groups(CUtensorMap* map, int dtype, const void* base, uint64_t rows,
+                         uint64_t cols, uint32_t gcols, uint32_t box_rows, uint32_t box_groups,
+                         uint32_t span) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cuda_fail(cudaErrorNotSupported);
-  const cuuint64_t dims[3] = {64, K, N / 64};
-  const cuuint64_t strides[2] = {N * 2, 128};
-  const cuuint32_t box[3] = {64, uint32_t(BK), groups};
+  const uint64_t esize = (dtype == kMapF32 || dtype == SWZ_TF32) ? 4 : 2;
+  const cuuint64_t dims[3] = {gcols, rows, cols / gcols};
+  const cuuint64_t strides[2] = {cols * esize, gcols * esize};
+  const cuuint32_t box[3] = {gcols, box_rows, box_groups};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r =
-      fn(map, dtype == SWZ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-         3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = fn(map, tma_type(dtype), 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, tma_swizzle(span),
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
   return SWZ_OK;
 }
@@ -646,6 +736,7 @@ struct Plan {
 
 template <int BN, bool PAIR, int KIND>
 static int kernel_capacity(const DeviceInfo& dev, int* programs) {
+  constexpr int SW = 128;
   using K_ = Cfg<BN, PAIR>;
   static std::mutex mu;
   static int cache[64] = {};
@@ -656,7 +747,7 @@ static int kernel_capacity(const DeviceInfo& dev, int* programs) {
       return SWZ_OK;
     }
   }
-  auto kern = gemm_kernel<BN, PAIR, KIND>;
+  auto kern = gemm_kernel<BN, PAIR, KIND, SW>;
   SWZ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     K_::SMEM_BYTES));
   int cap = 0;
@@ -745,14 +836,14 @@ static SkLayout sk_layout(const Plan& pl, int persistent, const swz_gemm_opts& o
   return L;
 }
 
-template <int BN, bool PAIR, int KIND>
-static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
-                  const CUtensorMap& tb3, const CUtensorMap& tc, const Params& prm,
-                  cudaStream_t stream) {
+template <int BN, bool PAIR, int KIND, int SW>
+static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& ta3,
+                  const CUtensorMap& tb, const CUtensorMap& tb3, const CUtensorMap& tc,
+                  const Params& prm, cudaStream_t stream) {
   using K_ = Cfg<BN, PAIR>;
   static std::mutex mu;
   static bool attr_set[64] = {};
-  auto kern = gemm_kernel<BN, PAIR, KIND>;
+  auto kern = gemm_kernel<BN, PAIR, KIND, SW>;
   int dev = 0;
   SWZ_CUDA_TRY(cudaGetDevice(&dev));
   {
@@ -777,7 +868,7 @@ static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  SWZ_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ta, tb, tb3, tc, prm));
+  SWZ_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ta, ta3, tb, tb3, tc, prm));
   return SWZ_OK;
 }
 
@@ -787,6 +878,21 @@ static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& tb,
 using namespace swz;
 using namespace swz::gemm;
 
+// kernel instance for the plan's tile shape, the operand kind and span SW
+template <int SW>
+static int dispatch(const Plan& pl, bool tf32, const CUtensorMap& ta, const CUtensorMap& ta3,
+                    const CUtensorMap& tb, const CUtensorMap& tb3, const CUtensorMap& tc,
+                    const Params& prm, cudaStream_t s) {
+  if (tf32) {
+    if (pl.pair) return launch<256, true, 1, SW>(pl, ta, ta3, tb, tb3, tc, prm, s);
+    if (pl.bn == 128) return launch<128, false, 1, SW>(pl, ta, ta3, tb, tb3, tc, prm, s);
+    return launch<256, false, 1, SW>(pl, ta, ta3, tb, tb3, tc, prm, s);
+  }
+  if (pl.pair) return launch<256, true, 0, SW>(pl, ta, ta3, tb, tb3, tc, prm, s);
+  if (pl.bn == 128) return launch<128, false, 0, SW>(pl, ta, ta3, tb, tb3, tc, prm, s);
+  return launch<256, false, 0, SW>(pl, ta, ta3, tb, tb3, tc, prm, s);
+}
+
 static int validate(const void* A, const void* B, const float* C, int M, int N, int K, int order,
                     int group, const swz_gemm_opts& o) {
   if (M < 0 || N < 0 || K < 0) return SWZ_EINVAL;
@@ -794,6 +900,9 @@ static int validate(const void* A, const void* B, const float* C, int M, int N, 
   if (order_uses_group(order) && group < 1) return SWZ_EINVAL;
   if (o.dtype != SWZ_F16 && o.dtype != SWZ_BF16 && o.dtype != SWZ_TF32) return SWZ_EINVAL;
   if (o.b_layout != SWZ_B_KN && o.b_layout != SWZ_B_NK) return SWZ_EINVAL;
+  if (o.smem_swizzle != 0 && o.smem_swizzle != 32 && o.smem_swizzle != 64 &&
+      o.smem_swizzle != 128)
+    return SWZ_EINVAL;
   if (M == 0 || N == 0) return SWZ_OK;
   if (!C || !aligned16(C) || N % 4 != 0) return SWZ_EINVAL;
   if (K == 0) return SWZ_OK;
@@ -899,29 +1008,40 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   // TF32 operands are taken K-major on both sides (B as N x K)
   if (o.dtype == SWZ_TF32 && o.b_layout != SWZ_B_NK) return SWZ_EUNSUPPORTED;
   const bool tf32 = o.dtype == SWZ_TF32;
-  const uint32_t bke = tf32 ? 32u : 64u;  // K elements per 128-byte stage row
+  const uint32_t span = o.smem_swizzle ? uint32_t(o.smem_swizzle) : 128u;
+  const uint32_t esize = tf32 ? 4u : 2u;
+  const uint32_t bke = 128u / esize;  // K elements per 128-byte stage row
+  const uint32_t xe = span / esize;   // elements per swizzle span
   const uint32_t local = uint32_t(pl.pair ? pl.bn / 2 : pl.bn);  // B columns per CTA
   const bool b_kmajor = o.b_layout == SWZ_B_NK;
-  CUtensorMap ta, tb, tb3, tc;
-  rc = encode_2d(&ta, o.dtype, A, uint64_t(M), uint64_t(K), bke, BM);
+  CUtensorMap ta, ta3, tb, tb3, tc;
+  // A: boxes of xe elements x 128 rows, one per span-wide column group of a
+  // stage; with span < 128 and K % xe == 0, all groups in one 3-D box
+  rc = encode_2d(&ta, o.dtype, A, uint64_t(M), uint64_t(K), xe, BM, span);
   if (rc != SWZ_OK) return rc;
+  const bool a3d = span < 128 && uint32_t(K) % xe == 0;
+  ta3 = ta;
+  if (a3d) {
+    rc = encode_groups(&ta3, o.dtype, A, uint64_t(M), uint64_t(K), xe, BM, 128 / span, span);
+    if (rc != SWZ_OK) return rc;
+  }
   bool b3d = false;
   if (b_kmajor) {
     // B given as N x K: like A, boxes of `local` (tb) or local/2 (tb3) rows
-    rc = encode_2d(&tb, o.dtype, B, uint64_t(N), uint64_t(K), bke, local);
+    rc = encode_2d(&tb, o.dtype, B, uint64_t(N), uint64_t(K), xe, local, span);
     if (rc != SWZ_OK) return rc;
-    rc = encode_2d(&tb3, o.dtype, B, uint64_t(N), uint64_t(K), bke, local / 2);
+    rc = encode_2d(&tb3, o.dtype, B, uint64_t(N), uint64_t(K), xe, local / 2, span);
     if (rc != SWZ_OK) return rc;
   } else {
-    rc = encode_2d(&tb, o.dtype, B, uint64_t(K), uint64_t(N), 64, BK);
+    const uint32_t xn = span / 2;  // B columns per span (16-bit elements)
+    rc = encode_2d(&tb, o.dtype, B, uint64_t(K), uint64_t(N), xn, BK, span);
     if (rc != SWZ_OK) return rc;
-    // B as (64 columns, K rows, N/64 column groups): a CTA's whole share of
-    // a tile in one box.  Only when N % 64 == 0: a partial last group would
-    // read the next row's elements instead of zeros.
-    b3d = (N % 64) == 0;
+    // B as (xn columns, K rows, N/xn column groups): a CTA's whole share of
+    // a tile in one box, when N % xn == 0
+    b3d = uint32_t(N) % xn == 0;
     tb3 = tb;
     if (b3d) {
-      rc = encode_b_groups(&tb3, o.dtype, B, uint64_t(K), uint64_t(N), local / 64);
+      rc = encode_groups(&tb3, o.dtype, B, uint64_t(K), uint64_t(N), xn, BK, local / xn, span);
       if (rc != SWZ_OK) return rc;
     }
   }
@@ -941,6 +1061,7 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   prm.idesc = make_idesc(o.dtype, pl.pair ? 256 : 128, pl.bn, !b_kmajor);
   prm.idesc_half = make_idesc(o.dtype, pl.pair ? 256 : 128, pl.bn / 2, !b_kmajor);
   prm.b_kmajor = b_kmajor ? 1u : 0u;
+  prm.a3d = a3d ? 1u : 0u;
   if (o.split_tail) {
     if (!persistent || o.stream_k) return SWZ_EINVAL;
     prm.split_tail = 1;
@@ -972,14 +1093,9 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   }
 
   prm.b3d = b3d ? 1u : 0u;
-  if (tf32) {
-    if (pl.pair) return launch<256, true, 1>(pl, ta, tb, tb3, tc, prm, s);
-    if (pl.bn == 128) return launch<128, false, 1>(pl, ta, tb, tb3, tc, prm, s);
-    return launch<256, false, 1>(pl, ta, tb, tb3, tc, prm, s);
-  }
-  if (pl.pair) return launch<256, true, 0>(pl, ta, tb, tb3, tc, prm, s);
-  if (pl.bn == 128) return launch<128, false, 0>(pl, ta, tb, tb3, tc, prm, s);
-  return launch<256, false, 0>(pl, ta, tb, tb3, tc, prm, s);
+  if (span == 64) return dispatch<64>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
+  if (span == 32) return dispatch<32>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
+  return dispatch<128>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
 }
 
 extern "C" int swz_gemm(const void* A, const void* B, float* C, int M, int N, int K, int order,
