@@ -355,9 +355,20 @@ def run_swz(args):
                           3)
                 med = statistics.median(t)
                 spans.append({"span_bytes": sp, "ms": med, "tflops": flops / med / 1e9})
+        # ---- static (work_idx striding) vs dynamic (atomic counter) -------
+        sched = {}
+        if args.only == "all" and not args.no_dynamic and persistent and not args.stream_k:
+            dws = torch.zeros(256, dtype=torch.uint8, device=dev)
+            for name, kw in (("static", {}), ("dynamic", dict(dynamic=True, workspace=dws))):
+                fn = lambda: swz.gemm(Ad, Bd, head_order, head_group, True, out=C, **kw, **cfg)
+                t = timed(fn, max(5, args.steps // 4), 3)
+                sched[name] = {"ms": statistics.median(t),
+                               "tflops": flops / statistics.median(t) / 1e9}
     clocks = sampler.summary()
     if spans:
         line["smem_swizzle_spans"] = spans
+    if sched:
+        line["scheduler"] = sched
 
     if ms is not None:
         ms_step = max_over_ranks(statistics.mean(ms), dev)
@@ -539,6 +550,7 @@ def main():
     ap.add_argument("--no-tf32", action="store_true")
     ap.add_argument("--no-tc-rate", action="store_true")
     ap.add_argument("--no-swizzle", action="store_true")
+    ap.add_argument("--no-dynamic", action="store_true")
     ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose", "mma_sync",
                                        "tc_rate", "swizzle"],
                     default="all",

@@ -153,6 +153,17 @@ typedef struct swz_gemm_opts {
                         bytes in every mode; with 64 and 32 a 128-byte row of
                         a stage is split into 2 or 4 column groups of the
                         span's width.  The C staging keeps the 128-byte span. */
+  int dynamic;       /* persistent only, not with stream_k or split_tail, span
+                        128 only: tiles are claimed at run time instead of
+                        dealt out by work_idx striding.  Program c takes work
+                        index c first, then P + the value of an atomic counter
+                        it increments (P = programs, or clusters with
+                        cta_pair), until the indices run out; each index goes
+                        through the tile order as usual.  The counter lives at
+                        the start of d_workspace (256-byte aligned, at least
+                        swz_gemm_workspace_size bytes = 256) and is cleared on
+                        `stream` before the launch; launches sharing a
+                        workspace must not overlap.                          */
 } swz_gemm_opts;
 
 /* debug_flags: withhold the first operand load so that the consumer's
@@ -166,7 +177,9 @@ typedef struct swz_gemm_opts {
  * tile_n != 256, or stream_k with more programs than can be resident at
  * once (its pieces wait on one another); SWZ_EINVAL for stream_k without
  * persistent or with a missing, misaligned (256 B) or too small workspace,
- * and for smem_swizzle not in {0, 32, 64, 128}.
+ * and for smem_swizzle not in {0, 32, 64, 128}; for dynamic the same
+ * workspace rules, SWZ_EINVAL without persistent or with stream_k or
+ * split_tail, SWZ_EUNSUPPORTED with a span other than 128.
  * In Stream-K mode the trace records, for a split tile, the program that
  * wrote it. */
 int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N, int K,

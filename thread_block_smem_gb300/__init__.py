@@ -51,7 +51,8 @@ class swz_gemm_opts(ctypes.Structure):
                 ("debug_flags", ctypes.c_uint32), ("timeout_ms", ctypes.c_uint32),
                 ("stream_k", ctypes.c_int), ("d_workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_uint64), ("b_layout", ctypes.c_int),
-                ("split_tail", ctypes.c_int), ("smem_swizzle", ctypes.c_int)]
+                ("split_tail", ctypes.c_int), ("smem_swizzle", ctypes.c_int),
+                ("dynamic", ctypes.c_int)]
 
 
 _lib = None
@@ -270,9 +271,10 @@ def tile_map(order, grid_m, grid_n, group=1, device="cuda", stream=None):
 
 def make_opts(dtype=SWZ_F16, tile_n=0, cta_pair=False, num_programs=0, trace=None,
               debug_flags=0, timeout_ms=0, stream_k=False, workspace=None, split_tail=False,
-              b_layout=SWZ_B_KN, smem_swizzle=0):
+              b_layout=SWZ_B_KN, smem_swizzle=0, dynamic=False):
     o = swz_gemm_opts()
     o.smem_swizzle = smem_swizzle
+    o.dynamic = 1 if dynamic else 0
     o.b_layout = b_layout
     o.split_tail = 1 if split_tail else 0
     o.stream_k = 1 if stream_k else 0
@@ -298,11 +300,14 @@ def gemm_plan(M, N, K, persistent=False, tile_n=0, cta_pair=False, num_programs=
 
 
 def workspace_size(M, N, K, persistent=True, tile_n=0, cta_pair=False, num_programs=0,
-                   stream_k=True):
-    """Bytes of workspace a Stream-K launch of this shape needs (0 if none)."""
+                   stream_k=True, dynamic=False):
+    """Bytes of workspace a Stream-K (or, with dynamic=True and
+    stream_k=False, a dynamic-scheduler) launch of this shape needs (0 if
+    none)."""
     rc, b = swz_gemm_workspace_size(M, N, K, int(bool(persistent)),
                                     make_opts(tile_n=tile_n, cta_pair=cta_pair,
-                                              num_programs=num_programs, stream_k=stream_k))
+                                              num_programs=num_programs, stream_k=stream_k,
+                                              dynamic=dynamic))
     _check(rc, "swz_gemm_workspace_size")
     return b
 
@@ -318,14 +323,17 @@ def _dtype_code(t):
 def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
          cta_pair=False, num_programs=0, trace=None, debug_flags=0, timeout_ms=0,
          stream_k=False, workspace=None, split_tail=False, b_transposed=False, smem_swizzle=0,
-         stream=None):
+         dynamic=False, stream=None):
     """C = A @ B (fp32) through swz_gemm_ex.  A: M x K; B: K x N, or N x K
     when ``b_transposed`` (B stored transposed); both fp16, both bf16, or both
     fp32 (multiplied as TF32); row-major contiguous CUDA tensors.  fp32 inputs
     need B as N x K: a K x N fp32 B is first transposed on the device with
     swz_transpose (one extra pass over B).  With stream_k, `workspace` is a
     zero-initialised CUDA tensor of at least workspace_size(...) bytes.
-    ``smem_swizzle``: swizzle span of the operand stages, 128 (0), 64 or 32."""
+    ``smem_swizzle``: swizzle span of the operand stages, 128 (0), 64 or 32.
+    ``dynamic``: claim tiles at run time through an atomic counter kept in
+    ``workspace`` (a CUDA tensor of at least workspace_size(..., dynamic=True)
+    bytes); persistent launches only."""
     import torch
     if A.dtype != B.dtype:
         raise TypeError("A and B must have the same dtype")
@@ -344,7 +352,7 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
     C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=A.device)
     opts = make_opts(code, tile_n, cta_pair, num_programs, trace, debug_flags, timeout_ms,
                      stream_k, workspace, split_tail, SWZ_B_NK if b_transposed else SWZ_B_KN,
-                     smem_swizzle)
+                     smem_swizzle, dynamic)
     _check(swz_gemm_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _order(order),
                        group, int(bool(persistent)), opts, _stream(stream)), "swz_gemm_ex")
     return C

@@ -49,6 +49,8 @@ template <int KIND>
 constexpr int bk_elems() { return KIND == 0 ? 64 : 32; }
 constexpr int kThreads = 192;  // 6 warps
 constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSchedDepth = 4;            // slots of the dynamic scheduler's ring
+constexpr uint32_t kNoWork = 0xFFFFFFFFu;  // ring entry: no more work
 
 template <int BN, bool PAIR>
 struct Cfg {
@@ -65,7 +67,9 @@ struct Cfg {
   // rows, 128-byte swizzle), written from registers and stored by TMA
   static constexpr int STG_BOX_BYTES = 32 * 32 * 4;
   static constexpr int STG_BYTES = 4 * 2 * STG_BOX_BYTES;
-  static constexpr int BAR_BYTES = (2 * STAGES + 5) * 8 + 16;
+  // stage full/empty, accumulator full/empty, drain, scheduler ring
+  // full/empty barriers; TMEM address, abort flag; the ring's work indices
+  static constexpr int BAR_BYTES = (2 * STAGES + 5 + 2 * kSchedDepth) * 8 + 8 + 4 * kSchedDepth;
   static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STG_BYTES + BAR_BYTES;
   static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "1024-byte swizzle atoms");
   static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation size");
@@ -117,6 +121,7 @@ struct Params {
   uint32_t epoch;      // value a finished partial's flag takes in this launch
   uint32_t* sk_flags;  // [cluster][rank][lane quarter]
   float4* sk_ws;       // [cluster][rank][BN/4 column groups][128 rows] float4
+  uint32_t* dyn_counter;  // dynamic scheduler: work indices claimed beyond the first wave
 };
 
 enum ItemKind : int { kWhole = 0, kFirst = 1, kPartial = 2 };
@@ -250,7 +255,7 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
   while (ptx::global_timer_ns() - t0 < ns) __nanosleep(1000);
 }
 
-template <int BN, bool PAIR, int KIND, int SW>
+template <int BN, bool PAIR, int KIND, int SW, bool DYN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3,
@@ -272,8 +277,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  auto sfull_bar = [&](uint32_t s) { return bar0 + 8u * (2 * STAGES + 5 + s); };
+  auto sempty_bar = [&](uint32_t s) { return bar0 + 8u * (2 * STAGES + 5 + kSchedDepth + s); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5 + 2 * kSchedDepth);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile uint32_t* ring_w = tmem_slot + 2;
 
   const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
@@ -296,6 +304,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(tempty_bar(a), PAIR ? 8 : 4);
     }
     ptx::mbar_init(drain_bar, 1);
+    if constexpr (DYN) {
+      // a slot is refilled once every reader has taken it: the MMA issuer
+      // and the 4 epilogue warps of the leader, plus (pair) the peer's
+      // producer and 4 epilogue warps
+      for (uint32_t r = 0; r < uint32_t(kSchedDepth); ++r) {
+        ptx::mbar_init(sfull_bar(r), 1);
+        ptx::mbar_init(sempty_bar(r), PAIR ? 10 : 5);
+      }
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -321,6 +338,75 @@ __global__ void __launch_bounds__(kThreads, 1)
            p.split_tail != 0);
   bool aborted = false;
 
+  // Dynamic scheduler (DYN): the producer of the leader CTA claims work
+  // indices -- its cluster id first, then P + the value of a global counter
+  // it increments atomically -- and publishes each in a ring of
+  // kSchedDepth shared-memory slots (also written into the peer CTA of a
+  // pair); the MMA issuer, the epilogue warps and the peer's producer read
+  // the same sequence from the ring.  kNoWork ends it.  Work items are whole
+  // tiles.  next_item gives a role's i-th item: the static schedule, or the
+  // ring (`fetch`: this thread claims and publishes).
+  auto ring_put = [&](uint32_t i, uint32_t w) -> bool {
+    const uint32_t slot = i % uint32_t(kSchedDepth);
+    if (!wait(sempty_bar(slot), ((i / uint32_t(kSchedDepth)) & 1u) ^ 1u, ctl)) return false;
+    ring_w[slot] = w;
+    if constexpr (PAIR) {
+      const uint32_t rw =
+          ptx::map_to_rank(ptx::smem_u32(const_cast<uint32_t*>(ring_w + slot)), 1);
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(rw), "r"(w) : "memory");
+      ptx::mbar_arrive_cluster(ptx::map_to_rank(sfull_bar(slot), 1));
+    }
+    ptx::mbar_arrive(sfull_bar(slot));
+    return true;
+  };
+  auto ring_take = [&](uint32_t i, uint32_t& w) -> bool {
+    const uint32_t slot = i % uint32_t(kSchedDepth);
+    if (!wait(sfull_bar(slot), (i / uint32_t(kSchedDepth)) & 1u, ctl)) return false;
+    w = ring_w[slot];
+    if (leader) ptx::mbar_arrive(sempty_bar(slot));
+    else ptx::mbar_arrive_cluster(ptx::map_to_rank(sempty_bar(slot), 0));
+    return true;
+  };
+  auto next_item = [&](uint32_t i, bool fetch, uint32_t& w, uint32_t& kbeg, uint32_t& kend,
+                       int& kind, int& half) -> bool {
+    if constexpr (!DYN) {
+      return sch.item(i, w, kbeg, kend, kind, half);
+    } else {
+      kbeg = 0;
+      kend = p.num_kb;
+      kind = kWhole;
+      half = -1;
+      if (fetch) {
+        w = i == 0 ? sch.c : sch.P + atomicAdd(p.dyn_counter, 1u);
+        if (w >= units) w = kNoWork;
+        if (!ring_put(i, w)) { aborted = true; return false; }
+      } else if (!ring_take(i, w)) {
+        aborted = true;
+        return false;
+      }
+      return w != kNoWork;
+    }
+  };
+  // warp-wide form for the epilogue warps: lane 0 reads the ring
+  auto next_item_warp = [&](uint32_t i, uint32_t& w, uint32_t& kbeg, uint32_t& kend, int& kind,
+                            int& half) -> bool {
+    if constexpr (!DYN) {
+      return sch.item(i, w, kbeg, kend, kind, half);
+    } else {
+      uint32_t wl = 0;
+      int ok = 1;
+      if (lane == 0) ok = ring_take(i, wl) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      w = __shfl_sync(0xFFFFFFFFu, wl, 0);
+      kbeg = 0;
+      kend = p.num_kb;
+      kind = kWhole;
+      half = -1;
+      if (!ok) { aborted = true; return false; }
+      return w != kNoWork;
+    }
+  };
+
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
@@ -340,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int xe = int(sw) / (KIND == 0 ? 2 : 4);
       const int xn = int(sw) / 2;
       const uint32_t b_box_bytes = uint32_t(BK) * sw;
-      for (uint32_t i = 0; !aborted && sch.item(i, w, kbeg, kend, kind, half); ++i) {
+      for (uint32_t i = 0; !aborted && next_item(i, leader, w, kbeg, kend, kind, half); ++i) {
         const TileCoord t = tile_of(p.order, w, p.sched_m, p.sched_n, uint32_t(p.group));
         const int32_t m0 = int32_t((t.m * CL + rank) * BM);
         // B columns this CTA loads: its share of the tile (or of one half)
@@ -451,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto kmajor_off = [&](int kk, uint32_t rows) {
         return uint64_t(((uint32_t(kk) * 32u / sw) * rows * sw + (uint32_t(kk) * 32u) % sw) >> 4);
       };
-      for (uint32_t i = 0; !aborted && sch.item(i, w, kbeg, kend, kind, half); ++i) {
+      for (uint32_t i = 0; !aborted && next_item(i, false, w, kbeg, kend, kind, half); ++i) {
         if (!wait(tempty_bar(acc), acc_phase ^ 1u, ctl)) { aborted = true; break; }
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
@@ -521,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc = 0, acc_phase = 0;
     uint32_t w, kbeg, kend;
     int kind, half;
-    for (uint32_t i = 0; sch.item(i, w, kbeg, kend, kind, half); ++i) {
+    for (uint32_t i = 0; next_item_warp(i, w, kbeg, kend, kind, half); ++i) {
       const bool ok = wait(tfull_bar(acc), acc_phase, ctl);
       if (!__all_sync(0xFFFFFFFFu, ok)) { aborted = true; break; }
       ptx::tc_fence_after();
@@ -747,7 +833,7 @@ static int kernel_capacity(const DeviceInfo& dev, int* programs) {
       return SWZ_OK;
     }
   }
-  auto kern = gemm_kernel<BN, PAIR, KIND, SW>;
+  auto kern = gemm_kernel<BN, PAIR, KIND, SW, false>;
   SWZ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     K_::SMEM_BYTES));
   int cap = 0;
@@ -825,6 +911,9 @@ struct SkLayout {
   uint64_t flags_bytes, data_bytes;
 };
 
+// workspace of a dynamic-scheduler launch: the claimed-work counter
+constexpr uint64_t kDynWorkspaceBytes = 256;
+
 static SkLayout sk_layout(const Plan& pl, int persistent, const swz_gemm_opts& o) {
   SkLayout L{false, 0, 0};
   const uint32_t cl = pl.pair ? 2u : 1u;
@@ -836,14 +925,14 @@ static SkLayout sk_layout(const Plan& pl, int persistent, const swz_gemm_opts& o
   return L;
 }
 
-template <int BN, bool PAIR, int KIND, int SW>
+template <int BN, bool PAIR, int KIND, int SW, bool DYN>
 static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& ta3,
                   const CUtensorMap& tb, const CUtensorMap& tb3, const CUtensorMap& tc,
                   const Params& prm, cudaStream_t stream) {
   using K_ = Cfg<BN, PAIR>;
   static std::mutex mu;
   static bool attr_set[64] = {};
-  auto kern = gemm_kernel<BN, PAIR, KIND, SW>;
+  auto kern = gemm_kernel<BN, PAIR, KIND, SW, DYN>;
   int dev = 0;
   SWZ_CUDA_TRY(cudaGetDevice(&dev));
   {
@@ -879,18 +968,18 @@ using namespace swz;
 using namespace swz::gemm;
 
 // kernel instance for the plan's tile shape, the operand kind and span SW
-template <int SW>
+template <int SW, bool DYN>
 static int dispatch(const Plan& pl, bool tf32, const CUtensorMap& ta, const CUtensorMap& ta3,
                     const CUtensorMap& tb, const CUtensorMap& tb3, const CUtensorMap& tc,
                     const Params& prm, cudaStream_t s) {
   if (tf32) {
-    if (pl.pair) return launch<256, true, 1, SW>(pl, ta, ta3, tb, tb3, tc, prm, s);
-    if (pl.bn == 128) return launch<128, false, 1, SW>(pl, ta, ta3, tb, tb3, tc, prm, s);
-    return launch<256, false, 1, SW>(pl, ta, ta3, tb, tb3, tc, prm, s);
+    if (pl.pair) return launch<256, true, 1, SW, DYN>(pl, ta, ta3, tb, tb3, tc, prm, s);
+    if (pl.bn == 128) return launch<128, false, 1, SW, DYN>(pl, ta, ta3, tb, tb3, tc, prm, s);
+    return launch<256, false, 1, SW, DYN>(pl, ta, ta3, tb, tb3, tc, prm, s);
   }
-  if (pl.pair) return launch<256, true, 0, SW>(pl, ta, ta3, tb, tb3, tc, prm, s);
-  if (pl.bn == 128) return launch<128, false, 0, SW>(pl, ta, ta3, tb, tb3, tc, prm, s);
-  return launch<256, false, 0, SW>(pl, ta, ta3, tb, tb3, tc, prm, s);
+  if (pl.pair) return launch<256, true, 0, SW, DYN>(pl, ta, ta3, tb, tb3, tc, prm, s);
+  if (pl.bn == 128) return launch<128, false, 0, SW, DYN>(pl, ta, ta3, tb, tb3, tc, prm, s);
+  return launch<256, false, 0, SW, DYN>(pl, ta, ta3, tb, tb3, tc, prm, s);
 }
 
 static int validate(const void* A, const void* B, const float* C, int M, int N, int K, int order,
@@ -967,6 +1056,10 @@ extern "C" int swz_gemm_workspace_size(int M, int N, int K, int persistent,
   if (opts) o = *opts;
   if (!bytes || M < 0 || N < 0 || K < 0) return SWZ_EINVAL;
   *bytes = 0;
+  if (o.dynamic && !o.stream_k) {
+    *bytes = persistent ? kDynWorkspaceBytes : 0;
+    return SWZ_OK;
+  }
   if (M == 0 || N == 0 || K == 0 || !o.stream_k || !persistent) return SWZ_OK;
   DeviceInfo dev{};
   const bool need_dev = o.num_programs == 0;
@@ -1066,6 +1159,12 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
     if (!persistent || o.stream_k) return SWZ_EINVAL;
     prm.split_tail = 1;
   }
+  if (o.dynamic) {
+    if (!persistent || o.stream_k || o.split_tail) return SWZ_EINVAL;
+    const uintptr_t ws = reinterpret_cast<uintptr_t>(o.d_workspace);
+    if (!ws || (ws & 255u) || o.workspace_bytes < kDynWorkspaceBytes) return SWZ_EINVAL;
+    if (span != 128) return SWZ_EUNSUPPORTED;
+  }
   prm.trace = o.d_trace;
   prm.debug_flags = o.debug_flags;
   prm.timeout_ns = uint64_t(o.timeout_ms ? o.timeout_ms : 2000u) * 1000000ull;
@@ -1093,9 +1192,15 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   }
 
   prm.b3d = b3d ? 1u : 0u;
-  if (span == 64) return dispatch<64>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
-  if (span == 32) return dispatch<32>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
-  return dispatch<128>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
+  if (o.dynamic) {
+    // the counter of claimed work indices starts at zero in every launch
+    prm.dyn_counter = static_cast<uint32_t*>(o.d_workspace);
+    SWZ_CUDA_TRY(cudaMemsetAsync(prm.dyn_counter, 0, sizeof(uint32_t), s));
+    return dispatch<128, true>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
+  }
+  if (span == 64) return dispatch<64, false>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
+  if (span == 32) return dispatch<32, false>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
+  return dispatch<128, false>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
 }
 
 extern "C" int swz_gemm(const void* A, const void* B, float* C, int M, int N, int K, int order,
