@@ -63,17 +63,17 @@ SWEEP = WORKLOADS["gemm8192_bf16_pair"]["sweep"]
 # DRAM traffic of one launch of the headline GEMM from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
 # source whose SHA-256 prefix is recorded with it.
-TRAFFIC = {"bytes": 1300055552, "gemm_cu_sha256": "232fb2601831c892",
+TRAFFIC = {"bytes": 1294022144, "gemm_cu_sha256": "1bf4096afdbe6417",
            "profile": "profiles/gemm_8192_bf16_pair_ncu.md"}
 
 
 # L2 hit rate (lts__t_sector_hit_rate.pct) of one cold launch per order from
 # an ncu capture of `bench.py --only sweep`; valid for the recorded kernel
 # source only.
-L2_NCU = {"gemm_cu_sha256": "232fb2601831c892", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
-          ("row", 1): 62.31, ("col", 1): 62.13, ("panel", 4): 69.04, ("panel", 8): 73.54,
-          ("panel", 16): 67.61, ("serpentine", 4): 70.93, ("serpentine", 8): 73.66,
-          ("serpentine", 16): 69.57, ("morton", 1): 69.16, ("xor", 1): 63.01}
+L2_NCU = {"gemm_cu_sha256": "1bf4096afdbe6417", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
+          ("row", 1): 62.18, ("col", 1): 61.87, ("panel", 4): 68.66, ("panel", 8): 73.41,
+          ("panel", 16): 70.01, ("serpentine", 4): 69.63, ("serpentine", 8): 72.44,
+          ("serpentine", 16): 69.62, ("morton", 1): 67.45, ("xor", 1): 63.26}
 
 
 def _gemm_src_hash():

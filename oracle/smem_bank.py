@@ -67,6 +67,32 @@ def cute_swizzle(offset, b, m, s):
     return offset ^ ((offset & mask) >> s)
 
 
+def tma_swizzle_bytes(addr, span):
+    """Physical byte address of logical byte address ``addr`` (relative to a
+    base aligned to the pattern) under the TMA / tensor-core swizzle of span
+    ``span`` = 128, 64 or 32 bytes.  Generalises the 128-byte rule of "Hopper
+    TMA 的 swizzling" as the PTX ISA's swizzle modes state it: the 16-byte
+    chunk bits of the address (bits 4 ..) are XOR-ed with the same number of
+    bits of the 128-byte line index (bits 7 ..); the span fixes how many:
+    3 for 128 bytes, 2 for 64, 1 for 32.  The pattern repeats every
+    8 * span bytes."""
+    bits = {128: 3, 64: 2, 32: 1}[span]
+    mask = (1 << bits) - 1
+    return addr ^ (((addr >> 7) & mask) << 4)
+
+
+def core_matrix_read_addresses(rows, k_byte, span, swizzled=True):
+    """Byte addresses of one 16-byte read from each of ``rows`` consecutive
+    rows of a K-major operand block whose rows are ``span`` bytes long (one
+    swizzle column group), at byte ``k_byte`` of the row: the pattern of a
+    tensor-core core-matrix read (8 rows x 16 bytes)."""
+    out = []
+    for r in range(rows):
+        a = r * span + k_byte
+        out.append(tma_swizzle_bytes(a, span) if swizzled else a)
+    return out
+
+
 def triton_source_column(r, c, vec, per_phase, max_phase):
     """Triton shared layout ("Triton - Shared Layout swizzling"): element
     (r, c) of the stored tile holds input column

@@ -144,3 +144,46 @@ def test_mma_sync_kernel_conflict_totals():
         assert got == want[name], name
         assert sb.cp_async_tile_conflicts(128, 64, lay) == 0
         assert sb.cp_async_tile_conflicts(64, 128, lay) == 0
+
+
+def test_tma_swizzle_spans_pinned():
+    # 128-byte span: the page's chunk formula on 128-byte rows
+    for y in range(16):
+        for x in range(64):
+            yy, xs = sb.tma_swizzle_128b(y, x, 64, 2)
+            assert sb.tma_swizzle_bytes(2 * (y * 64 + x), 128) == 2 * (yy * 64 + xs)
+    # every span: Swizzle<b,4,3> of the CUTLASS section on byte addresses
+    for span, b in ((128, 3), (64, 2), (32, 1)):
+        for a in range(0, 4096, 2):
+            assert sb.tma_swizzle_bytes(a, span) == sb.cute_swizzle(a, b, 4, 3)
+    # 64- and 32-byte spans as Triton layouts on rows of 32 / 16 fp16
+    # elements: (vec 8, perPhase 2, maxPhase 4) and (vec 8, perPhase 4,
+    # maxPhase 2) -- the stored column of each chunk matches
+    for span, pp, mp in ((64, 2, 4), (32, 4, 2)):
+        w = span // 2
+        for r in range(16):
+            for c in range(w):
+                phys = sb.tma_swizzle_bytes(2 * (r * w + c), span) // 2 - r * w
+                assert sb.triton_source_column(r, phys, 8, pp, mp) == c
+
+
+@pytest.mark.parametrize("span", [128, 64, 32])
+def test_tma_swizzle_permutes_chunks(span):
+    block = 8 * span
+    for base in (0, block, 5 * block):
+        img = [sb.tma_swizzle_bytes(base + a, span) for a in range(0, block, 16)]
+        assert sorted(img) == list(range(base, base + block, 16))  # chunks permuted in place
+        assert all(sb.tma_swizzle_bytes(base + a + 4, span) == i + 4
+                   for a, i in zip(range(0, block, 16), img))   # bytes stay in their chunk
+
+
+@pytest.mark.parametrize("span", [128, 64, 32])
+def test_core_matrix_reads_conflict_free(span):
+    # 8 rows x 16 bytes at every 16-byte position of the row: one wavefront
+    # with the swizzle; without it, rows `span` bytes apart collide: span / 16
+    # of the 8 rows share each 16-byte bank group
+    for k in range(0, span, 16):
+        addrs = sb.core_matrix_read_addresses(8, k, span)
+        assert sb.wavefronts(addrs, 16) == 1
+        plain = sb.core_matrix_read_addresses(8, k, span, swizzled=False)
+        assert sb.wavefronts(plain, 16) == span // 16
