@@ -52,6 +52,13 @@ WORKLOADS = {
                                      sweep=[("row", 1), ("col", 1), ("panel", 4), ("panel", 8),
                                             ("panel", 16), ("serpentine", 4),
                                             ("serpentine", 8), ("serpentine", 16)]),
+    "gemm6144x10240x4096_fp16_pair": dict(M=6144, N=10240, K=4096, dtype="fp16",
+                                          dist="uniform", cfg=dict(cta_pair=True, tile_n=128),
+                                          tile=(128, 128), cluster_m=2,
+                                          sweep=[("row", 1), ("col", 1), ("panel", 4),
+                                                 ("panel", 8), ("panel", 16),
+                                                 ("serpentine", 4), ("serpentine", 8),
+                                                 ("serpentine", 16)]),
     "gemm1024x1024x512_fp16": dict(M=1024, N=1024, K=512, dtype="fp16", dist="uniform",
                                    cfg=dict(tile_n=128), tile=(128, 128), cluster_m=1,
                                    sweep=[("row", 1), ("col", 1), ("panel", 4), ("morton", 1),
@@ -378,7 +385,8 @@ def run_swz(args):
             "value": world * flops / ms_step / 1e9, "ms_per_step": ms_step,
             "config": {"workload": f"{args.workload}: gemm {M}x{N}x{K} {wl['dtype']} "
                                    f"{'N(0,1)' if wl['dist'] == 'normal' else 'U[-1,1)'} -> fp32, "
-                                   + ("2-CTA clusters 256x256" if cfg.get("cta_pair") else
+                                   + (f"2-CTA clusters 256x{cfg.get('tile_n') or 256}"
+                                      if cfg.get("cta_pair") else
                                       f"1-CTA tiles 128x{cfg.get('tile_n')}")
                                    + (", persistent" if persistent else ", one CTA per tile")
                                    + (", Stream-K tail" if args.stream_k else ""),

@@ -118,8 +118,9 @@ typedef struct swz_gemm_opts {
                         multiplied as TF32; needs b_layout = SWZ_B_NK)        */
   int tile_n;        /* 128 or 256; 0 = automatic as in swz_gemm             */
   int cta_pair;      /* 1: 2-CTA clusters, tcgen05 cta_group::2, cluster tile
-                        256 x tile_n (tile_n must be 256; each CTA owns
-                        128 x 256 of C) -- [CPS] Example 2; 0: single CTA    */
+                        256 x tile_n (tile_n 256, the default, or 128; each
+                        CTA owns 128 x tile_n of C) -- [CPS] Example 2;
+                        0: single CTA                                        */
   int num_programs;  /* persistent only: CTAs to launch (a multiple of 2 with
                         cta_pair); 0 = resident capacity, capped at the tile
                         count                                                */
@@ -173,8 +174,9 @@ typedef struct swz_gemm_opts {
 
 /* swz_gemm with explicit tile shape, dtype, 2-CTA mode, program count, trace,
  * wait bound and Stream-K tail.  opts may be NULL (= swz_gemm).  Extra
- * errors: SWZ_EUNSUPPORTED for tile_n not in {0,128,256}, cta_pair with
- * tile_n != 256, or stream_k with more programs than can be resident at
+ * errors: SWZ_EUNSUPPORTED for tile_n not in {0,128,256}, split_tail with
+ * cta_pair, tile_n 128 and B as K x N, or stream_k with more programs than
+ * can be resident at
  * once (its pieces wait on one another); SWZ_EINVAL for stream_k without
  * persistent or with a missing, misaligned (256 B) or too small workspace,
  * and for smem_swizzle not in {0, 32, 64, 128}; for dynamic the same

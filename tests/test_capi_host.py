@@ -67,8 +67,9 @@ def test_plan_without_device(swz):
     assert swz.gemm_plan(300, 392, 200, True, tile_n=256, num_programs=1000) == (3, 2, 3, 2, 6)
     rc, _ = swz.swz_gemm_plan(1024, 1024, 512, 0, swz.make_opts(tile_n=192))
     assert rc == swz.SWZ_EUNSUPPORTED
-    rc, _ = swz.swz_gemm_plan(1024, 1024, 512, 0, swz.make_opts(tile_n=128, cta_pair=True))
-    assert rc == swz.SWZ_EUNSUPPORTED
+    # CTA pair with 128-wide tiles: cluster tiles 256 x 128, CTA tiles 128 x 128
+    assert swz.gemm_plan(6144, 10240, 4096, cta_pair=True, tile_n=128) == (48, 80, 24, 80, 3840)
+    assert swz.gemm_plan(1024, 1024, 512, cta_pair=True, tile_n=128) == (8, 8, 4, 8, 64)
     rc, _ = swz.swz_gemm_plan(1024, 1024, 512, 1, swz.make_opts(cta_pair=True, num_programs=7))
     assert rc == swz.SWZ_EINVAL
 
