@@ -70,17 +70,17 @@ SWEEP = WORKLOADS["gemm8192_bf16_pair"]["sweep"]
 # DRAM traffic of one launch of the headline GEMM from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
 # source whose SHA-256 prefix is recorded with it.
-TRAFFIC = {"bytes": 1294022144, "gemm_cu_sha256": "1bf4096afdbe6417",
+TRAFFIC = {"bytes": 1332563456, "gemm_cu_sha256": "adf66e77176db4e8",
            "profile": "profiles/gemm_8192_bf16_pair_ncu.md"}
 
 
 # L2 hit rate (lts__t_sector_hit_rate.pct) of one cold launch per order from
 # an ncu capture of `bench.py --only sweep`; valid for the recorded kernel
 # source only.
-L2_NCU = {"gemm_cu_sha256": "1bf4096afdbe6417", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
-          ("row", 1): 62.18, ("col", 1): 61.87, ("panel", 4): 68.66, ("panel", 8): 73.41,
-          ("panel", 16): 70.01, ("serpentine", 4): 69.63, ("serpentine", 8): 72.44,
-          ("serpentine", 16): 69.62, ("morton", 1): 67.45, ("xor", 1): 63.26}
+L2_NCU = {"gemm_cu_sha256": "adf66e77176db4e8", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
+          ("row", 1): 62.43, ("col", 1): 62.33, ("panel", 4): 69.23, ("panel", 8): 73.33,
+          ("panel", 16): 70.35, ("serpentine", 4): 70.33, ("serpentine", 8): 72.78,
+          ("serpentine", 16): 69.66, ("morton", 1): 70.50, ("xor", 1): 62.66}
 
 
 def _gemm_src_hash():
