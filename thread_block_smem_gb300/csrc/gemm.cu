@@ -47,17 +47,24 @@ constexpr int BK = 64;         // K elements per stage, 16-bit operands (128-byt
 // rows, so every byte offset below is shared by both kinds.
 template <int KIND>
 constexpr int bk_elems() { return KIND == 0 ? 64 : 32; }
+// 128-byte K atoms per stage with the 128-byte span, by tile width: a stage
+// of KA atoms carries 4 * KA MMAs per barrier round trip of the issuing
+// thread, whose per-stage overhead (~300 cycles) a 128-wide stage of 4 MMAs
+// (256 tensor cycles) cannot hide: 2 atoms for 128-wide tiles (+15 % for
+// the pair), 1 for 256-wide ones (2 would leave 3 stages or fewer).  Other
+// spans use one 128-byte row per stage.
+constexpr int stage_atoms(int bn) { return bn == 128 ? 2 : 1; }
 constexpr int kThreads = 192;  // 6 warps
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kSchedDepth = 4;            // slots of the dynamic scheduler's ring
 constexpr uint32_t kNoWork = 0xFFFFFFFFu;  // ring entry: no more work
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, int KA = 1>
 struct Cfg {
   static constexpr int CG = PAIR ? 2 : 1;
   static constexpr int BN_LOCAL = PAIR ? BN / 2 : BN;  // B columns this CTA loads
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = BK * BN_LOCAL * 2;
+  static constexpr int A_BYTES = BM * 128 * KA;        // 128 rows of KA 128-byte atoms
+  static constexpr int B_BYTES = 128 * KA * BN_LOCAL;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = kSmemBudget / STAGE_BYTES;
   static constexpr int TMEM_COLS = 2 * BN;
@@ -260,7 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Params p) {
-  using K_ = Cfg<BN, PAIR>;
+  constexpr int KA = SW == 128 ? stage_atoms(BN) : 1;
+  using K_ = Cfg<BN, PAIR, KA>;
   constexpr int CL = K_::CG;
   constexpr int STAGES = K_::STAGES;
 
@@ -433,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int local = half < 0 ? K_::BN_LOCAL : K_::BN_LOCAL / 2;
         const int32_t n0 = int32_t(t.n * BN + (half < 0 ? 0 : half * (BN / 2)) + rank * local);
         const int boxes = local / xn;  // xn = 64 when sw == 128
-        const uint32_t tx = uint32_t(CL) * uint32_t(K_::A_BYTES + local * 128);
+        const uint32_t tx = uint32_t(CL) * uint32_t(K_::A_BYTES + local * 128 * KA);
         for (uint32_t kb = kbeg; kb < kend; ++kb) {
           if (!wait(empty_bar(stage), phase ^ 1u, ctl)) { aborted = true; break; }
           if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), tx);
@@ -441,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             skip = false;
           } else {
             const uint32_t fb = PAIR ? ptx::map_to_rank(full_bar(stage), 0) : full_bar(stage);
-            const int32_t k0 = int32_t(kb * bk_elems<KIND>());
+            const int32_t k0 = int32_t(kb * bk_elems<KIND>() * KA);
             const uint32_t a_dst = sA + stage * K_::A_BYTES, b_dst = sB + stage * K_::B_BYTES;
             // A: one box of 128 rows per column group, or one 3-D box
             // (xe elements x 128 rows x groups) when the map allows it.
@@ -452,24 +460,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             // `local` rows (tmB: full width, tmB3: half width).
             const bool one_box = p.b3d && half < 0;
             if constexpr (SW == 128) {
+              // K-major operands: one box per 128-byte atom (KA of them);
+              // N-major B: boxes of 64 columns x BK * KA rows
+              constexpr int ke = bk_elems<KIND>();
               if constexpr (PAIR) {
-                ptx::tma_load_2d_pair(a_dst, &tmA, fb, k0, m0);
+#pragma unroll
+                for (int g = 0; g < KA; ++g)
+                  ptx::tma_load_2d_pair(a_dst + g * (BM * 128), &tmA, fb, k0 + g * ke, m0);
                 if (p.b_kmajor)
-                  ptx::tma_load_2d_pair(b_dst, half < 0 ? &tmB : &tmB3, fb, k0, n0);
+#pragma unroll
+                  for (int g = 0; g < KA; ++g)
+                    ptx::tma_load_2d_pair(b_dst + g * local * 128, half < 0 ? &tmB : &tmB3, fb,
+                                          k0 + g * ke, n0);
                 else if (one_box)
                   ptx::tma_load_3d_pair(b_dst, &tmB3, fb, 0, k0, n0 / 64);
                 else
                   for (int j = 0; j < boxes; ++j)
-                    ptx::tma_load_2d_pair(b_dst + j * (BK * 128), &tmB, fb, n0 + 64 * j, k0);
+                    ptx::tma_load_2d_pair(b_dst + j * (BK * KA * 128), &tmB, fb, n0 + 64 * j, k0);
               } else {
-                ptx::tma_load_2d(a_dst, &tmA, fb, k0, m0);
+#pragma unroll
+                for (int g = 0; g < KA; ++g)
+                  ptx::tma_load_2d(a_dst + g * (BM * 128), &tmA, fb, k0 + g * ke, m0);
                 if (p.b_kmajor)
-                  ptx::tma_load_2d(b_dst, half < 0 ? &tmB : &tmB3, fb, k0, n0);
+#pragma unroll
+                  for (int g = 0; g < KA; ++g)
+                    ptx::tma_load_2d(b_dst + g * local * 128, half < 0 ? &tmB : &tmB3, fb,
+                                     k0 + g * ke, n0);
                 else if (one_box)
                   ptx::tma_load_3d(b_dst, &tmB3, fb, 0, k0, n0 / 64);
                 else
                   for (int j = 0; j < boxes; ++j)
-                    ptx::tma_load_2d(b_dst + j * (BK * 128), &tmB, fb, n0 + 64 * j, k0);
+                    ptx::tma_load_2d(b_dst + j * (BK * KA * 128), &tmB, fb, n0 + 64 * j, k0);
               }
             } else if constexpr (PAIR) {
               if (p.a3d)
@@ -563,15 +584,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_addr = sA + stage * K_::A_BYTES;
           const uint32_t b_addr = sB + stage * K_::B_BYTES;
           if constexpr (SW == 128) {
+            // slice kk of the KA atoms: atom kk / 4, 32 bytes per slice
+            // inside it; N-major B: 16 K-rows of 128 bytes per slice
             const uint64_t adesc = make_sdesc(a_addr, 16, 1024, 2);
             const uint64_t bdesc = p.b_kmajor ? make_sdesc(b_addr, 16, 1024, 2)
-                                              : make_sdesc(b_addr, BK * 128, 1024, 2);
-            const uint64_t bstep = p.b_kmajor ? 2u : 128u;
+                                              : make_sdesc(b_addr, BK * KA * 128, 1024, 2);
+            const uint32_t b_atom = b_rows * 128u;  // K-major B: bytes of one atom
             ptx::mma<CL, KIND>(d, adesc, bdesc, idesc, kb != kbeg ? 1u : 0u);
 #pragma unroll
-            for (int kk = 1; kk < 4; ++kk)
-              ptx::mma<CL, KIND>(d, adesc + uint64_t(2 * kk), bdesc + bstep * uint64_t(kk),
-                                 idesc, 1u);
+            for (int kk = 1; kk < 4 * KA; ++kk) {
+              const uint64_t ao = uint64_t(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4);
+              const uint64_t bo =
+                  p.b_kmajor ? uint64_t(((kk / 4) * b_atom + (kk % 4) * 32u) >> 4)
+                             : uint64_t(128 * kk);
+              ptx::mma<CL, KIND>(d, adesc + ao, bdesc + bo, idesc, 1u);
+            }
           } else {
             const uint64_t adesc = make_sdesc(a_addr, 16, 8 * sw, lay);
             const uint64_t bdesc = p.b_kmajor ? make_sdesc(b_addr, 16, 8 * sw, lay)
@@ -829,7 +856,7 @@ struct Plan {
 template <int BN, bool PAIR, int KIND>
 static int kernel_capacity(const DeviceInfo& dev, int* programs) {
   constexpr int SW = 128;
-  using K_ = Cfg<BN, PAIR>;
+  using K_ = Cfg<BN, PAIR, stage_atoms(BN)>;
   static std::mutex mu;
   static int cache[64] = {};
   {
@@ -937,7 +964,7 @@ template <int BN, bool PAIR, int KIND, int SW, bool DYN>
 static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& ta3,
                   const CUtensorMap& tb, const CUtensorMap& tb3, const CUtensorMap& tc,
                   const Params& prm, cudaStream_t stream) {
-  using K_ = Cfg<BN, PAIR>;
+  using K_ = Cfg<BN, PAIR, SW == 128 ? stage_atoms(BN) : 1>;
   static std::mutex mu;
   static bool attr_set[64] = {};
   auto kern = gemm_kernel<BN, PAIR, KIND, SW, DYN>;
@@ -1117,6 +1144,8 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   const uint32_t esize = tf32 ? 4u : 2u;
   const uint32_t bke = 128u / esize;  // K elements per 128-byte stage row
   const uint32_t xe = span / esize;   // elements per swizzle span
+  // 128-byte K atoms per stage of the kernel this launch will use
+  const uint32_t ka = span == 128 ? uint32_t(stage_atoms(pl.bn)) : 1u;
   const uint32_t local = uint32_t(pl.pair ? pl.bn / 2 : pl.bn);  // B columns per CTA
   const bool b_kmajor = o.b_layout == SWZ_B_NK;
   CUtensorMap ta, ta3, tb, tb3, tc;
@@ -1139,14 +1168,15 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
     if (rc != SWZ_OK) return rc;
   } else {
     const uint32_t xn = span / 2;  // B columns per span (16-bit elements)
-    rc = encode_2d(&tb, o.dtype, B, uint64_t(K), uint64_t(N), xn, BK, span);
+    rc = encode_2d(&tb, o.dtype, B, uint64_t(K), uint64_t(N), xn, BK * ka, span);
     if (rc != SWZ_OK) return rc;
     // B as (xn columns, K rows, N/xn column groups): a CTA's whole share of
     // a tile in one box, when N % xn == 0
     b3d = uint32_t(N) % xn == 0;
     tb3 = tb;
     if (b3d) {
-      rc = encode_groups(&tb3, o.dtype, B, uint64_t(K), uint64_t(N), xn, BK, local / xn, span);
+      rc = encode_groups(&tb3, o.dtype, B, uint64_t(K), uint64_t(N), xn, BK * ka, local / xn,
+                         span);
       if (rc != SWZ_OK) return rc;
     }
   }
@@ -1162,7 +1192,7 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   prm.group = int(g);
   prm.sched_m = pl.sched_m;
   prm.sched_n = pl.sched_n;
-  prm.num_kb = uint32_t((uint32_t(K) + bke - 1) / bke);
+  prm.num_kb = uint32_t((uint32_t(K) + bke * ka - 1) / (bke * ka));
   prm.idesc = make_idesc(o.dtype, pl.pair ? 256 : 128, pl.bn, !b_kmajor);
   prm.idesc_half = make_idesc(o.dtype, pl.pair ? 256 : 128, pl.bn / 2, !b_kmajor);
   prm.b_kmajor = b_kmajor ? 1u : 0u;
