@@ -83,6 +83,14 @@ L2_NCU = {"gemm_cu_sha256": "adf66e77176db4e8", "profile": "profiles/gemm_8192_b
           ("serpentine", 16): 69.66, ("morton", 1): 70.50, ("xor", 1): 62.66}
 
 
+# dram__bytes_read.sum of the same captures (one cold launch per order)
+L2_NCU_DRAM = {("row", 1): 2056320000, ("col", 1): 2060878336, ("panel", 4): 1450616064,
+               ("panel", 8): 1125236480, ("panel", 16): 1260939264,
+               ("serpentine", 4): 1364476416, ("serpentine", 8): 1053510656,
+               ("serpentine", 16): 1247361536, ("morton", 1): 1371850752,
+               ("xor", 1): 2104232704}
+
+
 def _gemm_src_hash():
     with open(os.path.join(ROOT, "thread_block_smem_gb300", "csrc", "gemm.cu"), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -340,16 +348,23 @@ def run_swz(args):
                     orders.append({"order": order, "group": g, "error": swz.strerror(e.code)})
                     continue
                 med = statistics.median(t)
-                pred = swz.l2_model_hit_rate(order, g, M, N, K, wl["tile"][0], wl["tile"][1], 64,
-                                             2, l2_bytes, programs, wl["cluster_m"])
+                # the model at the kernel's tiling: K steps of 64 elements
+                # (two 128-byte atoms, 128 elements, for 128-wide tiles)
+                tk = 128 if wl["tile"][1] == 128 else 64
+                pred, pred_bytes = swz.l2_model_predict(order, g, M, N, K, wl["tile"][0],
+                                                        wl["tile"][1], tk, 2, l2_bytes,
+                                                        programs, wl["cluster_m"])
+                ncu_ok = (L2_NCU.get("gemm_cu_sha256") == _gemm_src_hash()
+                          and args.workload == "gemm8192_bf16_pair" and persistent
+                          and not args.stream_k)
                 orders.append({"order": order, "group": g, "ms": med,
                                "tflops": flops / med / 1e9,
                                "pct_peak": 100.0 * flops / med / 1e9 / peaks["bf16_tflops"],
                                "l2_model_hit_pct": pred,
-                               "l2_ncu_hit_pct": L2_NCU.get((order, g))
-                               if (L2_NCU.get("gemm_cu_sha256") == _gemm_src_hash()
-                                   and args.workload == "gemm8192_bf16_pair"
-                                   and persistent and not args.stream_k) else None})
+                               "l2_model_dram_read_bytes": pred_bytes,
+                               "l2_ncu_hit_pct": L2_NCU.get((order, g)) if ncu_ok else None,
+                               "dram_read_ncu_bytes": L2_NCU_DRAM.get((order, g))
+                               if ncu_ok else None})
         # ---- operand-stage swizzle span (TMA + tensor-core layout) ---------
         spans = []
         if args.only == "swizzle":  # one cold launch per span, for counter capture

@@ -278,6 +278,15 @@ int swz_l2_model(int order, int group, int M, int N, int K, int tile_m, int tile
                  int tile_k, int elem_bytes, int64_t l2_bytes, int concurrency,
                  int cluster_m, int64_t* h_hits, int64_t* h_misses);
 
+/* swz_l2_model plus the bytes the misses bring in (each miss of an A tile
+ * counts tile_m * tile_k * elem_bytes, of a B tile tile_k * tile_n *
+ * elem_bytes): the model's prediction of the operand bytes read from DRAM.
+ * Errors: SWZ_EINVAL (as swz_l2_model, or h_miss_bytes NULL). */
+int swz_l2_model_bytes(int order, int group, int M, int N, int K, int tile_m, int tile_n,
+                       int tile_k, int elem_bytes, int64_t l2_bytes, int concurrency,
+                       int cluster_m, int64_t* h_hits, int64_t* h_misses,
+                       int64_t* h_miss_bytes);
+
 /*
  * swz_gemm_streamk_noalloc -- Stream-K GEMM for callers that cannot allocate
  * device memory.  No source page has a counterpart; this is a library

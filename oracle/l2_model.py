@@ -33,6 +33,7 @@ class ByteLRU:
         self.bytes_held = 0
         self.hits = 0
         self.misses = 0
+        self.miss_bytes = 0  # bytes brought in by misses: the predicted DRAM reads
 
     def touch(self, key, nbytes):
         held = self._held
@@ -41,6 +42,7 @@ class ByteLRU:
             held.move_to_end(key)
             return True
         self.misses += 1
+        self.miss_bytes += nbytes
         held[key] = nbytes
         self.bytes_held += nbytes
         while self.bytes_held > self.capacity and len(held) > 1:

@@ -23,7 +23,7 @@ def _oracle_counts(order, group, M, N, K, tm, tn, tk, eb, l2b, conc, cm):
     gk = math.ceil(K / tk)
     seq = l2.cta_tiles_of_clusters(order, gm, gn, group, cm)
     c = l2.simulate(seq, gk, tm * tk * eb, tk * tn * eb, l2b, conc)
-    return c.hits, c.misses
+    return c.hits, c.misses, c.miss_bytes
 
 
 CASES = [
@@ -44,7 +44,10 @@ CASES = [
 def test_native_model_matches_oracle(swz, case):
     rc, h, m = swz.swz_l2_model(*case)
     assert rc == 0
-    assert (h, m) == _oracle_counts(*case)
+    want = _oracle_counts(*case)
+    assert (h, m) == want[:2]
+    rc, h2, m2, b = swz.swz_l2_model_bytes(*case)
+    assert rc == 0 and (h2, m2, b) == want
 
 
 @pytest.mark.slow
@@ -55,6 +58,15 @@ def test_native_model_reproduces_printed_rates(swz):
         got = swz.l2_model_hit_rate(order, g, 8192, 8192, 8192, 128, 128, 32, 2,
                                     64 << 20, 168, 1)
         assert round(got, 2) == pytest.approx(pct, abs=1e-9), (order, g, got)
+
+
+def test_native_miss_bytes_compulsory(swz):
+    # a cache larger than every operand tile together: each tile is read once
+    M, N, K, tm, tn, tk = 1000, 1200, 300, 128, 256, 64
+    gm, gn, gk = math.ceil(M / tm), math.ceil(N / tn), math.ceil(K / tk)
+    rc, h, m, b = swz.swz_l2_model_bytes(to.SERPENTINE, 2, M, N, K, tm, tn, tk, 2, 1 << 40, 7, 1)
+    assert rc == 0 and m == gm * gk + gk * gn
+    assert b == gm * gk * tm * tk * 2 + gk * gn * tk * tn * 2
 
 
 def test_native_model_rejects_bad_args(swz):

@@ -41,8 +41,9 @@ def test_lru_keeps_one_oversized_entry():
 def test_unbounded_cache_only_compulsory_misses():
     gm, gn, gk = 6, 7, 5
     tiles = to.tile_sequence(to.PANEL, gm, gn, 3)
-    c = l2.simulate(tiles, gk, 100, 100, 10**12, concurrency=4)
+    c = l2.simulate(tiles, gk, 100, 300, 10**12, concurrency=4)
     assert c.misses == gm * gk + gn * gk
+    assert c.miss_bytes == gm * gk * 100 + gn * gk * 300  # compulsory bytes
     assert c.hits == 2 * gm * gn * gk - c.misses
 
 

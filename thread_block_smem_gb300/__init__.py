@@ -35,7 +35,8 @@ LAYOUTS = {"naive": SWZ_SMEM_NAIVE, "padded": SWZ_SMEM_PADDED, "xor": SWZ_SMEM_X
 EXPORTS = ["swz_tile_map", "swz_is_bijective", "swz_gemm", "swz_gemm_ex", "swz_gemm_plan",
            "swz_transpose", "swz_check_status", "swz_strerror", "swz_last_cuda_error",
            "swz_device_info", "swz_l2_model", "swz_gemm_workspace_size",
-           "swz_gemm_streamk_noalloc", "swz_gemm_host", "swz_gemm_mma_sync", "swz_tc_rate"]
+           "swz_gemm_streamk_noalloc", "swz_gemm_host", "swz_gemm_mma_sync", "swz_tc_rate",
+           "swz_l2_model_bytes"]
 
 
 class SwzError(RuntimeError):
@@ -81,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.swz_device_info.argtypes = [ip, ip, ip, ip]
         i64p = ctypes.POINTER(ctypes.c_int64)
         L.swz_l2_model.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.c_int64, i, i, i64p, i64p]
+        L.swz_l2_model_bytes.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.c_int64, i, i, i64p,
+                                         i64p, i64p]
         L.swz_gemm_workspace_size.argtypes = [i, i, i, i, ctypes.POINTER(swz_gemm_opts),
                                               ctypes.POINTER(ctypes.c_uint64)]
         L.swz_gemm_streamk_noalloc.argtypes = [vp, vp, vp, i, i, i, i, i,
@@ -228,6 +231,24 @@ def swz_l2_model(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_b
     rc = lib().swz_l2_model(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes,
                             l2_bytes, concurrency, cluster_m, ctypes.byref(h), ctypes.byref(m))
     return rc, h.value, m.value
+
+
+def swz_l2_model_bytes(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_bytes,
+                       concurrency, cluster_m=1):
+    h, m, b = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    rc = lib().swz_l2_model_bytes(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes,
+                                  l2_bytes, concurrency, cluster_m, ctypes.byref(h),
+                                  ctypes.byref(m), ctypes.byref(b))
+    return rc, h.value, m.value, b.value
+
+
+def l2_model_predict(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_bytes,
+                     concurrency, cluster_m=1):
+    """(predicted L2 hit rate in percent, predicted operand DRAM bytes)."""
+    rc, h, m, b = swz_l2_model_bytes(_order(order), group, M, N, K, tile_m, tile_n, tile_k,
+                                     elem_bytes, l2_bytes, concurrency, cluster_m)
+    _check(rc, "swz_l2_model_bytes")
+    return (100.0 * h / (h + m) if h + m else 0.0), b
 
 
 def l2_model_hit_rate(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_bytes,

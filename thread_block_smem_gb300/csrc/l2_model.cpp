@@ -33,6 +33,7 @@ class LruBytes {
       return;
     }
     ++misses_;
+    miss_bytes_ += bytes;
     order_.emplace_back(key, bytes);
     where_.emplace(key, std::prev(order_.end()));
     held_ += bytes;
@@ -45,9 +46,10 @@ class LruBytes {
 
   int64_t hits() const { return hits_; }
   int64_t misses() const { return misses_; }
+  int64_t miss_bytes() const { return miss_bytes_; }
 
  private:
-  int64_t cap_, held_ = 0, hits_ = 0, misses_ = 0;
+  int64_t cap_, held_ = 0, hits_ = 0, misses_ = 0, miss_bytes_ = 0;
   std::list<std::pair<uint64_t, int64_t>> order_;
   std::unordered_map<uint64_t, std::list<std::pair<uint64_t, int64_t>>::iterator> where_;
 };
@@ -57,13 +59,14 @@ inline uint64_t key_b(uint64_t k, uint64_t n) { return (uint64_t(1) << 63) | (n 
 
 }  // namespace
 
-extern "C" int swz_l2_model(int order, int group, int M, int N, int K, int tile_m, int tile_n,
-                            int tile_k, int elem_bytes, int64_t l2_bytes, int concurrency,
-                            int cluster_m, int64_t* hits, int64_t* misses) {
+extern "C" int swz_l2_model_bytes(int order, int group, int M, int N, int K, int tile_m,
+                                  int tile_n, int tile_k, int elem_bytes, int64_t l2_bytes,
+                                  int concurrency, int cluster_m, int64_t* hits,
+                                  int64_t* misses, int64_t* miss_bytes) {
   if (!swz::order_is_valid(order) || (swz::order_uses_group(order) && group < 1)) return SWZ_EINVAL;
   if (M <= 0 || N <= 0 || K <= 0 || tile_m <= 0 || tile_n <= 0 || tile_k <= 0) return SWZ_EINVAL;
   if (elem_bytes <= 0 || l2_bytes < 0 || concurrency <= 0 || cluster_m <= 0) return SWZ_EINVAL;
-  if (!hits || !misses) return SWZ_EINVAL;
+  if (!hits || !misses || !miss_bytes) return SWZ_EINVAL;
   const int64_t span_m = int64_t(tile_m) * cluster_m;
   const uint32_t sm = uint32_t((int64_t(M) + span_m - 1) / span_m);
   const uint32_t gn = uint32_t((int64_t(N) + tile_n - 1) / tile_n);
@@ -93,5 +96,15 @@ extern "C" int swz_l2_model(int order, int group, int M, int N, int K, int tile_
   }
   *hits = cache.hits();
   *misses = cache.misses();
+  *miss_bytes = cache.miss_bytes();
   return SWZ_OK;
+}
+
+extern "C" int swz_l2_model(int order, int group, int M, int N, int K, int tile_m, int tile_n,
+                            int tile_k, int elem_bytes, int64_t l2_bytes, int concurrency,
+                            int cluster_m, int64_t* hits, int64_t* misses) {
+  if (!hits || !misses) return SWZ_EINVAL;
+  int64_t bytes = 0;
+  return swz_l2_model_bytes(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_bytes,
+                            concurrency, cluster_m, hits, misses, &bytes);
 }
