@@ -351,12 +351,18 @@ def run_swz(args):
                 # the model at the kernel's tiling: K steps of 64 elements
                 # (two 128-byte atoms, 128 elements, for 128-wide tiles)
                 tk = 128 if wl["tile"][1] == 128 else 64
+                # model parameters: the device's L2 and resident programs,
+                # unless overridden (the first page's --l2-cache-mb, --num-sms)
+                model_l2 = int(args.l2_cache_mb * 2**20) if args.l2_cache_mb else l2_bytes
+                model_conc = args.num_sms if args.num_sms else programs  # CTAs in a wave
                 pred, pred_bytes = swz.l2_model_predict(order, g, M, N, K, wl["tile"][0],
-                                                        wl["tile"][1], tk, 2, l2_bytes,
-                                                        programs, wl["cluster_m"])
+                                                        wl["tile"][1], tk, 2, model_l2,
+                                                        model_conc, wl["cluster_m"])
                 ncu_ok = (L2_NCU.get("gemm_cu_sha256") == _gemm_src_hash()
                           and args.workload == "gemm8192_bf16_pair" and persistent
                           and not args.stream_k)
+                line["l2_model"] = {"l2_bytes": model_l2, "concurrency_ctas": model_conc,
+                                    "tile": [wl["tile"][0], wl["tile"][1], tk]}
                 orders.append({"order": order, "group": g, "ms": med,
                                "tflops": flops / med / 1e9,
                                "pct_peak": 100.0 * flops / med / 1e9 / peaks["bf16_tflops"],
@@ -573,6 +579,11 @@ def main():
     ap.add_argument("--no-tf32", action="store_true")
     ap.add_argument("--no-tc-rate", action="store_true")
     ap.add_argument("--no-swizzle", action="store_true")
+    ap.add_argument("--l2-cache-mb", type=float, default=0.0,
+                    help="L2 size the offline model assumes (default: the device's)")
+    ap.add_argument("--num-sms", type=int, default=0,
+                    help="concurrent CTAs the offline model assumes, as SMs (default: the "
+                         "launch's resident programs)")
     ap.add_argument("--no-dynamic", action="store_true")
     ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose", "mma_sync",
                                        "tc_rate", "swizzle"],
