@@ -16,15 +16,21 @@
 //   * 192 threads per CTA, one CTA per SM.  Warp 0: TMA producer.  Warp 1:
 //     TMEM allocator and (one lane) tcgen05.mma issuer.  Warps 2-5: epilogue
 //     (warp w reads TMEM lanes 32*(w%4) .. +31).
-//   * K is consumed in blocks of 64 elements (128 bytes per A row) through a
-//     ring of STAGES shared-memory stages guarded by full/empty mbarriers.
-//     A tile: 128 x 64, K-major.  B tile: 64 x BN_LOCAL, N-major (B is K x N
-//     row-major), loaded as 64-column boxes.
+//   * K is consumed in stages of KA 128-byte atoms per operand row (64 fp16
+//     / bf16 or 32 TF32 elements per atom; KA = 1 for 256-wide tiles, 2 for
+//     128-wide ones) through a ring of STAGES shared-memory stages guarded by
+//     full/empty mbarriers.  A: 128 rows, K-major.  B: BN_LOCAL columns,
+//     N-major (B given K x N, 64-column boxes) or K-major (B given N x K).
+//     The swizzle span (128, 64 or 32 bytes) is a template parameter; the
+//     64- and 32-byte spans split each 128-byte row into column groups.
 //   * The accumulator lives in TMEM, double-buffered (2 x BN fp32 columns),
 //     so the epilogue of tile i overlaps the MMAs of tile i+1.
-//   * CTA pair (PAIR): 2-CTA cluster, tcgen05 cta_group::2, MMA 256 x 256.
-//     Each CTA loads its own 128 rows of A and its half (128 columns) of B;
+//   * CTA pair (PAIR): 2-CTA cluster, tcgen05 cta_group::2, MMA 256 x BN.
+//     Each CTA loads its own 128 rows of A and its half of B's columns;
 //     the leader issues the MMAs and its commits are multicast to both CTAs.
+//   * Work items come from the static schedule (Schedule: work_idx striding,
+//     optional Stream-K tail or split tail) or, with DYN, from an atomic
+//     counter published to all roles through a shared-memory ring.
 //   * Every wait is bounded (globaltimer); on expiry the kernel records
 //     SWZ_ETIMEOUT in a device status word, drains what it issued, frees TMEM
 //     and returns.
