@@ -212,6 +212,25 @@ int swz_gemm_host(const void* h_A, const void* h_B, float* h_C, int M, int N, in
                   int order, int group, const swz_gemm_opts* opts, void* d_A, void* d_B,
                   float* d_C, int slabs, void* stream);
 
+/*
+ * swz_gemm_host_tiled -- swz_gemm_host with C cut into blocks x blocks
+ * blocks (0 = 4; at most 8; block edges multiples of 256) finished in a
+ * growing square: row slab t of A and column panel t of B are copied in
+ * (A0, B0, A1, B1, ...), and as soon as both are resident blocks (t, 0..t)
+ * and (0..t-1, t) are multiplied (swz_gemm_ex, persistent = 1, order/group
+ * within the block) and copied out.  C thus leaves while A and B are still
+ * arriving; every C row of swz_gemm_host waits for all of B.  Column panels
+ * of a K x N B are gathered into d_B by pitched copies (packed K x n_j
+ * panels); with opts->b_layout = SWZ_B_NK (required for TF32) the panels
+ * are contiguous rows of B.  d_C holds the blocks packed, not C's layout;
+ * h_C receives C row-major (pitched copies).  Buffers, streams, ordering and
+ * errors as swz_gemm_host.  The result equals swz_gemm_host's bit for bit (a
+ * tile's K loop does not depend on the block it is computed in).
+ */
+int swz_gemm_host_tiled(const void* h_A, const void* h_B, float* h_C, int M, int N, int K,
+                        int order, int group, const swz_gemm_opts* opts, void* d_A,
+                        void* d_B, float* d_C, int blocks, void* stream);
+
 /* Bytes of d_workspace a launch with these arguments needs (0 when
  * stream_k is off, the launch is not persistent or the tiles divide evenly
  * among the programs).  Needs the device when persistent and num_programs is

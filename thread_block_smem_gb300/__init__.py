@@ -36,7 +36,7 @@ EXPORTS = ["swz_tile_map", "swz_is_bijective", "swz_gemm", "swz_gemm_ex", "swz_g
            "swz_transpose", "swz_check_status", "swz_strerror", "swz_last_cuda_error",
            "swz_device_info", "swz_l2_model", "swz_gemm_workspace_size",
            "swz_gemm_streamk_noalloc", "swz_gemm_host", "swz_gemm_mma_sync", "swz_tc_rate",
-           "swz_l2_model_bytes"]
+           "swz_l2_model_bytes", "swz_gemm_host_tiled"]
 
 
 class SwzError(RuntimeError):
@@ -90,6 +90,7 @@ def lib() -> ctypes.CDLL:
                                                ctypes.POINTER(swz_gemm_opts), vp]
         L.swz_gemm_host.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.POINTER(swz_gemm_opts),
                                     vp, vp, vp, i, vp]
+        L.swz_gemm_host_tiled.argtypes = L.swz_gemm_host.argtypes
         L.swz_gemm_mma_sync.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, i, i, vp]
         L.swz_tc_rate.argtypes = [i, i, vp, vp, i, i, vp, vp, vp]
         for name in EXPORTS:
@@ -146,6 +147,13 @@ def swz_gemm_host(hA, hB, hC, M, N, K, order, group, opts, dA, dB, dC, slabs=0, 
     return lib().swz_gemm_host(hA, hB, hC, M, N, K, order, group,
                                ctypes.byref(opts) if opts is not None else None,
                                dA, dB, dC, slabs, stream)
+
+
+def swz_gemm_host_tiled(hA, hB, hC, M, N, K, order, group, opts, dA, dB, dC, blocks=0,
+                        stream=0):
+    return lib().swz_gemm_host_tiled(hA, hB, hC, M, N, K, order, group,
+                                     ctypes.byref(opts) if opts is not None else None,
+                                     dA, dB, dC, blocks, stream)
 
 
 def swz_gemm_mma_sync(A, B, C, M, N, K, dtype, vec, per_phase, max_phase, pad, order, group,
@@ -381,12 +389,14 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
 
 def gemm_host(hA, hB, hC, dA, dB, dC, order="panel", group=8, *, tile_n=0, cta_pair=False,
               num_programs=0, stream_k=False, workspace=None, split_tail=False, slabs=0,
-              b_transposed=False, stream=None):
+              b_transposed=False, blocks=None, stream=None):
     """C = A @ B from host tensors through swz_gemm_host.  hA (M x K), hB
     (K x N, or N x K when ``b_transposed``; always N x K for fp32 / TF32): CPU
     fp16/bf16/fp32 tensors (pinned for overlap); hC: CPU fp32 M x N;
     dA, dB, dC: CUDA tensors of the same shapes used as staging.  Asynchronous
-    on `stream`; synchronise before reading hC."""
+    on `stream`; synchronise before reading hC.  With ``blocks`` (0 = 4, at
+    most 8) the call goes through swz_gemm_host_tiled: C in blocks x blocks
+    blocks finished in a growing square, so C leaves while A and B arrive."""
     import torch
     M, K = hA.shape
     N = hB.shape[0] if (b_transposed or hA.dtype == torch.float32) else hB.shape[1]
@@ -398,6 +408,12 @@ def gemm_host(hA, hB, hC, dA, dB, dC, order="panel", group=8, *, tile_n=0, cta_p
     code = _dtype_code(hA.dtype)
     opts = make_opts(code, tile_n, cta_pair, num_programs, None, 0, 0, stream_k, workspace,
                      split_tail, SWZ_B_NK if (b_transposed or code == SWZ_TF32) else SWZ_B_KN)
+    if blocks is not None:  # the growing-square pipeline (swz_gemm_host_tiled)
+        _check(swz_gemm_host_tiled(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K,
+                                   _order(order), group, opts, dA.data_ptr(), dB.data_ptr(),
+                                   dC.data_ptr(), blocks, _stream(stream)),
+               "swz_gemm_host_tiled")
+        return hC
     _check(swz_gemm_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K, _order(order),
                          group, opts, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), slabs,
                          _stream(stream)), "swz_gemm_host")
