@@ -91,6 +91,31 @@ L2_NCU_DRAM = {("row", 1): 2053200896, ("col", 1): 2055177472, ("panel", 4): 142
                ("xor", 1): 2056139008}
 
 
+def resolve_workload(args):
+    """The workload of the run: a named configuration, or a custom shape
+    (--m/--n/--k with --dtype, --tile-n, --pair; the first page's benchmark
+    flags), with the sweep's grouped orders at --group-sizes."""
+    if args.m or args.n or args.k:
+        if not (args.m and args.n and args.k):
+            raise SystemExit("--m, --n and --k go together")
+        tn = args.tile_n or 256
+        wl = dict(M=args.m, N=args.n, K=args.k, dtype=args.dtype,
+                  dist="normal" if args.dtype == "bf16" else "uniform",
+                  cfg=dict(cta_pair=True, tile_n=tn) if args.pair else dict(tile_n=tn),
+                  tile=(128, tn), cluster_m=2 if args.pair else 1, sweep=list(_ALL))
+        args.workload = (f"custom{args.m}x{args.n}x{args.k}_{args.dtype}"
+                         + (f"_pair{tn}" if args.pair else f"_tile{tn}"))
+    else:
+        wl = dict(WORKLOADS[args.workload])
+    if args.group_sizes:
+        gs = [int(x) for x in args.group_sizes.split(",") if x]
+        if any(g < 1 for g in gs):
+            raise SystemExit("--group-sizes: positive integers")
+        wl["sweep"] = ([o for o in wl["sweep"] if o[0] not in ("panel", "serpentine")]
+                       + [("panel", g) for g in gs] + [("serpentine", g) for g in gs])
+    return wl
+
+
 def _gemm_src_hash():
     with open(os.path.join(ROOT, "thread_block_smem_gb300", "csrc", "gemm.cu"), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
@@ -226,7 +251,7 @@ def run_reference(args):
     rank, world, _ = _dist()
     if rank != 0:
         return
-    wl = WORKLOADS[args.workload]
+    wl = resolve_workload(args)
     M, N, K = wl["M"], wl["N"], wl["K"]
     import synth_inputs as si
     from oracle import ref
@@ -277,7 +302,7 @@ def run_swz(args):
     do_transpose = args.only in ("all", "transpose") and not args.no_transpose
     do_mma_sync = args.only in ("all", "mma_sync") and not args.no_mma_sync
 
-    wl = WORKLOADS[args.workload]
+    wl = resolve_workload(args)
     M, N, K = wl["M"], wl["N"], wl["K"]
     cfg = dict(wl["cfg"])
     persistent = not args.non_persistent
@@ -580,6 +605,16 @@ def main():
     ap.add_argument("--no-transpose", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gemm8192_bf16_pair")
+    ap.add_argument("--m", type=int, default=0, help="custom shape (with --n, --k)")
+    ap.add_argument("--n", type=int, default=0)
+    ap.add_argument("--k", type=int, default=0)
+    ap.add_argument("--dtype", choices=["fp16", "bf16"], default="fp16",
+                    help="custom shape: operand type (bf16 draws N(0,1), fp16 U[-1,1))")
+    ap.add_argument("--tile-n", type=int, default=0, choices=[0, 128, 256],
+                    help="custom shape: tile width (default 256)")
+    ap.add_argument("--pair", action="store_true", help="custom shape: 2-CTA clusters")
+    ap.add_argument("--group-sizes", default="",
+                    help="comma-separated G / S values of the sweep's grouped orders")
     ap.add_argument("--order", choices=["row", "col", "panel", "morton", "xor", "serpentine"],
                     default=None, help="headline tile order (default panel)")
     ap.add_argument("--group", type=int, default=None, help="G or S of the headline order")

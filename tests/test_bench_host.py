@@ -70,3 +70,22 @@ def test_reference_arm_two_ranks_prints_one_line():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 1
     assert d["cpu_baseline"]["kind"] == "oracle" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_resolve_workload_custom_and_group_sizes():
+    import argparse
+    base = dict(workload="gemm8192_bf16_pair", m=0, n=0, k=0, dtype="fp16", tile_n=0,
+                pair=False, group_sizes="")
+    wl = bench.resolve_workload(argparse.Namespace(**base))
+    assert (wl["M"], wl["N"], wl["K"], wl["dtype"]) == (8192, 8192, 8192, "bf16")
+    a = argparse.Namespace(**dict(base, m=2048, n=1024, k=512, tile_n=128, pair=True,
+                                  group_sizes="3,5"))
+    wl = bench.resolve_workload(a)
+    assert (wl["M"], wl["N"], wl["K"]) == (2048, 1024, 512)
+    assert wl["cfg"] == dict(cta_pair=True, tile_n=128) and wl["cluster_m"] == 2
+    assert a.workload == "custom2048x1024x512_fp16_pair128"
+    grouped = [o for o in wl["sweep"] if o[0] in ("panel", "serpentine")]
+    assert grouped == [("panel", 3), ("panel", 5), ("serpentine", 3), ("serpentine", 5)]
+    assert ("row", 1) in wl["sweep"] and ("morton", 1) in wl["sweep"]
+    with pytest.raises(SystemExit):
+        bench.resolve_workload(argparse.Namespace(**dict(base, m=64)))
