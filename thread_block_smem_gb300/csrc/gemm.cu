@@ -162,6 +162,8 @@ struct Schedule {
   uint32_t n_half;  // 1 if this cluster takes a half-width tail tile
   uint64_t I;       // Stream-K tail iterations
   uint64_t s, e;    // this cluster's Stream-K tail range [s, e)
+  uint64_t Iq;      // I / P and I % P: range starts are stepped from one
+  uint32_t Ir;      // cluster to the next by addition (64-bit division is slow)
 
   __device__ __forceinline__ void init(uint32_t c_, uint32_t P_, uint32_t U_, uint32_t kb_,
                                        bool sk, bool split) {
@@ -178,8 +180,29 @@ struct Schedule {
     I = sk ? uint64_t(R) * kb : 0u;
     s = range_start(c);
     e = range_start(c + 1);
+    Iq = I / P;
+    Ir = uint32_t(I % P);
   }
   __device__ __forceinline__ uint64_t range_start(uint32_t cc) const { return I * cc / P; }
+  // Walks the range starts of clusters cc, cc + 1, ...: s = range_start(cc),
+  // r = (I * cc) mod P, so that range_start(cc + 1) = s + Iq + carry.
+  struct Cursor {
+    uint64_t s;
+    uint32_t r, cc;
+  };
+  __device__ __forceinline__ Cursor cursor(uint32_t cc) const {
+    const uint64_t t = I * cc;
+    return Cursor{t / P, uint32_t(t % P), cc};
+  }
+  __device__ __forceinline__ void step(Cursor& k) const {
+    k.s += Iq;
+    k.r += Ir;
+    if (k.r >= P) {
+      k.r -= P;
+      ++k.s;
+    }
+    ++k.cc;
+  }
   // The i-th piece of work: unit, K-block range [k0, k1), kind, and which
   // half of the N width (-1: the whole width).
   __device__ __forceinline__ bool item(uint32_t i, uint32_t& unit, uint32_t& k0, uint32_t& k1,
@@ -679,17 +702,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // c+1, c+2, ... whose (non-empty) ranges start inside this tile
         const uint64_t tile_end =
             kind == kFirst ? uint64_t(w - sch.dp_end + 1) * sch.kb : uint64_t(0);
+        const Schedule::Cursor peer0 =
+            kind == kFirst ? sch.cursor(sch.c + 1) : Schedule::Cursor{0, 0, sch.P};
         if (kind == kFirst) {
           bool got = true;
           if (lane == 0) {
-            for (uint32_t cc = sch.c + 1; cc < sch.P; ++cc) {
-              const uint64_t sc = sch.range_start(cc);
-              if (sc >= tile_end) break;
-              if (sc >= sch.range_start(cc + 1)) continue;  // empty range
-              if (!wait_flag(p.sk_flags + (cc * CL + rank) * 4u + q, p.epoch, ctl)) {
+            for (Schedule::Cursor k = peer0; k.cc < sch.P && k.s < tile_end;) {
+              Schedule::Cursor kn = k;
+              sch.step(kn);
+              // a non-empty range starting inside this tile: wait for it
+              if (k.s < kn.s &&
+                  !wait_flag(p.sk_flags + (k.cc * CL + rank) * 4u + q, p.epoch, ctl)) {
                 got = false;
                 break;
               }
+              k = kn;
             }
           }
           got = __shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) != 0;
@@ -713,19 +740,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           float f[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
-          for (uint32_t cc = sch.c + 1; kind == kFirst && cc < sch.P; ++cc) {
-            const uint64_t sc = sch.range_start(cc);
-            if (sc >= tile_end) break;
-            if (sc >= sch.range_start(cc + 1)) continue;
-            const float4* slot = p.sk_ws + size_t(cc * CL + rank) * (BN / 4) * BM;
+          for (Schedule::Cursor k = peer0; kind == kFirst && k.cc < sch.P && k.s < tile_end;) {
+            Schedule::Cursor kn = k;
+            sch.step(kn);
+            if (k.s < kn.s) {  // non-empty range: its partial is in the workspace
+              const float4* slot = p.sk_ws + size_t(k.cc * CL + rank) * (BN / 4) * BM;
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const float4 x = __ldcg(slot + size_t(c / 4 + v) * BM + row_local);
-              f[4 * v] += x.x;
-              f[4 * v + 1] += x.y;
-              f[4 * v + 2] += x.z;
-              f[4 * v + 3] += x.w;
+              for (int v = 0; v < 8; ++v) {
+                const float4 x = __ldcg(slot + size_t(c / 4 + v) * BM + row_local);
+                f[4 * v] += x.x;
+                f[4 * v + 1] += x.y;
+                f[4 * v + 2] += x.z;
+                f[4 * v + 3] += x.w;
+              }
             }
+            k = kn;
           }
           const uint32_t box = stg_warp + uint32_t((c / 32) & 1) * K_::STG_BOX_BYTES;
           // the store that last read this box (two chunks ago) must be done
