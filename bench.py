@@ -70,25 +70,25 @@ SWEEP = WORKLOADS["gemm8192_bf16_pair"]["sweep"]
 # DRAM traffic of one launch of the headline GEMM from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
 # source whose SHA-256 prefix is recorded with it.
-TRAFFIC = {"bytes": 1300006144, "gemm_cu_sha256": "560b96efcc27f81e",
+TRAFFIC = {"bytes": 1299947264, "gemm_cu_sha256": "904681fd60b79d9d",
            "profile": "profiles/gemm_8192_bf16_pair_ncu.md"}
 
 
 # L2 hit rate (lts__t_sector_hit_rate.pct) of one cold launch per order from
 # an ncu capture of `bench.py --only sweep`; valid for the recorded kernel
 # source only.
-L2_NCU = {"gemm_cu_sha256": "560b96efcc27f81e", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
-          ("row", 1): 62.41, ("col", 1): 61.67, ("panel", 4): 67.26, ("panel", 8): 71.52,
-          ("panel", 16): 65.86, ("serpentine", 4): 68.71, ("serpentine", 8): 74.39,
-          ("serpentine", 16): 69.71, ("morton", 1): 68.29, ("xor", 1): 63.66}
+L2_NCU = {"gemm_cu_sha256": "904681fd60b79d9d", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
+          ("row", 1): 62.42, ("col", 1): 62.95, ("panel", 4): 68.59, ("panel", 8): 75.15,
+          ("panel", 16): 65.72, ("serpentine", 4): 68.75, ("serpentine", 8): 73.07,
+          ("serpentine", 16): 69.87, ("morton", 1): 66.21, ("xor", 1): 63.61}
 
 
 # dram__bytes_read.sum of the same captures (one cold launch per order)
-L2_NCU_DRAM = {("row", 1): 2053200896, ("col", 1): 2055177472, ("panel", 4): 1424161024,
-               ("panel", 8): 1095937536, ("panel", 16): 1289179904,
-               ("serpentine", 4): 1277038592, ("serpentine", 8): 1046806528,
-               ("serpentine", 16): 1251909120, ("morton", 1): 1354614528,
-               ("xor", 1): 2056139008}
+L2_NCU_DRAM = {("row", 1): 2054370048, ("col", 1): 2054768896, ("panel", 4): 1417427200,
+               ("panel", 8): 1089470720, ("panel", 16): 1294013184,
+               ("serpentine", 4): 1276849408, ("serpentine", 8): 1049390080,
+               ("serpentine", 16): 1264726784, ("morton", 1): 1367223040,
+               ("xor", 1): 2055344640}
 
 
 def resolve_workload(args):

@@ -741,20 +741,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
           for (Schedule::Cursor k = peer0; kind == kFirst && k.cc < sch.P && k.s < tile_end;) {
-            Schedule::Cursor kn = k;
-            sch.step(kn);
-            if (k.s < kn.s) {  // non-empty range: its partial is in the workspace
-              const float4* slot = p.sk_ws + size_t(k.cc * CL + rank) * (BN / 4) * BM;
+            // two peers per round trip: the owner's fix-up is a chain of
+            // dependent L2 reads at the very end of the kernel
+            Schedule::Cursor k1 = k;
+            sch.step(k1);
+            Schedule::Cursor k2 = k1;
+            if (k1.cc < sch.P) sch.step(k2);
+            const bool v0 = k.s < k1.s;
+            const bool v1 = k1.cc < sch.P && k1.s < tile_end && k1.s < k2.s;
+            const float4* s0 = p.sk_ws + size_t(k.cc * CL + rank) * (BN / 4) * BM;
+            const float4* s1 = p.sk_ws + size_t((v1 ? k1.cc : k.cc) * CL + rank) * (BN / 4) * BM;
+            float4 x0[8], x1[8];
 #pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                const float4 x = __ldcg(slot + size_t(c / 4 + v) * BM + row_local);
-                f[4 * v] += x.x;
-                f[4 * v + 1] += x.y;
-                f[4 * v + 2] += x.z;
-                f[4 * v + 3] += x.w;
-              }
+            for (int v = 0; v < 8; ++v) {
+              const size_t off = size_t(c / 4 + v) * BM + row_local;
+              x0[v] = v0 ? __ldcg(s0 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+              x1[v] = v1 ? __ldcg(s1 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            k = kn;
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              f[4 * v] += x0[v].x;
+              f[4 * v + 1] += x0[v].y;
+              f[4 * v + 2] += x0[v].z;
+              f[4 * v + 3] += x0[v].w;
+              f[4 * v] += x1[v].x;
+              f[4 * v + 1] += x1[v].y;
+              f[4 * v + 2] += x1[v].z;
+              f[4 * v + 3] += x1[v].w;
+            }
+            k = (k1.cc < sch.P && k1.s < tile_end) ? k2 : k1;
           }
           const uint32_t box = stg_warp + uint32_t((c / 32) & 1) * K_::STG_BOX_BYTES;
           // the store that last read this box (two chunks ago) must be done
