@@ -59,6 +59,19 @@ WORKLOADS = {
                                                  ("panel", 8), ("panel", 16),
                                                  ("serpentine", 4), ("serpentine", 8),
                                                  ("serpentine", 16)]),
+    # shared A: 4-CTA clusters of two 128-wide pairs (CTA tiles 128 x 128).  The L2
+    # model sees it at the cluster tile: per 256 x 256 cluster tile A and B are
+    # each requested from L2 once (A by multicast, B in per-CTA quarters) --
+    # the request pattern of the model's 2-CTA cluster of 128 x 256 tiles,
+    # with half as many model CTAs in flight as launched CTAs
+    "gemm6144x10240x4096_fp16_shared_a": dict(M=6144, N=10240, K=4096, dtype="fp16",
+                                              dist="uniform",
+                                              cfg=dict(cta_pair=True, shared_a=True),
+                                              tile=(128, 256), cluster_m=2, tk=128, conc_div=2,
+                                              sweep=[("row", 1), ("col", 1), ("panel", 4),
+                                                     ("panel", 8), ("panel", 16),
+                                                     ("serpentine", 4), ("serpentine", 8),
+                                                     ("serpentine", 16)]),
     "gemm1024x1024x512_fp16": dict(M=1024, N=1024, K=512, dtype="fp16", dist="uniform",
                                    cfg=dict(tile_n=128), tile=(128, 128), cluster_m=1,
                                    sweep=[("row", 1), ("col", 1), ("panel", 4), ("morton", 1),
@@ -71,7 +84,7 @@ SWEEP = WORKLOADS["gemm8192_bf16_pair"]["sweep"]
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
 # source whose SHA-256 prefix is recorded with it.
 TRAFFIC = {"bytes": 1299947264, "gemm_cu_sha256": "904681fd60b79d9d",
-           "profile": "profiles/gemm_8192_bf16_pair_ncu.md"}
+           "workload": "gemm8192_bf16_pair", "profile": "profiles/gemm_8192_bf16_pair_ncu.md"}
 
 
 # L2 hit rate (lts__t_sector_hit_rate.pct) of one cold launch per order from
@@ -375,11 +388,12 @@ def run_swz(args):
                 med = statistics.median(t)
                 # the model at the kernel's tiling: K steps of 64 elements
                 # (two 128-byte atoms, 128 elements, for 128-wide tiles)
-                tk = 128 if wl["tile"][1] == 128 else 64
+                tk = wl.get("tk", 128 if wl["tile"][1] == 128 else 64)
                 # model parameters: the device's L2 and resident programs,
                 # unless overridden (the first page's --l2-cache-mb, --num-sms)
                 model_l2 = int(args.l2_cache_mb * 2**20) if args.l2_cache_mb else l2_bytes
-                model_conc = args.num_sms if args.num_sms else programs  # CTAs in a wave
+                model_conc = ((args.num_sms if args.num_sms else programs)  # CTAs in a wave
+                              // wl.get("conc_div", 1))
                 pred, pred_bytes = swz.l2_model_predict(order, g, M, N, K, wl["tile"][0],
                                                         wl["tile"][1], tk, 2, model_l2,
                                                         model_conc, wl["cluster_m"])
@@ -402,7 +416,7 @@ def run_swz(args):
             for sp in (128, 64, 32):
                 gemm_once(head_order, head_group, sp)
             torch.cuda.synchronize()
-        elif args.only == "all" and not args.no_swizzle:
+        elif args.only == "all" and not args.no_swizzle and not cfg.get("shared_a"):
             for sp in (128, 64, 32):
                 t = timed(lambda: gemm_once(head_order, head_group, sp), max(5, args.steps // 4),
                           3)
@@ -410,7 +424,8 @@ def run_swz(args):
                 spans.append({"span_bytes": sp, "ms": med, "tflops": flops / med / 1e9})
         # ---- static (work_idx striding) vs dynamic (atomic counter) -------
         sched = {}
-        if args.only == "all" and not args.no_dynamic and persistent and not args.stream_k:
+        if (args.only == "all" and not args.no_dynamic and persistent and not args.stream_k
+                and not cfg.get("shared_a")):  # shared A runs the static schedule only
             dws = torch.zeros(256, dtype=torch.uint8, device=dev)
             for name, kw in (("static", {}), ("dynamic", dict(dynamic=True, workspace=dws))):
                 fn = lambda: swz.gemm(Ad, Bd, head_order, head_group, True, out=C, **kw, **cfg)
@@ -426,7 +441,11 @@ def run_swz(args):
     if ms is not None:
         ms_step = max_over_ranks(statistics.mean(ms), dev)
         achieved = flops / statistics.mean(ms) / 1e9
-        traffic = TRAFFIC["bytes"] if TRAFFIC["gemm_cu_sha256"] == _gemm_src_hash() else None
+        # the captured launch is the default workload's headline launch only
+        traffic = (TRAFFIC["bytes"] if TRAFFIC["gemm_cu_sha256"] == _gemm_src_hash()
+                   and args.workload == TRAFFIC["workload"] and persistent
+                   and not args.stream_k and (head_order, head_group) == ("serpentine", 8)
+                   else None)
         line.update({
             "value": world * flops / ms_step / 1e9, "ms_per_step": ms_step,
             "config": {"workload": f"{args.workload}: gemm {M}x{N}x{K} {wl['dtype']} "

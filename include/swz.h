@@ -122,8 +122,8 @@ typedef struct swz_gemm_opts {
                         CTA owns 128 x tile_n of C) -- [CPS] Example 2;
                         0: single CTA                                        */
   int num_programs;  /* persistent only: CTAs to launch (a multiple of 2 with
-                        cta_pair); 0 = resident capacity, capped at the tile
-                        count                                                */
+                        cta_pair, of 4 with shared_a); 0 = resident capacity,
+                        capped at the tile count                             */
   int32_t* d_trace;  /* optional device array, 2 int32 per CTA tile, indexed
                         (cta_m * tiles_n + cta_n): {program (blockIdx.x),
                         iteration of that program's tile loop}               */
@@ -165,6 +165,16 @@ typedef struct swz_gemm_opts {
                         swz_gemm_workspace_size bytes = 256) and is cleared on
                         `stream` before the launch; launches sharing a
                         workspace must not overlap.                          */
+  int shared_a;      /* 1: with cta_pair and tile_n 128 (0 picks 128), 4-CTA
+                        clusters made of two CTA pairs side by side in N
+                        (cluster tile 256 x 256, scheduler grid ceil(M/256) x
+                        ceil(N/256), tile order applied to it).  The two CTAs
+                        that need the same 128 rows of A each load 64 of them
+                        and multicast them to both (TMA .multicast::cluster),
+                        halving A's L2 -> SM traffic.  fp16 / bf16 only, span
+                        128, static schedule (not with stream_k, split_tail
+                        or dynamic: SWZ_EUNSUPPORTED); num_programs a multiple
+                        of 4.  0: off                                        */
 } swz_gemm_opts;
 
 /* debug_flags: withhold the first operand load so that the consumer's
@@ -181,7 +191,10 @@ typedef struct swz_gemm_opts {
  * persistent or with a missing, misaligned (256 B) or too small workspace,
  * and for smem_swizzle not in {0, 32, 64, 128}; for dynamic the same
  * workspace rules, SWZ_EINVAL without persistent or with stream_k or
- * split_tail, SWZ_EUNSUPPORTED with a span other than 128.
+ * split_tail, SWZ_EUNSUPPORTED with a span other than 128; for shared_a
+ * SWZ_EINVAL for a value other than 0 or 1, SWZ_EUNSUPPORTED without cta_pair,
+ * with tile_n 256, TF32, a span other than 128, stream_k, split_tail or
+ * dynamic.
  * In Stream-K mode the trace records, for a split tile, the program that
  * wrote it. */
 int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N, int K,

@@ -186,27 +186,30 @@ def cta_tile(m_idx, n_idx, cta_idx, cluster_m, cluster_n):
     return m_idx * cluster_m + cb_m, n_idx * cluster_n + cb_n
 
 
-def persistent_trace(order, gm, gn, group, num_programs, cluster_m=1):
+def persistent_trace(order, gm, gn, group, num_programs, cluster_m=1, cluster_n=1):
     """What a persistent launch of ``num_programs`` CTAs does, CTA by CTA.
 
-    Programs are grouped into clusters of ``cluster_m`` CTAs along M; the
-    scheduler works on the cluster-tile grid (gm / cluster_m) x gn and every
-    CTA of a cluster takes its own row of the cluster tile ([CPS] Example 2).
-    With cluster_m = 1 and num_programs = tiles this is the non-persistent
-    launch of [TBS] (one program per tile, one loop iteration each).
+    Programs are grouped into clusters of cluster_m x cluster_n CTAs; the
+    scheduler works on the cluster-tile grid (gm / cluster_m) x (gn /
+    cluster_n) and every CTA of a cluster takes its own CTA tile of the
+    cluster tile ([CPS] Example 2: rank -> (rank mod cluster_m, rank div
+    cluster_m)).  With cluster_m = cluster_n = 1 and num_programs = tiles this
+    is the non-persistent launch of [TBS] (one program per tile, one loop
+    iteration each).
 
     Returns {(cta_m, cta_n): (program, iteration)} over all CTA tiles.
     """
-    if gm % cluster_m:
-        raise ValueError("cluster_m must divide gm")
-    num_clusters = num_programs // cluster_m
-    seqs = cluster_sequences(gm // cluster_m, gn, num_clusters, order, group)
+    if gm % cluster_m or gn % cluster_n:
+        raise ValueError("the cluster shape must divide the CTA-tile grid")
+    size = cluster_m * cluster_n
+    num_clusters = num_programs // size
+    seqs = cluster_sequences(gm // cluster_m, gn // cluster_n, num_clusters, order, group)
     trace = {}
     for c, seq in enumerate(seqs):
         for it, (_, m_idx, n_idx) in enumerate(seq):
-            for r in range(cluster_m):
-                prog = c * cluster_m + r
-                key = cta_tile(m_idx, n_idx, prog, cluster_m, 1)
+            for r in range(size):
+                prog = c * size + r
+                key = cta_tile(m_idx, n_idx, prog, cluster_m, cluster_n)
                 if key in trace:
                     raise AssertionError(f"tile {key} visited twice")
                 trace[key] = (prog, it)

@@ -1,0 +1,129 @@
+"""Shared A (cta_pair + shared_a): 4-CTA clusters of two 128-wide CTA pairs
+side by side in N, cluster tiles 256 x 256, CTA tiles 128 x 128.  The two CTAs
+that need the same 128 rows of A each load 64 of them and multicast them to
+both pairs.
+
+Exact on small-integer inputs (ragged M, N and K; a second pair whose columns
+lie partly or wholly beyond N; both B layouts; fp16 and bf16; persistent or
+not); the per-tile trace equals the oracle's persistent schedule on the 2 x 2
+cluster grid; the 6144 x 10240 x 4096 configuration meets the tolerance on
+sampled outputs; the modes it does not provide are refused on the host; an
+expired wait is reported and leaves the context usable.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth_inputs as si
+from gpu_util import MAX_ABS, REL_FRO, errors, require_gpu
+from oracle import ref
+from oracle import tile_order as to
+
+pytestmark = pytest.mark.gpu
+
+SA = dict(cta_pair=True, shared_a=True)
+
+
+@pytest.fixture(scope="module")
+def swz():
+    return require_gpu()
+
+
+@pytest.mark.parametrize("shape", [(300, 392, 200), (256, 256, 64), (1, 8, 8), (129, 136, 72),
+                                   (513, 264, 1000), (768, 640, 576), (200, 96, 136)])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("b_t", [False, True])
+def test_exact_integer(swz, shape, dtype, b_t):
+    M, N, K = shape
+    A, B = si.small_int_gemm_inputs(M, N, K, dtype, lo=-4, hi=4, seed=M + N + K)
+    want = ref.gemm_f64(A, B)
+    Bd = B.t().contiguous().cuda() if b_t else B.cuda()
+    for persistent in (False, True):
+        for order, g in ((to.PANEL, 4), (to.SERPENTINE, 2), (to.ROW, 1)):
+            C = swz.gemm(A.cuda(), Bd, order, g, persistent, b_transposed=b_t, timeout_ms=500,
+                         **SA)
+            swz.check_status()
+            assert torch.equal(C.cpu().double(), want), (shape, persistent, order)
+
+
+@pytest.mark.parametrize("programs", [4, 8, 12])
+def test_persistent_counts(swz, programs):
+    # fewer clusters than cluster tiles: each cluster loops over several
+    M, N, K = 1024, 1280, 320
+    A, B = si.small_int_gemm_inputs(M, N, K, "bf16", lo=-3, hi=3, seed=programs)
+    C = swz.gemm(A.cuda(), B.cuda(), "serpentine", 2, True, num_programs=programs, **SA)
+    swz.check_status()
+    assert torch.equal(C.cpu().double(), ref.gemm_f64(A, B))
+
+
+@pytest.mark.parametrize("order,g", [(to.PANEL, 2), (to.SERPENTINE, 2), (to.ROW, 1),
+                                     (to.COL, 1)])
+@pytest.mark.parametrize("programs", [0, 8, 4])
+def test_trace(swz, order, g, programs):
+    # 768 x 1024 with 256 x 256 cluster tiles: a 3 x 4 cluster grid, 6 x 8 CTA tiles
+    A, B = si.gemm_inputs(768, 1024, 192, "fp16", "uniform", seed=2)
+    trace = torch.full((6 * 8 * 2,), -1, dtype=torch.int32, device="cuda")
+    persistent = programs > 0
+    C = swz.gemm(A.cuda(), B.cuda(), order, g, persistent, num_programs=programs, trace=trace,
+                 **SA)
+    swz.check_status()
+    want = to.persistent_trace(order, 6, 8, g, programs if persistent else 48, cluster_m=2,
+                               cluster_n=2)
+    got = trace.view(6, 8, 2).cpu().tolist()
+    assert {(m, n): tuple(got[m][n]) for m in range(6) for n in range(8)} == want
+    mx, rel = errors(C.cpu().numpy(), ref.gemm_f64(A, B).numpy())
+    assert mx <= MAX_ABS and rel <= REL_FRO
+
+
+def test_same_result_as_pairs(swz):
+    # the same tiles and the same K order per tile: bit-identical to the
+    # 128-wide pair on real-valued inputs
+    A, B = si.gemm_inputs(1000, 1304, 1000, "bf16", "normal", seed=4)
+    Ad, Bd = A.cuda(), B.cuda()
+    C1 = swz.gemm(Ad, Bd, "panel", 4, True, **SA)
+    C2 = swz.gemm(Ad, Bd, "panel", 4, True, cta_pair=True, tile_n=128)
+    swz.check_status()
+    assert torch.equal(C1, C2)
+
+
+def test_refused_modes(swz):
+    A, B = si.small_int_gemm_inputs(256, 256, 64, "fp16", seed=1)
+    Ad, Bd = A.cuda(), B.cuda()
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    for kw in (dict(stream_k=True, workspace=ws), dict(split_tail=True),
+               dict(dynamic=True, workspace=ws), dict(smem_swizzle=64), dict(tile_n=256)):
+        with pytest.raises(swz.SwzError) as e:
+            swz.gemm(Ad, Bd, "row", 1, True, **kw, **SA)
+        assert e.value.code == swz.SWZ_EUNSUPPORTED, kw
+    with pytest.raises(swz.SwzError) as e:
+        swz.gemm(A.float().cuda(), B.float().cuda(), "row", 1, True, **SA)  # TF32
+    assert e.value.code == swz.SWZ_EUNSUPPORTED
+    with pytest.raises(swz.SwzError) as e:
+        swz.gemm(Ad, Bd, "row", 1, True, num_programs=6, **SA)
+    assert e.value.code == swz.SWZ_EINVAL
+
+
+def test_timeout_reported(swz):
+    A, B = si.gemm_inputs(512, 512, 256, "fp16", "uniform", seed=3)
+    Ad, Bd = A.cuda(), B.cuda()
+    swz.gemm(Ad, Bd, "row", 1, True, debug_flags=swz.SWZ_DEBUG_SKIP_FIRST_LOAD, timeout_ms=50,
+             **SA)
+    s = torch.cuda.current_stream().cuda_stream
+    assert swz.swz_check_status(s) == swz.SWZ_ETIMEOUT
+    C = swz.gemm(Ad, Bd, "row", 1, True, **SA)
+    swz.check_status()
+    mx, rel = errors(C.cpu().numpy(), ref.gemm_f64(A, B).numpy())
+    assert mx <= MAX_ABS and rel <= REL_FRO
+
+
+@pytest.mark.parametrize("order,g", [(to.ROW, 1), (to.PANEL, 8), (to.SERPENTINE, 8)])
+def test_cfg4_sampled(swz, order, g):
+    M, N, K = 6144, 10240, 4096
+    A, B = si.gemm_inputs(M, N, K, "fp16", "uniform", seed=0)
+    C = swz.gemm(A.cuda(), B.cuda(), order, g, True, **SA)
+    swz.check_status()
+    ii, jj = si.sample_indices(M, N, 128, 128, 2, seed=11)
+    want = ref.gemm_entries_f64(A, B, ii, jj)
+    got = C[torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()].cpu().double().numpy()
+    assert np.abs(got - want).max() <= MAX_ABS
+    assert np.linalg.norm(got - want) / np.linalg.norm(want) <= REL_FRO

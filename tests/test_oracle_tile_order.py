@@ -156,3 +156,23 @@ def test_persistent_trace_closed_forms():
     for (cm, n), (prog, it) in tr.items():
         w = cids[(cm // 2, n)]
         assert prog == 2 * (w % 4) + cm % 2 and it == w // 4
+
+
+def test_persistent_trace_2x2_clusters():
+    # [CPS] Example 2 with cluster_m = cluster_n = 2: a 6 x 8 CTA grid is a
+    # 3 x 4 cluster grid; rank r of a cluster owns CTA tile (2m + r mod 2,
+    # 2n + r div 2) of cluster tile (m, n)
+    cids = {mn: w for w, mn in enumerate(to.tile_sequence(to.SERPENTINE, 3, 4, 2))}
+    P = 12  # 3 clusters
+    tr = to.persistent_trace(to.SERPENTINE, 6, 8, 2, P, cluster_m=2, cluster_n=2)
+    assert len(tr) == 48
+    for (cm, cn), (prog, it) in tr.items():
+        w = cids[(cm // 2, cn // 2)]
+        assert prog == 4 * (w % 3) + (cm % 2) + 2 * (cn % 2) and it == w // 3
+    # hand-derived: serpentine S=2 on the 3 x 4 cluster grid, id 1 = cluster
+    # tile (0, 1); cluster 1 takes it first (iteration 0); CTA tile (1, 2) is
+    # its row 1, column 0 -> rank 1 -> program 4 + 1
+    assert tr[(1, 2)] == (5, 0)
+    assert tr[(0, 3)] == (6, 0)   # rank 2 of cluster 1: row 0, column 1
+    with pytest.raises(ValueError):
+        to.persistent_trace(to.ROW, 6, 7, 1, 4, cluster_m=2, cluster_n=2)

@@ -53,7 +53,7 @@ class swz_gemm_opts(ctypes.Structure):
                 ("stream_k", ctypes.c_int), ("d_workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_uint64), ("b_layout", ctypes.c_int),
                 ("split_tail", ctypes.c_int), ("smem_swizzle", ctypes.c_int),
-                ("dynamic", ctypes.c_int)]
+                ("dynamic", ctypes.c_int), ("shared_a", ctypes.c_int)]
 
 
 _lib = None
@@ -300,8 +300,9 @@ def tile_map(order, grid_m, grid_n, group=1, device="cuda", stream=None):
 
 def make_opts(dtype=SWZ_F16, tile_n=0, cta_pair=False, num_programs=0, trace=None,
               debug_flags=0, timeout_ms=0, stream_k=False, workspace=None, split_tail=False,
-              b_layout=SWZ_B_KN, smem_swizzle=0, dynamic=False):
+              b_layout=SWZ_B_KN, smem_swizzle=0, dynamic=False, shared_a=False):
     o = swz_gemm_opts()
+    o.shared_a = 1 if shared_a else 0
     o.smem_swizzle = smem_swizzle
     o.dynamic = 1 if dynamic else 0
     o.b_layout = b_layout
@@ -320,10 +321,12 @@ def make_opts(dtype=SWZ_F16, tile_n=0, cta_pair=False, num_programs=0, trace=Non
     return o
 
 
-def gemm_plan(M, N, K, persistent=False, tile_n=0, cta_pair=False, num_programs=0):
+def gemm_plan(M, N, K, persistent=False, tile_n=0, cta_pair=False, num_programs=0,
+              shared_a=False):
     """(tiles_m, tiles_n, sched_m, sched_n, programs) of a GEMM launch."""
     rc, v = swz_gemm_plan(M, N, K, int(bool(persistent)),
-                          make_opts(tile_n=tile_n, cta_pair=cta_pair, num_programs=num_programs))
+                          make_opts(tile_n=tile_n, cta_pair=cta_pair, num_programs=num_programs,
+                                    shared_a=shared_a))
     _check(rc, "swz_gemm_plan")
     return v
 
@@ -352,7 +355,7 @@ def _dtype_code(t):
 def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
          cta_pair=False, num_programs=0, trace=None, debug_flags=0, timeout_ms=0,
          stream_k=False, workspace=None, split_tail=False, b_transposed=False, smem_swizzle=0,
-         dynamic=False, stream=None):
+         dynamic=False, shared_a=False, stream=None):
     """C = A @ B (fp32) through swz_gemm_ex.  A: M x K; B: K x N, or N x K
     when ``b_transposed`` (B stored transposed); both fp16, both bf16, or both
     fp32 (multiplied as TF32); row-major contiguous CUDA tensors.  fp32 inputs
@@ -362,7 +365,9 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
     ``smem_swizzle``: swizzle span of the operand stages, 128 (0), 64 or 32.
     ``dynamic``: claim tiles at run time through an atomic counter kept in
     ``workspace`` (a CUDA tensor of at least workspace_size(..., dynamic=True)
-    bytes); persistent launches only."""
+    bytes); persistent launches only.  ``shared_a`` (with ``cta_pair``):
+    4-CTA clusters of two 128-wide pairs that load each A tile once and
+    multicast it to both."""
     import torch
     if A.dtype != B.dtype:
         raise TypeError("A and B must have the same dtype")
@@ -381,7 +386,7 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
     C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=A.device)
     opts = make_opts(code, tile_n, cta_pair, num_programs, trace, debug_flags, timeout_ms,
                      stream_k, workspace, split_tail, SWZ_B_NK if b_transposed else SWZ_B_KN,
-                     smem_swizzle, dynamic)
+                     smem_swizzle, dynamic, shared_a)
     _check(swz_gemm_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _order(order),
                        group, int(bool(persistent)), opts, _stream(stream)), "swz_gemm_ex")
     return C
@@ -389,7 +394,7 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
 
 def gemm_host(hA, hB, hC, dA, dB, dC, order="panel", group=8, *, tile_n=0, cta_pair=False,
               num_programs=0, stream_k=False, workspace=None, split_tail=False, slabs=0,
-              b_transposed=False, blocks=None, stream=None):
+              b_transposed=False, blocks=None, shared_a=False, stream=None):
     """C = A @ B from host tensors through swz_gemm_host.  hA (M x K), hB
     (K x N, or N x K when ``b_transposed``; always N x K for fp32 / TF32): CPU
     fp16/bf16/fp32 tensors (pinned for overlap); hC: CPU fp32 M x N;
@@ -407,7 +412,8 @@ def gemm_host(hA, hB, hC, dA, dB, dC, order="panel", group=8, *, tile_n=0, cta_p
         raise TypeError("A and B must have the same dtype")
     code = _dtype_code(hA.dtype)
     opts = make_opts(code, tile_n, cta_pair, num_programs, None, 0, 0, stream_k, workspace,
-                     split_tail, SWZ_B_NK if (b_transposed or code == SWZ_TF32) else SWZ_B_KN)
+                     split_tail, SWZ_B_NK if (b_transposed or code == SWZ_TF32) else SWZ_B_KN,
+                     shared_a=shared_a)
     if blocks is not None:  # the growing-square pipeline (swz_gemm_host_tiled)
         _check(swz_gemm_host_tiled(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K,
                                    _order(order), group, opts, dA.data_ptr(), dB.data_ptr(),

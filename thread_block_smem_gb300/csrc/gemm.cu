@@ -28,6 +28,14 @@
 //   * CTA pair (PAIR): 2-CTA cluster, tcgen05 cta_group::2, MMA 256 x BN.
 //     Each CTA loads its own 128 rows of A and its half of B's columns;
 //     the leader issues the MMAs and its commits are multicast to both CTAs.
+//   * Shared A (MCA, with PAIR, 128-wide tiles, 128-byte span): 4-CTA
+//     clusters of two pairs side by side in N (cluster tile 256 x 256).  The
+//     two CTAs that need the same 128 rows of A (cluster ranks r and r + 2)
+//     each load 64 of them and multicast them to both, so each A byte leaves
+//     L2 once per cluster instead of twice: a 128-wide pair reads 1.5x the
+//     operand bytes per FLOP of a 256-wide one, and L2 -> SM delivery, not the
+//     tensor pipe, bounds it.  A stage is refilled only when both pairs'
+//     MMAs have released it (every leader's commit reaches all four CTAs).
 //   * Work items come from the static schedule (Schedule: work_idx striding,
 //     optional Stream-K tail or split tail) or, with DYN, from an atomic
 //     counter published to all roles through a shared-memory ring.
@@ -241,21 +249,22 @@ struct Schedule {
 
 struct Ctl {
   volatile int* abort_flag;
-  uint32_t peer_abort;  // shared::cluster address of the peer's flag (PAIR)
+  uint32_t peer_abort[3];  // shared::cluster addresses of the other CTAs' flags
+  uint32_t n_peers;        // other CTAs in the cluster
   uint64_t timeout_ns;
-  bool pair;
 };
 
 __device__ __noinline__ void raise_abort(const Ctl& c) {
   atomicCAS(&g_status_word, 0u, 1u);
   *c.abort_flag = 1;
-  if (c.pair) asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(c.peer_abort), "r"(1) : "memory");
+  for (uint32_t j = 0; j < c.n_peers; ++j)
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(c.peer_abort[j]), "r"(1) : "memory");
 }
 
 // Waits for the phase of `bar` with parity `parity`; false if the kernel
 // is aborting or the bound expired (then the abort is raised).
 __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Ctl& c) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  if (ptx::mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = ptx::global_timer_ns();
   for (uint32_t n = 1;; ++n) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -291,7 +300,7 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
   while (ptx::global_timer_ns() - t0 < ns) __nanosleep(1000);
 }
 
-template <int BN, bool PAIR, int KIND, int SW, bool DYN>
+template <int BN, bool PAIR, int KIND, int SW, bool DYN, bool MCA = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3,
@@ -299,7 +308,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int KA = SW == 128 ? stage_atoms(BN) : 1;
   using K_ = Cfg<BN, PAIR, KA>;
   constexpr int CL = K_::CG;
+  constexpr int NP = MCA ? 2 : 1;  // CTA pairs per cluster, side by side in N
+  constexpr int CLN = CL * NP;     // CTAs per cluster
   constexpr int STAGES = K_::STAGES;
+  static_assert(!MCA || (PAIR && BN == 128 && SW == 128 && !DYN), "shared-A configuration");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -321,20 +333,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* ring_w = tmem_slot + 2;
 
   const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
+  const uint32_t crank = PAIR ? ptx::cluster_ctarank() : 0u;  // rank in the cluster
+  const uint32_t rank = crank & 1u;   // rank in the CTA pair: which 128 rows of the pair's tile
+  const uint32_t pidx = crank >> 1;   // pair index (MCA): which 128 columns of the cluster tile
+  const uint32_t lead = crank & ~1u;  // cluster rank of the pair's leader
   const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
     ptx::prefetch_tensormap(&tmA);
-    if constexpr (SW != 128) {
-      if (p.a3d) ptx::prefetch_tensormap(&tmA3);
+    if constexpr (SW != 128 || MCA) {
+      if (MCA || p.a3d) ptx::prefetch_tensormap(&tmA3);
     }
     ptx::prefetch_tensormap(&tmB);
     if (p.b3d) ptx::prefetch_tensormap(&tmB3);
     ptx::prefetch_tensormap(&tmC);
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), 1);
+      ptx::mbar_init(empty_bar(s), NP);  // one commit from each pair's leader
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(tfull_bar(a), 1);
@@ -365,13 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   Ctl ctl;
   ctl.abort_flag = abort_flag;
-  ctl.peer_abort = PAIR ? ptx::map_to_rank(ptx::smem_u32(abort_flag), rank ^ 1u) : 0u;
+  ctl.n_peers = CLN - 1;
+  for (uint32_t j = 1; j < uint32_t(CLN); ++j)
+    ctl.peer_abort[j - 1] = ptx::map_to_rank(ptx::smem_u32(abort_flag), crank ^ j);
   ctl.timeout_ns = p.timeout_ns;
-  ctl.pair = PAIR;
 
   const uint32_t units = p.sched_m * p.sched_n;
   Schedule sch;
-  sch.init(blockIdx.x / CL, gridDim.x / CL, units, p.num_kb, p.stream_k != 0,
+  sch.init(blockIdx.x / CLN, gridDim.x / CLN, units, p.num_kb, p.stream_k != 0,
            p.split_tail != 0);
   bool aborted = false;
 
@@ -468,7 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t m0 = int32_t((t.m * CL + rank) * BM);
         // B columns this CTA loads: its share of the tile (or of one half)
         const int local = half < 0 ? K_::BN_LOCAL : K_::BN_LOCAL / 2;
-        const int32_t n0 = int32_t(t.n * BN + (half < 0 ? 0 : half * (BN / 2)) + rank * local);
+        const int32_t n0 = int32_t((t.n * NP + pidx) * BN + (half < 0 ? 0 : half * (BN / 2)) +
+                                   rank * local);
         const int boxes = local / xn;  // xn = 64 when sw == 128
         const uint32_t tx = uint32_t(CL) * uint32_t(K_::A_BYTES + local * 128 * KA);
         for (uint32_t kb = kbeg; kb < kend; ++kb) {
@@ -477,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (skip) {
             skip = false;
           } else {
-            const uint32_t fb = PAIR ? ptx::map_to_rank(full_bar(stage), 0) : full_bar(stage);
+            const uint32_t fb = PAIR ? ptx::map_to_rank(full_bar(stage), lead) : full_bar(stage);
             const int32_t k0 = int32_t(kb * bk_elems<KIND>() * KA);
             const uint32_t a_dst = sA + stage * K_::A_BYTES, b_dst = sB + stage * K_::B_BYTES;
             // A: one box of 128 rows per column group, or one 3-D box
@@ -493,9 +510,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               // N-major B: boxes of 64 columns x BK * KA rows
               constexpr int ke = bk_elems<KIND>();
               if constexpr (PAIR) {
+                if constexpr (MCA) {
+                  // rows 64*pidx .. +63 of this CTA's A block, multicast to
+                  // this CTA and the one at rank ^ 2 (same rows, other pair);
+                  // tmA3 holds the 64-row box
+                  const uint16_t mask = uint16_t(0x5u << rank);
 #pragma unroll
-                for (int g = 0; g < KA; ++g)
-                  ptx::tma_load_2d_pair(a_dst + g * (BM * 128), &tmA, fb, k0 + g * ke, m0);
+                  for (int g = 0; g < KA; ++g)
+                    ptx::tma_load_2d_pair_mc(a_dst + g * (BM * 128) + pidx * (64 * 128), &tmA3, fb,
+                                             k0 + g * ke, m0 + int32_t(pidx * 64), mask);
+                } else {
+#pragma unroll
+                  for (int g = 0; g < KA; ++g)
+                    ptx::tma_load_2d_pair(a_dst + g * (BM * 128), &tmA, fb, k0 + g * ke, m0);
+                }
                 if (p.b_kmajor)
 #pragma unroll
                   for (int g = 0; g < KA; ++g)
@@ -601,17 +629,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             b_step[kk] = p.b_kmajor ? kmajor_off(kk, b_rows) : uint64_t((16u * sw * kk) >> 4);
           }
         }
-        // Unrolled: the single issuing thread's per-stage loop overhead is
-        // on the critical path (a stage of 4 MMAs is 256-512 tensor cycles
-        // and the barrier wait, four issues and the commit take ~450 of
-        // them); unrolling by 8 cut it by 3 % (256-wide pair) to 17 %
-        // (128-wide pair).
-#pragma unroll 8
-        for (uint32_t kb = kbeg; kb < kend; ++kb) {
-          if (!wait(full_bar(stage), phase, ctl)) { aborted = true; break; }
-          ptx::tc_fence_after();
-          const uint32_t a_addr = sA + stage * K_::A_BYTES;
-          const uint32_t b_addr = sB + stage * K_::B_BYTES;
+        // One stage's MMAs (4 * KA k-slices of 16 / 8 elements) and the
+        // commit that releases the stage when they complete.
+        auto issue_stage = [&](uint32_t st, bool first) {
+          const uint32_t a_addr = sA + st * K_::A_BYTES;
+          const uint32_t b_addr = sB + st * K_::B_BYTES;
           if constexpr (SW == 128) {
             // slice kk of the KA atoms: atom kk / 4, 32 bytes per slice
             // inside it; N-major B: 16 K-rows of 128 bytes per slice
@@ -619,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bdesc = p.b_kmajor ? make_sdesc(b_addr, 16, 1024, 2)
                                               : make_sdesc(b_addr, BK * KA * 128, 1024, 2);
             const uint32_t b_atom = b_rows * 128u;  // K-major B: bytes of one atom
-            ptx::mma<CL, KIND>(d, adesc, bdesc, idesc, kb != kbeg ? 1u : 0u);
+            ptx::mma<CL, KIND>(d, adesc, bdesc, idesc, first ? 0u : 1u);
 #pragma unroll
             for (int kk = 1; kk < 4 * KA; ++kk) {
               const uint64_t ao = uint64_t(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4);
@@ -632,25 +654,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t adesc = make_sdesc(a_addr, 16, 8 * sw, lay);
             const uint64_t bdesc = p.b_kmajor ? make_sdesc(b_addr, 16, 8 * sw, lay)
                                               : make_sdesc(b_addr, BK * sw, 8 * sw, lay);
-            ptx::mma<CL, KIND>(d, adesc, bdesc, idesc, kb != kbeg ? 1u : 0u);
+            ptx::mma<CL, KIND>(d, adesc, bdesc, idesc, first ? 0u : 1u);
 #pragma unroll
             for (int kk = 1; kk < 4; ++kk)
               ptx::mma<CL, KIND>(d, adesc + a_step[kk], bdesc + b_step[kk], idesc, 1u);
           }
           issued = true;
-          if constexpr (PAIR) ptx::mma_commit_pair(empty_bar(stage), 0x3);
-          else ptx::mma_commit(empty_bar(stage));
+          // the stage is free once every pair that reads it is done: MCA
+          // stages also hold A that the other pair's CTAs loaded
+          if constexpr (PAIR) ptx::mma_commit_pair(empty_bar(st), MCA ? 0xF : 0x3);
+          else ptx::mma_commit(empty_bar(st));
+        };
+        // The issuing thread is the critical path: an MMA takes nearly as
+        // long to issue as a 128-wide one takes to run (64 tensor cycles),
+        // and every barrier test and branch between MMAs leaves the tensor
+        // pipe idle, so the k-loop is unrolled and the barrier test that
+        // usually succeeds is the non-blocking one.  (Taking the two-atom
+        // stages two at a time, 16 MMAs per test, was slower: a stage then
+        // waits for its successor's data too, which halves the time the
+        // producer has to refill every other stage.)
+#pragma unroll 8
+        for (uint32_t kb = kbeg; kb < kend; ++kb) {
+          if (!wait(full_bar(stage), phase, ctl)) { aborted = true; break; }
+          ptx::tc_fence_after();
+          issue_stage(stage, kb == kbeg);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (aborted) break;
-        if constexpr (PAIR) ptx::mma_commit_pair(tfull_bar(acc), 0x3);
+        if constexpr (PAIR) ptx::mma_commit_pair(tfull_bar(acc), uint16_t(0x3u << lead));
         else ptx::mma_commit(tfull_bar(acc));
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       if (aborted && issued) {
         // drain: wait (bounded) until every MMA issued so far has completed
-        if constexpr (PAIR) ptx::mma_commit_pair(drain_bar, 0x1);
+        if constexpr (PAIR) ptx::mma_commit_pair(drain_bar, uint16_t(1u << lead));
         else ptx::mma_commit(drain_bar);
         const uint64_t t0 = ptx::global_timer_ns();
         while (!ptx::mbar_try_wait(drain_bar, 0) && ptx::global_timer_ns() - t0 < p.timeout_ns) {
@@ -674,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xFFFFFFFFu, ok)) { aborted = true; break; }
       ptx::tc_fence_after();
       const TileCoord t = tile_of(p.order, w, p.sched_m, p.sched_n, uint32_t(p.group));
-      const uint32_t cta_m = t.m * CL + rank, cta_n = t.n;
+      const uint32_t cta_m = t.m * CL + rank, cta_n = t.n * NP + pidx;
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + acc * BN;
       if (kind == kPartial) {
         float4* slot = p.sk_ws + size_t(sch.c * CL + rank) * (BN / 4) * BM;
@@ -693,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
+          if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), lead));
           else ptx::mbar_arrive(tempty_bar(acc));
           ptx::st_release_gpu(p.sk_flags + (sch.c * CL + rank) * 4u + q, p.epoch);
         }
@@ -792,10 +830,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
+          if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), lead));
           else ptx::mbar_arrive(tempty_bar(acc));
           if (warp == 2 && p.trace) {
-            const uint64_t idx = uint64_t(cta_m) * p.sched_n + cta_n;
+            const uint64_t idx = uint64_t(cta_m) * (p.sched_n * NP) + cta_n;
             p.trace[2 * idx] = int32_t(blockIdx.x);
             p.trace[2 * idx + 1] = int32_t(i);
           }
@@ -899,13 +937,15 @@ static int encode_groups(CUtensorMap* map, int dtype, const void* base, uint64_t
 struct Plan {
   int bn;
   bool pair;
+  bool mca;  // 4-CTA clusters of two pairs sharing A
   uint32_t tiles_m, tiles_n, sched_m, sched_n, units;
   int programs;
 };
 
-template <int BN, bool PAIR, int KIND>
+template <int BN, bool PAIR, int KIND, bool MCA = false>
 static int kernel_capacity(const DeviceInfo& dev, int* programs) {
   constexpr int SW = 128;
+  constexpr int CLN = (PAIR ? 2 : 1) * (MCA ? 2 : 1);
   using K_ = Cfg<BN, PAIR, stage_atoms(BN)>;
   static std::mutex mu;
   static int cache[64] = {};
@@ -916,25 +956,27 @@ static int kernel_capacity(const DeviceInfo& dev, int* programs) {
       return SWZ_OK;
     }
   }
-  auto kern = gemm_kernel<BN, PAIR, KIND, SW, false>;
+  auto kern = gemm_kernel<BN, PAIR, KIND, SW, false, MCA>;
   SWZ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     K_::SMEM_BYTES));
   int cap = 0;
   if constexpr (PAIR) {
+    // clusters of CLN CTAs fit a GPC only whole: with 4 the count can leave
+    // SMs idle (GPCs whose SM count is not a multiple of 4)
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * dev.num_sms);
+    cfg.gridDim = dim3(CLN * dev.num_sms);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = K_::SMEM_BYTES;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = CLN;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int clusters = 0;
     SWZ_CUDA_TRY(cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg));
-    cap = 2 * clusters;
+    cap = CLN * clusters;
   } else {
     int per_sm = 0;
     SWZ_CUDA_TRY(
@@ -951,6 +993,7 @@ static int kernel_capacity(const DeviceInfo& dev, int* programs) {
 static int capacity_for(const Plan& pl, const DeviceInfo& dev, int* cap) {
   // the three configurations share their shared-memory footprint across
   // kinds, so the f16 kernels' residency stands for both
+  if (pl.mca) return kernel_capacity<128, true, 0, true>(dev, cap);
   if (pl.pair) {
     if (pl.bn == 128) return kernel_capacity<128, true, 0>(dev, cap);
     return kernel_capacity<256, true, 0>(dev, cap);
@@ -962,20 +1005,26 @@ static int capacity_for(const Plan& pl, const DeviceInfo& dev, int* cap) {
 static int make_plan(int M, int N, int persistent, const swz_gemm_opts& o, const DeviceInfo* dev,
                      Plan* pl) {
   if (o.tile_n != 0 && o.tile_n != 128 && o.tile_n != 256) return SWZ_EUNSUPPORTED;
+  if (o.shared_a != 0 && o.shared_a != 1) return SWZ_EINVAL;
   pl->pair = o.cta_pair != 0;
-  pl->bn = o.tile_n ? o.tile_n : (pl->pair || N > 128 ? 256 : 128);
-  const int cl = pl->pair ? 2 : 1;
+  pl->mca = o.shared_a != 0;
+  // shared A: two 128-wide pairs per cluster
+  if (pl->mca && (!pl->pair || o.tile_n == 256)) return SWZ_EUNSUPPORTED;
+  pl->bn = o.tile_n ? o.tile_n : (pl->mca ? 128 : pl->pair || N > 128 ? 256 : 128);
+  const int np = pl->mca ? 2 : 1;       // pairs side by side in N
+  const int cl = pl->pair ? 2 : 1;      // CTAs of a pair, stacked in M
+  const int cln = cl * np;              // CTAs per cluster
   const uint64_t sm = (uint64_t(M) + BM * cl - 1) / (BM * cl);
-  const uint64_t sn = (uint64_t(N) + pl->bn - 1) / pl->bn;
-  if (sm * sn * cl > uint64_t(INT32_MAX)) return SWZ_EINVAL;
+  const uint64_t sn = (uint64_t(N) + uint64_t(pl->bn) * np - 1) / (uint64_t(pl->bn) * np);
+  if (sm * sn * cln > uint64_t(INT32_MAX)) return SWZ_EINVAL;
   pl->sched_m = uint32_t(sm);
   pl->sched_n = uint32_t(sn);
   pl->tiles_m = uint32_t(sm * cl);
-  pl->tiles_n = uint32_t(sn);
+  pl->tiles_n = uint32_t(sn * np);
   pl->units = uint32_t(sm * sn);
-  if (o.num_programs < 0 || (o.num_programs % cl) != 0) return SWZ_EINVAL;
+  if (o.num_programs < 0 || (o.num_programs % cln) != 0) return SWZ_EINVAL;
   if (!persistent) {
-    pl->programs = int(pl->units) * cl;
+    pl->programs = int(pl->units) * cln;
   } else {
     int cap = o.num_programs;
     if (cap == 0) {
@@ -983,8 +1032,8 @@ static int make_plan(int M, int N, int persistent, const swz_gemm_opts& o, const
       const int rc = capacity_for(*pl, *dev, &cap);
       if (rc != SWZ_OK) return rc;
     }
-    const uint32_t units_cap = uint32_t(cap / cl);
-    pl->programs = int(pl->units < units_cap ? pl->units : units_cap) * cl;
+    const uint32_t units_cap = uint32_t(cap / cln);
+    pl->programs = int(pl->units < units_cap ? pl->units : units_cap) * cln;
   }
   return SWZ_OK;
 }
@@ -1010,14 +1059,14 @@ static SkLayout sk_layout(const Plan& pl, int persistent, const swz_gemm_opts& o
   return L;
 }
 
-template <int BN, bool PAIR, int KIND, int SW, bool DYN>
+template <int BN, bool PAIR, int KIND, int SW, bool DYN, bool MCA = false>
 static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& ta3,
                   const CUtensorMap& tb, const CUtensorMap& tb3, const CUtensorMap& tc,
                   const Params& prm, cudaStream_t stream) {
   using K_ = Cfg<BN, PAIR, SW == 128 ? stage_atoms(BN) : 1>;
   static std::mutex mu;
   static bool attr_set[64] = {};
-  auto kern = gemm_kernel<BN, PAIR, KIND, SW, DYN>;
+  auto kern = gemm_kernel<BN, PAIR, KIND, SW, DYN, MCA>;
   int dev = 0;
   SWZ_CUDA_TRY(cudaGetDevice(&dev));
   {
@@ -1036,7 +1085,7 @@ static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& ta3,
   cudaLaunchAttribute attr[1];
   if constexpr (PAIR) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = MCA ? 4 : 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -1057,6 +1106,10 @@ template <int SW, bool DYN>
 static int dispatch(const Plan& pl, bool tf32, const CUtensorMap& ta, const CUtensorMap& ta3,
                     const CUtensorMap& tb, const CUtensorMap& tb3, const CUtensorMap& tc,
                     const Params& prm, cudaStream_t s) {
+  if constexpr (SW == 128 && !DYN) {
+    if (pl.mca) return launch<128, true, 0, SW, DYN, true>(pl, ta, ta3, tb, tb3, tc, prm, s);
+  }
+  if (pl.mca) return SWZ_EUNSUPPORTED;
   if (tf32) {
     if (pl.pair && pl.bn == 128)
       return launch<128, true, 1, SW, DYN>(pl, ta, ta3, tb, tb3, tc, prm, s);
@@ -1191,6 +1244,9 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   if (o.dtype == SWZ_TF32 && o.b_layout != SWZ_B_NK) return SWZ_EUNSUPPORTED;
   const bool tf32 = o.dtype == SWZ_TF32;
   const uint32_t span = o.smem_swizzle ? uint32_t(o.smem_swizzle) : 128u;
+  // shared A: 16-bit operands, the 128-byte span, the static whole-tile schedule
+  if (pl.mca && (tf32 || span != 128 || o.stream_k || o.split_tail || o.dynamic))
+    return SWZ_EUNSUPPORTED;
   const uint32_t esize = tf32 ? 4u : 2u;
   const uint32_t bke = 128u / esize;  // K elements per 128-byte stage row
   const uint32_t xe = span / esize;   // elements per swizzle span
@@ -1207,6 +1263,10 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   ta3 = ta;
   if (a3d) {
     rc = encode_groups(&ta3, o.dtype, A, uint64_t(M), uint64_t(K), xe, BM, 128 / span, span);
+    if (rc != SWZ_OK) return rc;
+  } else if (pl.mca) {
+    // shared A: each CTA loads half of a 128-row block (64-row boxes)
+    rc = encode_2d(&ta3, o.dtype, A, uint64_t(M), uint64_t(K), xe, BM / 2, span);
     if (rc != SWZ_OK) return rc;
   }
   bool b3d = false;
