@@ -613,6 +613,23 @@ def run_swz(args):
                 rec["peak_loaded_tflops"] = sms * fpc * load_mhz / 1e6
             tc[name] = rec
             del At, Bt
+        # the issuing thread's stage loop: per stage a barrier test, the
+        # tensor fence, S MMAs and a commit (swz_tc_rate_ex), 2-CTA MMAs of
+        # 256 x 128 and 256 x 256; fraction of the back-to-back rate above
+        g = torch.Generator().manual_seed(1)
+        At = (torch.rand((128, 64), generator=g) * 2 - 1).to(torch.bfloat16).to(dev)
+        Bt = (torch.rand((256, 64), generator=g) * 2 - 1).to(torch.bfloat16).to(dev)
+        issue = []
+        for n, stage in ((128, 0), (128, 4), (128, 8), (128, 16), (256, 4), (256, 8)):
+            times, flop, _ = swz.tc_rate(At, Bt[:n].contiguous(), 16384, cta_pair=True,
+                                         mmas_per_stage=stage)
+            cyc = times[:, 0].double()
+            f = float((16384 * flop / cyc).median())
+            issue.append({"mma": f"256x{n}x16 bf16, CTA pair", "mmas_per_stage": stage,
+                          "cycles_per_mma": float((cyc / 16384).median()),
+                          "frac_of_rate": f / tc["bf16"]["flop_per_clk_per_sm"]})
+        tc["issue_loop"] = issue
+        del At, Bt
         if "roofline" in line and "peak_max_clock_tflops" in tc["bf16"]:
             a = line["roofline"]["achieved"]
             tc["headline_frac_of_bf16_max_clock_peak"] = a / tc["bf16"]["peak_max_clock_tflops"]

@@ -390,6 +390,31 @@ int swz_gemm_streamk_noalloc(const void* A, const void* B, float* C, int M, int 
 int swz_tc_rate(int dtype, int n, const void* A, const void* B, int n_mma, int num_ctas,
                 uint64_t* d_times, float* d_D, void* stream);
 
+/*
+ * swz_tc_rate_ex -- swz_tc_rate (= cta_pair 0, mmas_per_stage 0) with two
+ * more shapes of the issue loop, to measure what the GEMM's single issuing
+ * thread can sustain:
+ *   cta_pair        1: 2-CTA clusters, tcgen05 cta_group::2 MMAs of 256 x n x
+ *                   k issued by the even CTA of each pair; CTA 2i+r holds A
+ *                   (both CTAs the same 128 rows) and B rows r*n/2 .. +n/2-1.
+ *                   n 128 or 256; num_ctas even (0 = the SM count rounded
+ *                   down to even).
+ *   mmas_per_stage  0: n_mma MMAs back to back.  4, 8 or 16: the loop is cut
+ *                   into stages as in the GEMM -- per stage a non-blocking
+ *                   test of a barrier whose phase is already complete (it
+ *                   never waits), the tensor fence, that many MMAs and a
+ *                   commit -- unrolled by 8; n_mma % mmas_per_stage == 0.
+ * d_times holds one record per issuing CTA (num_ctas / 2 with cta_pair), in
+ * the format of swz_tc_rate; d_D is CTA 0's accumulator (rows 0..127 of a
+ * pair's 256) with the same identity.  FLOP / clock / SM = n_mma * 2 * 128 *
+ * n * k / cycles in both modes (a pair's MMA is two SMs' work).  Errors: as
+ * swz_tc_rate; SWZ_EINVAL for cta_pair or mmas_per_stage out of range;
+ * SWZ_EUNSUPPORTED for SWZ_TF32 with a pair or stages.
+ */
+int swz_tc_rate_ex(int dtype, int n, int cta_pair, int mmas_per_stage, const void* A,
+                   const void* B, int n_mma, int num_ctas, uint64_t* d_times, float* d_D,
+                   void* stream);
+
 /* Synchronises `stream`, then returns and clears the current device's
  * status word: SWZ_OK, or SWZ_ETIMEOUT if a kernel's bounded wait expired
  * since the last check. */

@@ -80,3 +80,61 @@ def test_tc_rate_errors(swz):
     assert swz.swz_tc_rate(7, 256, n_mma=4, num_ctas=1, **args) == swz.SWZ_EINVAL
     assert swz.swz_tc_rate(swz.SWZ_BF16, 256, Ad.data_ptr() + 8, Bd.data_ptr(), 4, 1,
                            t.data_ptr(), None, s) == swz.SWZ_EINVAL
+
+
+@pytest.mark.parametrize("n", [128, 256])
+@pytest.mark.parametrize("stage", [0, 4, 8, 16])
+@pytest.mark.parametrize("pair", [False, True])
+def test_pair_and_stage_modes_exact(swz, n, stage, pair):
+    # a pair's MMA is 256 x n: CTA 0 holds rows 0..127 of the accumulator and
+    # B's columns come half from each CTA; stages change only the issue loop
+    A, B = _operands("bf16", n, seed=n + stage)
+    n_mma = 32
+    times, flop, D = swz.tc_rate(A.cuda(), B.cuda(), n_mma, num_ctas=4, read_acc=True,
+                                 cta_pair=pair, mmas_per_stage=stage)
+    assert times.shape == ((2 if pair else 4), 4)
+    assert (times[:, 3] == 0).all()
+    assert torch.equal(D.cpu().double(), ref.gemm_f64(A, B.t().contiguous()) * (n_mma // 4))
+
+
+def test_stage_loop_rates(swz):
+    # back to back, a pair's MMAs run at the one-CTA rate per SM; cutting the
+    # loop into stages never makes it faster than that, and stages of 16
+    # 128-wide MMAs keep at least 90 % of it
+    A, B = _operands("bf16", 256, seed=5)
+    Ad, Bd = A.cuda(), B.cuda()
+    swz.tc_rate(Ad, Bd, 1024)  # warm-up
+
+    def fpc(n, pair, stage):
+        t, flop, _ = swz.tc_rate(Ad, Bd[:n].contiguous(), 16384, cta_pair=pair,
+                                 mmas_per_stage=stage)
+        assert (t[:, 3] == 0).all()
+        return (16384 * flop / t[:, 0].double()).median().item()
+
+    base = fpc(256, False, 0)
+    assert abs(fpc(256, True, 0) / base - 1.0) < 0.03
+    for stage in (4, 8, 16):
+        assert fpc(128, True, stage) <= base * 1.03
+    assert fpc(128, True, 16) >= 0.9 * base
+
+
+def test_tc_rate_ex_errors(swz):
+    A, B = _operands("bf16", 256, seed=2)
+    Ad, Bd = A.cuda(), B.cuda()
+    t = torch.zeros(4 * 4, dtype=torch.int64, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    E, U = swz.SWZ_EINVAL, swz.SWZ_EUNSUPPORTED
+
+    def call(dtype=swz.SWZ_BF16, n=256, pair=0, stage=0, n_mma=16, ctas=2):
+        return swz.swz_tc_rate_ex(dtype, n, pair, stage, Ad.data_ptr(), Bd.data_ptr(), n_mma,
+                                  ctas, t.data_ptr(), None, s)
+
+    assert call(stage=5) == E
+    assert call(stage=8, n_mma=12) == E        # not a whole number of stages
+    assert call(pair=2) == E
+    assert call(pair=1, n=64) == E             # a pair's MMA is 128 or 256 wide
+    assert call(pair=1, ctas=3) == E           # whole pairs only
+    assert call(dtype=swz.SWZ_TF32, pair=1) == U
+    assert call(dtype=swz.SWZ_TF32, stage=4) == U
+    assert call() == swz.SWZ_OK
+    swz.check_status()

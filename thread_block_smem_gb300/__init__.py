@@ -36,6 +36,7 @@ EXPORTS = ["swz_tile_map", "swz_is_bijective", "swz_gemm", "swz_gemm_ex", "swz_g
            "swz_transpose", "swz_check_status", "swz_strerror", "swz_last_cuda_error",
            "swz_device_info", "swz_l2_model", "swz_gemm_workspace_size",
            "swz_gemm_streamk_noalloc", "swz_gemm_host", "swz_gemm_mma_sync", "swz_tc_rate",
+           "swz_tc_rate_ex",
            "swz_l2_model_bytes", "swz_gemm_host_tiled"]
 
 
@@ -93,6 +94,7 @@ def lib() -> ctypes.CDLL:
         L.swz_gemm_host_tiled.argtypes = L.swz_gemm_host.argtypes
         L.swz_gemm_mma_sync.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, i, i, vp]
         L.swz_tc_rate.argtypes = [i, i, vp, vp, i, i, vp, vp, vp]
+        L.swz_tc_rate_ex.argtypes = [i, i, i, i, vp, vp, i, i, vp, vp, vp]
         for name in EXPORTS:
             if name != "swz_strerror":
                 getattr(L, name).restype = ctypes.c_int
@@ -187,12 +189,21 @@ def swz_tc_rate(dtype, n, A, B, n_mma, num_ctas, d_times, d_D=None, stream=0):
     return lib().swz_tc_rate(dtype, n, A, B, n_mma, num_ctas, d_times, d_D, stream)
 
 
-def tc_rate(A, B, n_mma, num_ctas=0, read_acc=False, stream=None):
-    """Runs swz_tc_rate on CUDA operand tiles A (128 x 64 fp16/bf16 or
+def swz_tc_rate_ex(dtype, n, cta_pair, mmas_per_stage, A, B, n_mma, num_ctas, d_times,
+                   d_D=None, stream=0):
+    return lib().swz_tc_rate_ex(dtype, n, cta_pair, mmas_per_stage, A, B, n_mma, num_ctas,
+                                d_times, d_D, stream)
+
+
+def tc_rate(A, B, n_mma, num_ctas=0, read_acc=False, stream=None, cta_pair=False,
+            mmas_per_stage=0):
+    """Runs swz_tc_rate_ex on CUDA operand tiles A (128 x 64 fp16/bf16 or
     128 x 32 fp32) and B (n x 64 / n x 32, B stored N x K).  Returns the
-    per-CTA records as a CPU int64 tensor of shape (ctas, 4) -- cycles, ns,
-    SM id, status -- the FLOP of one instruction, and CTA 0's accumulator
-    (128 x n fp32 CUDA tensor) when ``read_acc``."""
+    records of the issuing CTAs as a CPU int64 tensor of shape (records, 4)
+    -- cycles, ns, SM id, status -- the FLOP one SM does per instruction,
+    and CTA 0's accumulator (128 x n fp32 CUDA tensor) when ``read_acc``.
+    ``cta_pair``: 2-CTA MMAs of 256 x n; ``mmas_per_stage``: 4, 8 or 16 cuts
+    the issue loop into stages as the GEMM's is (0: back to back)."""
     import torch
     code = _dtype_code(A.dtype)
     if B.dtype != A.dtype or not (A.is_contiguous() and B.is_contiguous()):
@@ -201,12 +212,14 @@ def tc_rate(A, B, n_mma, num_ctas=0, read_acc=False, stream=None):
     n = B.shape[0]
     if tuple(A.shape) != (128, k_row) or tuple(B.shape) != (n, k_row):
         raise ValueError("A must be 128 x (128 bytes), B n x (128 bytes)")
-    ctas = num_ctas or swz_device_info()[1][0]
-    times = torch.zeros((ctas, 4), dtype=torch.int64, device=A.device)
+    cg = 2 if cta_pair else 1
+    ctas = num_ctas or swz_device_info()[1][0] // cg * cg
+    times = torch.zeros((ctas // cg, 4), dtype=torch.int64, device=A.device)
     D = torch.zeros((128, n), dtype=torch.float32, device=A.device) if read_acc else None
-    _check(swz_tc_rate(code, n, A.data_ptr(), B.data_ptr(), n_mma, ctas, times.data_ptr(),
-                       D.data_ptr() if D is not None else None, _stream(stream)),
-           "swz_tc_rate")
+    _check(swz_tc_rate_ex(code, n, int(bool(cta_pair)), mmas_per_stage, A.data_ptr(),
+                          B.data_ptr(), n_mma, ctas, times.data_ptr(),
+                          D.data_ptr() if D is not None else None, _stream(stream)),
+           "swz_tc_rate_ex")
     k = 8 if code == SWZ_TF32 else 16
     return times.cpu(), 2 * 128 * n * k, D
 
