@@ -83,25 +83,25 @@ SWEEP = WORKLOADS["gemm8192_bf16_pair"]["sweep"]
 # DRAM traffic of one launch of the headline GEMM from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
 # source whose SHA-256 prefix is recorded with it.
-TRAFFIC = {"bytes": 1299947264, "gemm_cu_sha256": "904681fd60b79d9d",
+TRAFFIC = {"bytes": 1299243008, "gemm_cu_sha256": "1f3782b899ee4e8e",
            "workload": "gemm8192_bf16_pair", "profile": "profiles/gemm_8192_bf16_pair_ncu.md"}
 
 
 # L2 hit rate (lts__t_sector_hit_rate.pct) of one cold launch per order from
 # an ncu capture of `bench.py --only sweep`; valid for the recorded kernel
 # source only.
-L2_NCU = {"gemm_cu_sha256": "904681fd60b79d9d", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
-          ("row", 1): 62.42, ("col", 1): 62.95, ("panel", 4): 68.59, ("panel", 8): 75.15,
-          ("panel", 16): 65.72, ("serpentine", 4): 68.75, ("serpentine", 8): 73.07,
-          ("serpentine", 16): 69.87, ("morton", 1): 66.21, ("xor", 1): 63.61}
+L2_NCU = {"gemm_cu_sha256": "1f3782b899ee4e8e", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
+          ("row", 1): 63.47, ("col", 1): 59.83, ("panel", 4): 68.01, ("panel", 8): 72.79,
+          ("panel", 16): 68.25, ("serpentine", 4): 70.88, ("serpentine", 8): 72.78,
+          ("serpentine", 16): 69.16, ("morton", 1): 66.31, ("xor", 1): 63.15}
 
 
 # dram__bytes_read.sum of the same captures (one cold launch per order)
-L2_NCU_DRAM = {("row", 1): 2054370048, ("col", 1): 2054768896, ("panel", 4): 1417427200,
-               ("panel", 8): 1089470720, ("panel", 16): 1294013184,
-               ("serpentine", 4): 1276849408, ("serpentine", 8): 1049390080,
-               ("serpentine", 16): 1264726784, ("morton", 1): 1367223040,
-               ("xor", 1): 2055344640}
+L2_NCU_DRAM = {("row", 1): 2051801344, ("col", 1): 2157394432, ("panel", 4): 1717671424,
+               ("panel", 8): 1067699200, ("panel", 16): 1231138048,
+               ("serpentine", 4): 1359949312, ("serpentine", 8): 1047890176,
+               ("serpentine", 16): 1230136064, ("morton", 1): 1583689472,
+               ("xor", 1): 2208052480}
 
 
 def resolve_workload(args):

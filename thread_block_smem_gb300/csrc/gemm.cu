@@ -261,10 +261,10 @@ __device__ __noinline__ void raise_abort(const Ctl& c) {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(c.peer_abort[j]), "r"(1) : "memory");
 }
 
-// Waits for the phase of `bar` with parity `parity`; false if the kernel
-// is aborting or the bound expired (then the abort is raised).
-__device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Ctl& c) {
-  if (ptx::mbar_test_wait(bar, parity)) return true;
+// The waiting part of wait(), out of line: the issuing threads' unrolled
+// loops then carry one test and one call per stage instead of a copy of this
+// loop each.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Ctl& c) {
   const uint64_t t0 = ptx::global_timer_ns();
   for (uint32_t n = 1;; ++n) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
@@ -276,6 +276,13 @@ __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Ctl& c
       }
     }
   }
+}
+
+// Waits for the phase of `bar` with parity `parity`; false if the kernel
+// is aborting or the bound expired (then the abort is raised).
+__device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Ctl& c) {
+  if (ptx::mbar_test_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, c);
 }
 
 // Waits until the 32-bit flag at `flag` (global) equals `value`, with the
