@@ -127,3 +127,20 @@ def test_cfg4_sampled(swz, order, g):
     got = C[torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()].cpu().double().numpy()
     assert np.abs(got - want).max() <= MAX_ABS
     assert np.linalg.norm(got - want) / np.linalg.norm(want) <= REL_FRO
+
+
+@pytest.mark.parametrize("blocks", [None, 2])
+def test_host_pipelines(swz, blocks):
+    # from pinned host memory, row slabs or growing-square blocks, each slab
+    # or block launched with shared A
+    M, N, K = 1000, 1304, 136
+    A, B = si.small_int_gemm_inputs(M, N, K, "fp16", lo=-4, hi=4, seed=7)
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hC = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+    dA, dB = torch.empty_like(A, device="cuda"), torch.empty_like(B, device="cuda")
+    dC = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    kw = dict(blocks=blocks) if blocks is not None else dict(slabs=3)
+    swz.gemm_host(hA, hB, hC, dA, dB, dC, "serpentine", 2, **kw, **SA)
+    torch.cuda.current_stream().synchronize()
+    swz.check_status()
+    assert torch.equal(hC.double(), ref.gemm_f64(A, B))
