@@ -708,9 +708,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Warp w owns TMEM lanes (rows) 32*(w%4) .. +31.  A partial piece goes to
     // this cluster's workspace slot and is published per warp with a release
     // flag; the owner of the tile's first piece waits, warp by warp, for the
-    // matching warps of the later pieces and adds them in K order.
+    // matching warps of the later pieces, streams their blocks into shared
+    // memory and adds them in K order.
     const uint32_t q = warp & 3u;
-    const uint32_t row_local = q * 32u + lane;
     uint32_t acc = 0, acc_phase = 0;
     uint32_t w, kbeg, kend;
     int kind, half;
@@ -722,7 +722,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t cta_m = t.m * CL + rank, cta_n = t.n * NP + pidx;
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + acc * BN;
       if (kind == kPartial) {
-        float4* slot = p.sk_ws + size_t(sch.c * CL + rank) * (BN / 4) * BM;
+        // workspace slot of this CTA: per warp and 32-column chunk one
+        // contiguous 4 KB block, float4 (column group v, row) at v*32 + row,
+        // so that the owner fetches a block with one bulk copy
+        float4* slot = p.sk_ws + size_t(sch.c * CL + rank) * (BN / 4) * BM +
+                       size_t(q) * (BN / 32) * 256;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t r[32];
@@ -730,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_ld_wait();
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            __stcg(slot + size_t(c / 4 + v) * BM + row_local,
+            __stcg(slot + size_t(c / 32) * 256 + v * 32 + lane,
                    make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
                                __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
         }
@@ -749,24 +753,77 @@ __global__ void __launch_bounds__(kThreads, 1)
             kind == kFirst ? uint64_t(w - sch.dp_end + 1) * sch.kb : uint64_t(0);
         const Schedule::Cursor peer0 =
             kind == kFirst ? sch.cursor(sch.c + 1) : Schedule::Cursor{0, 0, sch.P};
+        // advances k to the first cluster at or after it whose range is
+        // non-empty and starts inside this tile (k.cc == P: none left)
+        auto next_peer = [&](Schedule::Cursor& k) {
+          while (k.cc < sch.P && k.s < tile_end) {
+            Schedule::Cursor kn = k;
+            sch.step(kn);
+            if (k.s < kn.s) return;
+            k = kn;
+          }
+          k.cc = sch.P;
+        };
+        uint32_t npeers = 0;
         if (kind == kFirst) {
           bool got = true;
           if (lane == 0) {
-            for (Schedule::Cursor k = peer0; k.cc < sch.P && k.s < tile_end;) {
-              Schedule::Cursor kn = k;
-              sch.step(kn);
-              // a non-empty range starting inside this tile: wait for it
-              if (k.s < kn.s &&
-                  !wait_flag(p.sk_flags + (k.cc * CL + rank) * 4u + q, p.epoch, ctl)) {
+            Schedule::Cursor k = peer0;
+            for (next_peer(k); k.cc < sch.P;) {
+              if (!wait_flag(p.sk_flags + (k.cc * CL + rank) * 4u + q, p.epoch, ctl)) {
                 got = false;
                 break;
               }
-              k = kn;
+              ++npeers;
+              sch.step(k);
+              next_peer(k);
             }
           }
           got = __shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) != 0;
+          npeers = __shfl_sync(0xFFFFFFFFu, npeers, 0);
           if (!got) { aborted = true; break; }
           __threadfence();
+        }
+        // The peers' blocks (chunk by chunk, peers in K order) stream into a
+        // ring of 4 KB slots in this warp's quarter of the operand stages,
+        // idle now: this is the cluster's last item, its MMAs are complete
+        // and no load is pending.  Up to `kRing` bulk copies are in flight,
+        // where fetching block by block into registers would leave one
+        // dependent L2 round trip per chunk at the very end of the kernel.
+        constexpr uint32_t kRingWarp = uint32_t(STAGES * K_::STAGE_BYTES / 4) & ~4095u;
+        constexpr uint32_t kRing = kRingWarp / 4096u - 1u;  // the last 4 KB holds the barriers
+        static_assert(kRing >= 2, "fix-up ring");
+        const uint32_t ring = sA + (warp - 2u) * kRingWarp;
+        const uint32_t ring_bar0 = ring + kRing * 4096u;
+        const uint32_t nitems = npeers * uint32_t(BN / 32);
+        uint32_t issued = 0, consumed = 0, ic = 0;
+        Schedule::Cursor ik = peer0;
+        auto issue = [&]() {  // lane 0: the next block, chunk ic of peer ik
+          const uint32_t sl = issued % kRing;
+          const uint32_t bar = ring_bar0 + 8u * sl;
+          const float4* src = p.sk_ws + size_t(ik.cc * CL + rank) * (BN / 4) * BM +
+                              (size_t(q) * (BN / 32) + ic) * 256;
+          ptx::mbar_arrive_expect_tx(bar, 4096u);
+          ptx::bulk_load(ring + sl * 4096u, src, 4096u, bar);
+          ++issued;
+          sch.step(ik);
+          next_peer(ik);
+          if (ik.cc >= sch.P) {
+            ++ic;
+            ik = peer0;
+            next_peer(ik);
+          }
+        };
+        if (nitems > 0) {
+          if (lane == 0) {
+            for (uint32_t j = 0; j < kRing; ++j) ptx::mbar_init(ring_bar0 + 8u * j, 1);
+            ptx::fence_mbar_init();
+            ptx::fence_proxy_async_smem();
+            ptx::fence_proxy_async_global();  // the acquired partials, read by bulk copies
+            next_peer(ik);
+            while (issued < nitems && issued < kRing) issue();
+          }
+          __syncwarp();
         }
         // C tile rows of this warp: (cta_m*128 + q*32) .. +31.  Each 32-column
         // chunk goes registers -> staging box (row r at r*128 bytes, its 16-byte
@@ -785,37 +842,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           float f[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
-          for (Schedule::Cursor k = peer0; kind == kFirst && k.cc < sch.P && k.s < tile_end;) {
-            // two peers per round trip: the owner's fix-up is a chain of
-            // dependent L2 reads at the very end of the kernel
-            Schedule::Cursor k1 = k;
-            sch.step(k1);
-            Schedule::Cursor k2 = k1;
-            if (k1.cc < sch.P) sch.step(k2);
-            const bool v0 = k.s < k1.s;
-            const bool v1 = k1.cc < sch.P && k1.s < tile_end && k1.s < k2.s;
-            const float4* s0 = p.sk_ws + size_t(k.cc * CL + rank) * (BN / 4) * BM;
-            const float4* s1 = p.sk_ws + size_t((v1 ? k1.cc : k.cc) * CL + rank) * (BN / 4) * BM;
-            float4 x0[8], x1[8];
+          for (uint32_t j = 0; j < npeers; ++j) {
+            const uint32_t sl = consumed % kRing;
+            const bool okb = wait(ring_bar0 + 8u * sl, (consumed / kRing) & 1u, ctl);
+            if (!__all_sync(0xFFFFFFFFu, okb)) { aborted = true; break; }
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
-              const size_t off = size_t(c / 4 + v) * BM + row_local;
-              x0[v] = v0 ? __ldcg(s0 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
-              x1[v] = v1 ? __ldcg(s1 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+              float4 x;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                           : "r"(ring + sl * 4096u + uint32_t(v * 32 + lane) * 16u)
+                           : "memory");
+              f[4 * v] += x.x;
+              f[4 * v + 1] += x.y;
+              f[4 * v + 2] += x.z;
+              f[4 * v + 3] += x.w;
             }
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              f[4 * v] += x0[v].x;
-              f[4 * v + 1] += x0[v].y;
-              f[4 * v + 2] += x0[v].z;
-              f[4 * v + 3] += x0[v].w;
-              f[4 * v] += x1[v].x;
-              f[4 * v + 1] += x1[v].y;
-              f[4 * v + 2] += x1[v].z;
-              f[4 * v + 3] += x1[v].w;
+            __syncwarp();
+            ++consumed;
+            if (lane == 0 && issued < nitems) {
+              ptx::fence_proxy_async_smem();  // this slot's reads before its next fill
+              issue();
             }
-            k = (k1.cc < sch.P && k1.s < tile_end) ? k2 : k1;
           }
+          if (aborted) break;
           const uint32_t box = stg_warp + uint32_t((c / 32) & 1) * K_::STG_BOX_BYTES;
           // the store that last read this box (two chunks ago) must be done
           if (lane == 0) ptx::bulk_wait_group_read<1>();
@@ -833,6 +883,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tma_store_2d(&tmC, box, col0 + c, row0);
             ptx::bulk_commit_group();
           }
+        }
+        if (aborted) {
+          // a ring wait expired: let the copies already issued land first
+          if (lane == 0 && issued > consumed) spin_ns(50000);
+          __syncwarp();
+          break;
         }
         ptx::tc_fence_before();
         __syncwarp();
