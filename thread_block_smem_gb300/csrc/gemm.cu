@@ -143,6 +143,7 @@ struct Params {
   uint32_t* sk_flags;  // [cluster][rank][lane quarter]
   float4* sk_ws;       // [cluster][rank][BN/4 column groups][128 rows] float4
   uint32_t* dyn_counter;  // dynamic scheduler: work indices claimed beyond the first wave
+  uint32_t epi_pace_ns;   // gap between an epilogue warp's chunk stores (tiles with a successor)
 };
 
 enum ItemKind : int { kWhole = 0, kFirst = 1, kPartial = 2 };
@@ -834,6 +835,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int width = half < 0 ? BN : BN / 2;
         const int32_t col0 = int32_t(cta_n) * BN + (half < 0 ? 0 : half * (BN / 2));
         const uint32_t stg_warp = sStg + (warp - 2u) * 2u * K_::STG_BOX_BYTES;
+        // A tile's C leaves as 4 x width/32 TMA stores of 4 KB; issued in one
+        // burst they share the TMA unit with the operand loads of the next
+        // tile's first stages, and the MMA thread stalls there.  When another
+        // tile follows, the stores are spread out with a short gap (about a
+        // sixteenth of a tile's duration, set on the host); the last tile's
+        // epilogue, which nothing overlaps, goes at full speed.
+        uint64_t pace_ns = 0;
+        if constexpr (!DYN) {
+          uint32_t w2, b2, e2;
+          int k2, h2;
+          if (p.epi_pace_ns && sch.item(i + 1, w2, b2, e2, k2, h2)) pace_ns = p.epi_pace_ns;
+        }
 #pragma unroll 1
         for (int c = 0; c < width; c += 32) {
           uint32_t r[32];
@@ -882,6 +895,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             ptx::tma_store_2d(&tmC, box, col0 + c, row0);
             ptx::bulk_commit_group();
+          }
+          if (pace_ns && c + 32 < width) {
+            const uint64_t t0 = ptx::global_timer_ns();
+            while (ptx::global_timer_ns() - t0 < pace_ns) __nanosleep(100);
           }
         }
         if (aborted) {
@@ -1385,6 +1402,13 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   }
   prm.trace = o.d_trace;
   prm.debug_flags = o.debug_flags;
+  // epilogue store gap: ~1/16 of a tile's duration (proportional to K and the
+  // tile width, twice as long for TF32), at most 1 us; persistent launches
+  // only (a CTA of a non-persistent launch has no following tile)
+  if (persistent) {
+    const uint64_t pace = uint64_t(K) * uint64_t(pl.bn) * (tf32 ? 2u : 1u) / 1024u;
+    prm.epi_pace_ns = uint32_t(pace < 1000u ? pace : 1000u);
+  }
   prm.timeout_ns = uint64_t(o.timeout_ms ? o.timeout_ms : 2000u) * 1000000ull;
 
   if (o.stream_k) {
