@@ -83,25 +83,25 @@ SWEEP = WORKLOADS["gemm8192_bf16_pair"]["sweep"]
 # DRAM traffic of one launch of the headline GEMM from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
 # source whose SHA-256 prefix is recorded with it.
-TRAFFIC = {"bytes": 1368870400, "gemm_cu_sha256": "bcc59c3163df5202",
+TRAFFIC = {"bytes": 1305241344, "gemm_cu_sha256": "882923aceb2d1025",
            "workload": "gemm8192_bf16_pair", "profile": "profiles/gemm_8192_bf16_pair_ncu.md"}
 
 
 # L2 hit rate (lts__t_sector_hit_rate.pct) of one cold launch per order from
 # an ncu capture of `bench.py --only sweep`; valid for the recorded kernel
 # source only.
-L2_NCU = {"gemm_cu_sha256": "bcc59c3163df5202", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
-          ("row", 1): 63.92, ("col", 1): 62.48, ("panel", 4): 69.90, ("panel", 8): 73.11,
-          ("panel", 16): 70.79, ("serpentine", 4): 70.40, ("serpentine", 8): 73.43,
-          ("serpentine", 16): 70.60, ("morton", 1): 68.93, ("xor", 1): 64.10}
+L2_NCU = {"gemm_cu_sha256": "882923aceb2d1025", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
+          ("row", 1): 62.82, ("col", 1): 62.98, ("panel", 4): 70.52, ("panel", 8): 73.28,
+          ("panel", 16): 69.07, ("serpentine", 4): 71.01, ("serpentine", 8): 73.33,
+          ("serpentine", 16): 70.15, ("morton", 1): 69.30, ("xor", 1): 63.46}
 
 
 # dram__bytes_read.sum of the same captures (one cold launch per order)
-L2_NCU_DRAM = {("row", 1): 2063652096, ("col", 1): 2075050752, ("panel", 4): 1481139200,
-               ("panel", 8): 1165899264, ("panel", 16): 1285728512,
-               ("serpentine", 4): 1344821504, ("serpentine", 8): 1113030144,
-               ("serpentine", 16): 1256106496, ("morton", 1): 1465968384,
-               ("xor", 1): 2122376960}
+L2_NCU_DRAM = {("row", 1): 2057360128, ("col", 1): 2076388352, ("panel", 4): 1415586560,
+               ("panel", 8): 1096021248, ("panel", 16): 1283553280,
+               ("serpentine", 4): 1287037952, ("serpentine", 8): 1054710784,
+               ("serpentine", 16): 1266096128, ("morton", 1): 1366725120,
+               ("xor", 1): 2083619072}
 
 
 def resolve_workload(args):
