@@ -846,6 +846,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t w2, b2, e2;
           int k2, h2;
           if (p.epi_pace_ns && sch.item(i + 1, w2, b2, e2, k2, h2)) pace_ns = p.epi_pace_ns;
+        } else {
+          // the ring's next slot, if the producer has published it already
+          // (it claims a tile before loading it, so usually long before);
+          // only looked at, not taken
+          const uint32_t nx = (i + 1) % uint32_t(kSchedDepth);
+          if (p.epi_pace_ns &&
+              ptx::mbar_test_wait(sfull_bar(nx), ((i + 1) / uint32_t(kSchedDepth)) & 1u) &&
+              ring_w[nx] != kNoWork)
+            pace_ns = p.epi_pace_ns;
         }
 #pragma unroll 1
         for (int c = 0; c < width; c += 32) {
