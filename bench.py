@@ -83,25 +83,25 @@ SWEEP = WORKLOADS["gemm8192_bf16_pair"]["sweep"]
 # DRAM traffic of one launch of the headline GEMM from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
 # source whose SHA-256 prefix is recorded with it.
-TRAFFIC = {"bytes": 1305241344, "gemm_cu_sha256": "882923aceb2d1025",
+TRAFFIC = {"bytes": 1300425728, "gemm_cu_sha256": "9080a5a48f99a438",
            "workload": "gemm8192_bf16_pair", "profile": "profiles/gemm_8192_bf16_pair_ncu.md"}
 
 
 # L2 hit rate (lts__t_sector_hit_rate.pct) of one cold launch per order from
 # an ncu capture of `bench.py --only sweep`; valid for the recorded kernel
 # source only.
-L2_NCU = {"gemm_cu_sha256": "882923aceb2d1025", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
-          ("row", 1): 62.82, ("col", 1): 62.98, ("panel", 4): 70.52, ("panel", 8): 73.28,
-          ("panel", 16): 69.07, ("serpentine", 4): 71.01, ("serpentine", 8): 73.33,
-          ("serpentine", 16): 70.15, ("morton", 1): 69.30, ("xor", 1): 63.46}
+L2_NCU = {"gemm_cu_sha256": "9080a5a48f99a438", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
+          ("row", 1): 63.57, ("col", 1): 62.71, ("panel", 4): 68.58, ("panel", 8): 72.75,
+          ("panel", 16): 66.93, ("serpentine", 4): 70.40, ("serpentine", 8): 73.14,
+          ("serpentine", 16): 70.07, ("morton", 1): 67.50, ("xor", 1): 64.83}
 
 
 # dram__bytes_read.sum of the same captures (one cold launch per order)
-L2_NCU_DRAM = {("row", 1): 2057360128, ("col", 1): 2076388352, ("panel", 4): 1415586560,
-               ("panel", 8): 1096021248, ("panel", 16): 1283553280,
-               ("serpentine", 4): 1287037952, ("serpentine", 8): 1054710784,
-               ("serpentine", 16): 1266096128, ("morton", 1): 1366725120,
-               ("xor", 1): 2083619072}
+L2_NCU_DRAM = {("row", 1): 2053212672, ("col", 1): 2054282496, ("panel", 4): 1416570880,
+               ("panel", 8): 1088454400, ("panel", 16): 1293243392,
+               ("serpentine", 4): 1276696320, ("serpentine", 8): 1053804544,
+               ("serpentine", 16): 1265667840, ("morton", 1): 1367307520,
+               ("xor", 1): 2055155456}
 
 
 def resolve_workload(args):
