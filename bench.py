@@ -397,6 +397,12 @@ def run_swz(args):
                 pred, pred_bytes = swz.l2_model_predict(order, g, M, N, K, wl["tile"][0],
                                                         wl["tile"][1], tk, 2, model_l2,
                                                         model_conc, wl["cluster_m"])
+                # the same model fed half the L2: GB300's L2 is two halves,
+                # one per die, and operand lines that SMs of both dies read
+                # can take room in both
+                pred_h, pred_h_bytes = swz.l2_model_predict(order, g, M, N, K, wl["tile"][0],
+                                                            wl["tile"][1], tk, 2, model_l2 // 2,
+                                                            model_conc, wl["cluster_m"])
                 ncu_ok = (L2_NCU.get("gemm_cu_sha256") == _gemm_src_hash()
                           and args.workload == "gemm8192_bf16_pair" and persistent
                           and not args.stream_k)
@@ -407,6 +413,8 @@ def run_swz(args):
                                "pct_peak": 100.0 * flops / med / 1e9 / peaks["bf16_tflops"],
                                "l2_model_hit_pct": pred,
                                "l2_model_dram_read_bytes": pred_bytes,
+                               "l2_model_half_hit_pct": pred_h,
+                               "l2_model_half_dram_read_bytes": pred_h_bytes,
                                "l2_ncu_hit_pct": L2_NCU.get((order, g)) if ncu_ok else None,
                                "dram_read_ncu_bytes": L2_NCU_DRAM.get((order, g))
                                if ncu_ok else None})
@@ -472,6 +480,14 @@ def run_swz(args):
         if len(good) > 1:
             line["spearman_l2_model_vs_tflops"] = spearman(
                 [o["l2_model_hit_pct"] for o in good], [o["tflops"] for o in good])
+        # predicted against measured DRAM reads, where the capture is for this source
+        meas = [o for o in orders if o.get("dram_read_ncu_bytes")]
+        if len(meas) > 1:
+            line["spearman_model_dram_vs_ncu_dram"] = {
+                "full_l2": spearman([o["l2_model_dram_read_bytes"] for o in meas],
+                                    [o["dram_read_ncu_bytes"] for o in meas]),
+                "half_l2": spearman([o["l2_model_half_dram_read_bytes"] for o in meas],
+                                    [o["dram_read_ncu_bytes"] for o in meas])}
 
     # ---- end to end through the public API from pinned host buffers --------
     # swz_gemm_host: B in, then A in / GEMM / C out overlapped in row slabs;
