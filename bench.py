@@ -578,13 +578,15 @@ def run_swz(args):
         line["transpose"] = tr
 
     # ---- TF32 path (fp32 inputs, B stored N x K), 8192^3 ---------------------
-    if args.only == "all" and not args.no_tf32:
+    # (--only tf32: three warm-up launches and one cold launch, for capture)
+    if (args.only == "all" and not args.no_tf32) or args.only == "tf32":
         g = torch.Generator().manual_seed(0)
         A32 = (torch.rand((M, K), generator=g) * 2 - 1).to(dev)
         Bt32 = (torch.rand((N, K), generator=g) * 2 - 1).to(dev)
         C32 = torch.empty((M, N), dtype=torch.float32, device=dev)
         t = timed(lambda: swz.gemm(A32, Bt32, head_order, head_group, True, out=C32,
-                                   b_transposed=True, cta_pair=True), 10, 3)
+                                   b_transposed=True, cta_pair=True),
+                  10 if args.only == "all" else 1, 3)
         med = statistics.median(t)
         # the recipe's nominal dense ratio tf32 / bf16 = 1.1 / 2.25 PFLOP/s
         peak_tf32 = peaks["bf16_tflops"] * 1.1 / 2.25
@@ -721,11 +723,12 @@ def main():
                          "launch's resident programs)")
     ap.add_argument("--no-dynamic", action="store_true")
     ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose", "mma_sync",
-                                       "tc_rate", "swizzle"],
+                                       "tc_rate", "swizzle", "tf32"],
                     default="all",
                     help="gemm: headline steps only; sweep / swizzle: one cold launch per "
                          "order / operand swizzle span; "
-                         "transpose: the transposes only (profiling modes)")
+                         "transpose: the transposes only; tf32: the TF32 8192^3 GEMM, "
+                         "3 warm-up launches and one cold one (profiling modes)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
