@@ -577,6 +577,25 @@ def run_swz(args):
             del x, y
         line["transpose"] = tr
 
+    # ---- cuBLAS on the same shape, for counter comparison only -------------
+    # (--only cublas: torch.matmul's bf16 kernel with bf16 and with fp32
+    # output, three warm-up launches and one cold launch each; never timed
+    # into the line's numbers)
+    if args.only == "cublas":
+        g = torch.Generator().manual_seed(0)
+        Ab = torch.randn((M, K), generator=g).to(torch.bfloat16).to(dev)
+        Bb = torch.randn((K, N), generator=g).to(torch.bfloat16).to(dev)
+        cub = {}
+        for name, fn in (("bf16_out", lambda: torch.matmul(Ab, Bb)),
+                         ("fp32_out", lambda: torch.mm(Ab, Bb, out_dtype=torch.float32))):
+            try:
+                t = timed(fn, 1, 3)
+                cub[name] = {"ms": t[0], "tflops": flops / t[0] / 1e9}
+            except (RuntimeError, TypeError) as e:  # out_dtype not in this torch
+                cub[name] = {"error": type(e).__name__}
+        line["cublas_reference"] = cub
+        del Ab, Bb
+
     # ---- TF32 path (fp32 inputs, B stored N x K), 8192^3 ---------------------
     # (--only tf32: three warm-up launches and one cold launch, for capture)
     if (args.only == "all" and not args.no_tf32) or args.only == "tf32":
@@ -723,12 +742,13 @@ def main():
                          "launch's resident programs)")
     ap.add_argument("--no-dynamic", action="store_true")
     ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose", "mma_sync",
-                                       "tc_rate", "swizzle", "tf32"],
+                                       "tc_rate", "swizzle", "tf32", "cublas"],
                     default="all",
                     help="gemm: headline steps only; sweep / swizzle: one cold launch per "
                          "order / operand swizzle span; "
                          "transpose: the transposes only; tf32: the TF32 8192^3 GEMM, "
-                         "3 warm-up launches and one cold one (profiling modes)")
+                         "3 warm-up launches and one cold one; cublas: torch.matmul on the "
+                         "workload's shape for counter comparison (profiling modes)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
     if args.impl == "reference":
