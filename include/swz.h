@@ -156,11 +156,14 @@ typedef struct swz_gemm_opts {
                         span's width.  The C staging keeps the 128-byte span. */
   int dynamic;       /* persistent only, not with stream_k or split_tail, span
                         128 only: tiles are claimed at run time instead of
-                        dealt out by work_idx striding.  Program c takes work
-                        index c first, then P + the value of an atomic counter
-                        it increments (P = programs, or clusters with
-                        cta_pair), until the indices run out; each index goes
-                        through the tile order as usual.  The counter lives at
+                        dealt out by work_idx striding.  1: program c takes
+                        work index c first, then P + the value of an atomic
+                        counter it increments (P = programs, or clusters with
+                        cta_pair), until the indices run out.  2: program c
+                        takes c, c + P, ... for the floor(U / P) full waves
+                        (U = scheduler units) and claims only the last,
+                        partial wave: index floor(U / P) * P + the counter.
+                        Each index goes through the tile order as usual.  The counter lives at
                         the start of d_workspace (256-byte aligned, at least
                         swz_gemm_workspace_size bytes = 256) and is cleared on
                         `stream` before the launch; launches sharing a
@@ -190,8 +193,9 @@ typedef struct swz_gemm_opts {
  * once (its pieces wait on one another); SWZ_EINVAL for stream_k without
  * persistent or with a missing, misaligned (256 B) or too small workspace,
  * and for smem_swizzle not in {0, 32, 64, 128}; for dynamic the same
- * workspace rules, SWZ_EINVAL without persistent or with stream_k or
- * split_tail, SWZ_EUNSUPPORTED with a span other than 128; for shared_a
+ * workspace rules, SWZ_EINVAL for a value other than 0, 1 or 2, without
+ * persistent or with stream_k or split_tail, SWZ_EUNSUPPORTED with a span
+ * other than 128; for shared_a
  * SWZ_EINVAL for a value other than 0 or 1, SWZ_EUNSUPPORTED without cta_pair,
  * with tile_n 256, TF32, a span other than 128, stream_k, split_tail or
  * dynamic.

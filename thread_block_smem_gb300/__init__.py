@@ -317,7 +317,7 @@ def make_opts(dtype=SWZ_F16, tile_n=0, cta_pair=False, num_programs=0, trace=Non
     o = swz_gemm_opts()
     o.shared_a = 1 if shared_a else 0
     o.smem_swizzle = smem_swizzle
-    o.dynamic = 1 if dynamic else 0
+    o.dynamic = int(dynamic)  # False / True, or 1 / 2 (2: only the last wave claimed)
     o.b_layout = b_layout
     o.split_tail = 1 if split_tail else 0
     o.stream_k = 1 if stream_k else 0
@@ -378,7 +378,8 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
     ``smem_swizzle``: swizzle span of the operand stages, 128 (0), 64 or 32.
     ``dynamic``: claim tiles at run time through an atomic counter kept in
     ``workspace`` (a CUDA tensor of at least workspace_size(..., dynamic=True)
-    bytes); persistent launches only.  ``shared_a`` (with ``cta_pair``):
+    bytes); persistent launches only.  ``dynamic=2``: the full waves by
+    work-index striding and only the last, partial wave claimed.  ``shared_a`` (with ``cta_pair``):
     4-CTA clusters of two 128-wide pairs that load each A tile once and
     multicast it to both."""
     import torch

@@ -144,6 +144,7 @@ struct Params {
   float4* sk_ws;       // [cluster][rank][BN/4 column groups][128 rows] float4
   uint32_t* dyn_counter;  // dynamic scheduler: work indices claimed beyond the first wave
   uint32_t epi_pace_ns;   // gap between an epilogue warp's chunk stores (tiles with a successor)
+  uint32_t dyn_static;    // dynamic: items each cluster takes by striding before claiming
 };
 
 enum ItemKind : int { kWhole = 0, kFirst = 1, kPartial = 2 };
@@ -428,6 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     else ptx::mbar_arrive_cluster(ptx::map_to_rank(sempty_bar(slot), 0));
     return true;
   };
+  uint32_t dyn_published = 0;  // the claiming producer: items published so far
+  bool dyn_ended = false;
   auto next_item = [&](uint32_t i, bool fetch, uint32_t& w, uint32_t& kbeg, uint32_t& kend,
                        int& kind, int& half) -> bool {
     if constexpr (!DYN) {
@@ -438,9 +441,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       kind = kWhole;
       half = -1;
       if (fetch) {
-        w = i == 0 ? sch.c : sch.P + atomicAdd(p.dyn_counter, 1u);
-        if (w >= units) w = kNoWork;
-        if (!ring_put(i, w)) { aborted = true; return false; }
+        // Published one item ahead: the peer CTA's producer learns its next
+        // tile from the ring, and publishing only when this producer starts
+        // that tile's loads delayed the peer's loads, and with them the
+        // pair's MMAs, at every tile boundary.  The first dyn_static items
+        // come by work-index striding, the rest are claimed.
+        while (!dyn_ended && dyn_published <= i + 1u) {
+          const uint32_t k = dyn_published;
+          uint32_t wk = k < p.dyn_static ? sch.c + k * sch.P
+                                         : p.dyn_static * sch.P + atomicAdd(p.dyn_counter, 1u);
+          if (wk >= units) wk = kNoWork;
+          if (!ring_put(k, wk)) { aborted = true; return false; }
+          ++dyn_published;
+          dyn_ended = wk == kNoWork;
+        }
+        w = kNoWork;
+        if (i < dyn_published) w = ring_w[i % uint32_t(kSchedDepth)];
       } else if (!ring_take(i, w)) {
         aborted = true;
         return false;
@@ -1403,6 +1419,7 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
     if (pl.pair && pl.bn == 128 && !b_kmajor) return SWZ_EUNSUPPORTED;
     prm.split_tail = 1;
   }
+  if (o.dynamic < 0 || o.dynamic > 2) return SWZ_EINVAL;
   if (o.dynamic) {
     if (!persistent || o.stream_k || o.split_tail) return SWZ_EINVAL;
     const uintptr_t ws = reinterpret_cast<uintptr_t>(o.d_workspace);
@@ -1446,6 +1463,10 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   if (o.dynamic) {
     // the counter of claimed work indices starts at zero in every launch
     prm.dyn_counter = static_cast<uint32_t*>(o.d_workspace);
+    // 1: each cluster's first work index by striding, then claims; 2: the
+    // full waves by striding, only the last, partial wave claimed
+    const uint32_t clusters = uint32_t(pl.programs) / (pl.pair ? (pl.mca ? 4u : 2u) : 1u);
+    prm.dyn_static = o.dynamic == 2 ? pl.units / clusters : 1u;
     SWZ_CUDA_TRY(cudaMemsetAsync(prm.dyn_counter, 0, sizeof(uint32_t), s));
     return dispatch<128, true>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
   }
