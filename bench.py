@@ -83,25 +83,25 @@ SWEEP = WORKLOADS["gemm8192_bf16_pair"]["sweep"]
 # DRAM traffic of one launch of the headline GEMM from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
 # source whose SHA-256 prefix is recorded with it.
-TRAFFIC = {"bytes": 1300425728, "gemm_cu_sha256": "9080a5a48f99a438",
+TRAFFIC = {"bytes": 1292697856, "gemm_cu_sha256": "6a48eb250946c3b5",
            "workload": "gemm8192_bf16_pair", "profile": "profiles/gemm_8192_bf16_pair_ncu.md"}
 
 
 # L2 hit rate (lts__t_sector_hit_rate.pct) of one cold launch per order from
 # an ncu capture of `bench.py --only sweep`; valid for the recorded kernel
 # source only.
-L2_NCU = {"gemm_cu_sha256": "9080a5a48f99a438", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
-          ("row", 1): 63.57, ("col", 1): 62.71, ("panel", 4): 68.58, ("panel", 8): 72.75,
-          ("panel", 16): 66.93, ("serpentine", 4): 70.40, ("serpentine", 8): 73.14,
-          ("serpentine", 16): 70.07, ("morton", 1): 67.50, ("xor", 1): 64.83}
+L2_NCU = {"gemm_cu_sha256": "6a48eb250946c3b5", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
+          ("row", 1): 63.54, ("col", 1): 62.99, ("panel", 4): 69.33, ("panel", 8): 73.86,
+          ("panel", 16): 71.76, ("serpentine", 4): 71.52, ("serpentine", 8): 74.93,
+          ("serpentine", 16): 70.93, ("morton", 1): 69.09, ("xor", 1): 63.70}
 
 
 # dram__bytes_read.sum of the same captures (one cold launch per order)
-L2_NCU_DRAM = {("row", 1): 2053212672, ("col", 1): 2054282496, ("panel", 4): 1416570880,
-               ("panel", 8): 1088454400, ("panel", 16): 1293243392,
-               ("serpentine", 4): 1276696320, ("serpentine", 8): 1053804544,
-               ("serpentine", 16): 1265667840, ("morton", 1): 1367307520,
-               ("xor", 1): 2055155456}
+L2_NCU_DRAM = {("row", 1): 2023820032, ("col", 1): 2044800256, ("panel", 4): 1438507776,
+               ("panel", 8): 1080026880, ("panel", 16): 1243260160,
+               ("serpentine", 4): 1303341056, ("serpentine", 8): 1041679360,
+               ("serpentine", 16): 1231461120, ("morton", 1): 1382896896,
+               ("xor", 1): 2098445056}
 
 
 def resolve_workload(args):
@@ -508,7 +508,9 @@ def run_swz(args):
                 torch.cuda.synchronize()
                 if i >= 3:
                     t.append(e0.elapsed_time(e1))
-            return statistics.mean(t)
+            # median: a single host-side stall (page-ins of pinned memory,
+            # another process on the host) must not decide the figure
+            return statistics.median(t)
 
         # a job of several GEMMs from host memory: consecutive calls alternate
         # between two streams, each with its own device buffers and pinned C,
