@@ -24,7 +24,10 @@
 //     The swizzle span (128, 64 or 32 bytes) is a template parameter; the
 //     64- and 32-byte spans split each 128-byte row into column groups.
 //   * The accumulator lives in TMEM, double-buffered (2 x BN fp32 columns),
-//     so the epilogue of tile i overlaps the MMAs of tile i+1.
+//     so the epilogue of tile i overlaps the MMAs of tile i+1.  When a tile
+//     follows, the epilogue spreads its C stores (4 KB TMA boxes) over part
+//     of the next tile instead of issuing them in one burst that would
+//     share the TMA unit with that tile's first operand loads.
 //   * CTA pair (PAIR): 2-CTA cluster, tcgen05 cta_group::2, MMA 256 x BN.
 //     Each CTA loads its own 128 rows of A and its half of B's columns;
 //     the leader issues the MMAs and its commits are multicast to both CTAs.
@@ -32,13 +35,16 @@
 //     clusters of two pairs side by side in N (cluster tile 256 x 256).  The
 //     two CTAs that need the same 128 rows of A (cluster ranks r and r + 2)
 //     each load 64 of them and multicast them to both, so each A byte leaves
-//     L2 once per cluster instead of twice: a 128-wide pair reads 1.5x the
-//     operand bytes per FLOP of a 256-wide one, and L2 -> SM delivery, not the
-//     tensor pipe, bounds it.  A stage is refilled only when both pairs'
-//     MMAs have released it (every leader's commit reaches all four CTAs).
+//     L2 once per cluster instead of twice (a 128-wide tile needs 1.5x the
+//     operand bytes per FLOP of a 256-wide one).  A stage is refilled only
+//     when both pairs' MMAs have released it (every leader's commit reaches
+//     all four CTAs).  It halves A's L2 reads but not the bytes each SM
+//     receives, and measures no faster than the plain 128-wide pair.
 //   * Work items come from the static schedule (Schedule: work_idx striding,
 //     optional Stream-K tail or split tail) or, with DYN, from an atomic
-//     counter published to all roles through a shared-memory ring.
+//     counter published one item ahead to all roles through a shared-memory
+//     ring.  A Stream-K tile's owner streams its peers' partial sums into a
+//     ring of slots in its idle operand stages with bulk copies.
 //   * Every wait is bounded (globaltimer); on expiry the kernel records
 //     SWZ_ETIMEOUT in a device status word, drains what it issued, frees TMEM
 //     and returns.
