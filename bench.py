@@ -83,25 +83,25 @@ SWEEP = WORKLOADS["gemm8192_bf16_pair"]["sweep"]
 # DRAM traffic of one launch of the headline GEMM from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
 # source whose SHA-256 prefix is recorded with it.
-TRAFFIC = {"bytes": 1292697856, "gemm_cu_sha256": "6a48eb250946c3b5",
+TRAFFIC = {"bytes": 1307546112, "gemm_cu_sha256": "32dfb91f838bdc4f",
            "workload": "gemm8192_bf16_pair", "profile": "profiles/gemm_8192_bf16_pair_ncu.md"}
 
 
 # L2 hit rate (lts__t_sector_hit_rate.pct) of one cold launch per order from
 # an ncu capture of `bench.py --only sweep`; valid for the recorded kernel
 # source only.
-L2_NCU = {"gemm_cu_sha256": "6a48eb250946c3b5", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
-          ("row", 1): 63.54, ("col", 1): 62.99, ("panel", 4): 69.33, ("panel", 8): 73.86,
-          ("panel", 16): 71.76, ("serpentine", 4): 71.52, ("serpentine", 8): 74.93,
-          ("serpentine", 16): 70.93, ("morton", 1): 69.09, ("xor", 1): 63.70}
+L2_NCU = {"gemm_cu_sha256": "32dfb91f838bdc4f", "profile": "profiles/gemm_8192_bf16_orders_l2.md",
+          ("row", 1): 62.56, ("col", 1): 61.44, ("panel", 4): 70.64, ("panel", 8): 71.18,
+          ("panel", 16): 66.87, ("serpentine", 4): 70.25, ("serpentine", 8): 72.44,
+          ("serpentine", 16): 69.65, ("morton", 1): 69.53, ("xor", 1): 63.88}
 
 
 # dram__bytes_read.sum of the same captures (one cold launch per order)
-L2_NCU_DRAM = {("row", 1): 2023820032, ("col", 1): 2044800256, ("panel", 4): 1438507776,
-               ("panel", 8): 1080026880, ("panel", 16): 1243260160,
-               ("serpentine", 4): 1303341056, ("serpentine", 8): 1041679360,
-               ("serpentine", 16): 1231461120, ("morton", 1): 1382896896,
-               ("xor", 1): 2098445056}
+L2_NCU_DRAM = {("row", 1): 2054057728, ("col", 1): 2054787840, ("panel", 4): 1418204672,
+               ("panel", 8): 1098593024, ("panel", 16): 1300169216,
+               ("serpentine", 4): 1277612288, ("serpentine", 8): 1059105536,
+               ("serpentine", 16): 1270239744, ("morton", 1): 1364993024,
+               ("xor", 1): 2055510528}
 
 
 def resolve_workload(args):
@@ -523,7 +523,7 @@ def run_swz(args):
                     (torch.empty_like(Ad), torch.empty_like(Bd), torch.empty_like(C),
                      torch.empty_like(hC).pin_memory(), None if ws is None else torch.zeros_like(ws))]
             t = []
-            for rep in range(2 + 3):
+            for rep in range(2 + 5):
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -538,7 +538,7 @@ def run_swz(args):
                 torch.cuda.synchronize()
                 if rep >= 2:
                     t.append(e0.elapsed_time(e1) / n_calls)
-            return statistics.mean(t)
+            return statistics.median(t)  # host memory is shared: one slow rep must not decide
 
         # growing-square blocks (swz_gemm_host_tiled): C leaves while A and B
         # arrive; the row-slab pipeline (swz_gemm_host) is reported beside it
