@@ -22,6 +22,19 @@
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Work is enqueued asynchronously; no call synchronises except
  *     swz_check_status.
+ *   - CUDA graphs: the calls on device buffers (swz_tile_map, swz_gemm,
+ *     swz_gemm_ex, swz_gemm_streamk_noalloc, swz_gemm_mma_sync,
+ *     swz_transpose, swz_tc_rate, swz_tc_rate_ex) allocate nothing and do
+ *     not synchronise, so they may be recorded by stream capture and the
+ *     graph replayed.  The host-buffer calls (swz_gemm_host*) work on
+ *     streams of the library's own and are not for capture; neither is
+ *     swz_check_status, which synchronises.  Make one ordinary call with
+ *     the same configuration on the device first: the first call of each
+ *     kernel variant sets its shared-memory limit and caches occupancy and
+ *     device queries.  What a call clears before its launch (the dynamic
+ *     scheduler's counter, Stream-K's piece flags) is recorded as a memset
+ *     and cleared again in every replay; a captured call keeps its
+ *     arguments, so buffers are rewritten in place between replays.
  *   - Every call returns SWZ_OK (0) or a negative swz_status.  Arguments are
  *     validated before anything is enqueued; on error nothing is enqueued.
  *     No exception crosses the ABI.  Calls are thread-safe; the only
@@ -135,8 +148,10 @@ typedef struct swz_gemm_opts {
                         needs d_workspace of swz_gemm_workspace_size bytes   */
   void* d_workspace; /* device scratch for stream_k: partial accumulators and
                         per-piece flags.  Zero-fill it once before its first
-                        use; the library keeps it consistent afterwards.
-                        Launches sharing a workspace must not overlap.       */
+                        use; the library keeps it consistent afterwards
+                        (in graph replays too: a captured call clears the
+                        flags before its launch).  Launches sharing a
+                        workspace must not overlap.                          */
   uint64_t workspace_bytes; /* size of d_workspace                           */
   int b_layout;      /* SWZ_B_KN (default): B is K x N row-major; SWZ_B_NK: B
                         is stored transposed, N x K row-major (K contiguous)  */

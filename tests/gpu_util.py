@@ -26,3 +26,18 @@ def errors(got, want):
 # ||C - Cref||_F / ||Cref||_F <= 1e-3.
 MAX_ABS = 1e-2
 REL_FRO = 1e-3
+
+
+def capture_graph(fn):
+    """Run fn once eagerly on a side stream (one-time set-up of the kernels it
+    launches), then record it into a torch.cuda.CUDAGraph and return that."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g

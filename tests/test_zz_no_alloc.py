@@ -10,7 +10,8 @@ import pytest
 import torch
 
 import synth_inputs as si
-from gpu_util import MAX_ABS, REL_FRO, errors, require_gpu
+from gpu_util import MAX_ABS, REL_FRO, capture_graph, errors, require_gpu
+from oracle import ref
 
 pytestmark = pytest.mark.gpu
 
@@ -72,3 +73,28 @@ def test_noalloc_rejects_launch_beyond_scratch(swz):
                                       swz.SWZ_ROW, 1, opts, _stream())
     assert rc == swz.SWZ_ESCRATCH
     assert "scratch" in swz.swz_strerror(rc)
+
+
+def test_noalloc_graph_replay(swz):
+    # the flag clearing is recorded with the launch, so every replay of the
+    # captured call starts from clear flags; new operands in every replay
+    M, N, K = 1280, 1024, 576
+    Ad = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
+    Bd = torch.zeros((K, N), dtype=torch.bfloat16, device="cuda")
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    opts = swz.make_opts(swz.SWZ_BF16, cta_pair=True, num_programs=6)
+
+    def call():
+        rc = swz.swz_gemm_streamk_noalloc(Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(), M, N, K,
+                                          swz.SWZ_PANEL, 2, opts, _stream())
+        assert rc == swz.SWZ_OK, swz.swz_strerror(rc)
+
+    g = capture_graph(call)
+    for seed in (21, 22, 23):
+        A, B = si.small_int_gemm_inputs(M, N, K, "bf16", lo=-3, hi=3, seed=seed)
+        Ad.copy_(A)
+        Bd.copy_(B)
+        C.fill_(float("nan"))
+        g.replay()
+        assert swz.swz_check_status(_stream()) == swz.SWZ_OK
+        assert torch.equal(C.cpu().double(), ref.gemm_f64(A, B)), seed

@@ -1458,6 +1458,14 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
       static std::atomic<uint32_t> epoch{0};
       uint32_t e = epoch.fetch_add(1) + 1;
       if (e == 0) e = epoch.fetch_add(1) + 1;
+      // A captured launch keeps this epoch in every replay, so a replay would
+      // find the previous replay's flags already at it: under capture the
+      // flags are cleared on the stream before the launch (a memset node that
+      // runs in every replay; epochs are never 0).
+      cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+      SWZ_CUDA_TRY(cudaStreamIsCapturing(s, &capturing));
+      if (capturing != cudaStreamCaptureStatusNone)
+        SWZ_CUDA_TRY(cudaMemsetAsync(reinterpret_cast<void*>(ws), 0, size_t(L.flags_bytes), s));
       prm.stream_k = 1;
       prm.epoch = e;
       prm.sk_flags = reinterpret_cast<uint32_t*>(ws);
