@@ -317,7 +317,7 @@ def run_swz(args):
     peaks, peak_src = _peaks()
     stream = torch.cuda.current_stream()
     flush = torch.empty(2 * max(l2_bytes, 64 << 20) // 4, dtype=torch.float32, device=dev)
-    do_gemm = args.only in ("all", "gemm", "sweep", "swizzle")
+    do_gemm = args.only in ("all", "gemm", "sweep", "swizzle", "launch")
     do_transpose = args.only in ("all", "transpose") and not args.no_transpose
     do_mma_sync = args.only in ("all", "mma_sync") and not args.no_mma_sync
 
@@ -565,6 +565,64 @@ def run_swz(args):
                                      "api": f"swz_gemm_host, {args.e2e_slabs} row slabs, "
                                             "one call timed alone"}}
         del hA, hB, hC
+    # ---- launch cost: R GEMMs back to back, called one by one and recorded
+    # in one CUDA graph (--only launch; for small shapes, where the host work
+    # of a call is comparable with its kernel).  Wall clock from the first
+    # enqueue to the end of the last kernel, per call; the graph's device
+    # time from events around a replay.  L2 stays warm (operands reused).
+    if args.only == "launch":
+        R, reps = 50, 7
+
+        def calls():
+            for _ in range(R):
+                gemm_once(head_order, head_group)
+
+        for _ in range(3):
+            calls()
+        torch.cuda.synchronize()
+        eager, enqueue = [], []
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            calls()
+            t1 = time.perf_counter()
+            torch.cuda.synchronize()
+            eager.append((time.perf_counter() - t0) / R)
+            enqueue.append((t1 - t0) / R)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            calls()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            calls()
+        graph.replay()
+        torch.cuda.synchronize()
+        replay, replay_dev = [], []
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            t0 = time.perf_counter()
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            replay.append((time.perf_counter() - t0) / R)
+            replay_dev.append(e0.elapsed_time(e1) / 1e3 / R)
+        cold = statistics.median(timed(lambda: gemm_once(head_order, head_group), 10, 3)) / 1e3
+        med = statistics.median
+        line["launch"] = {
+            "calls": R, "reps": reps, "order": head_order, "group": head_group,
+            "eager_us_per_call": med(eager) * 1e6,
+            "eager_enqueue_us_per_call": med(enqueue) * 1e6,
+            "eager_tflops": flops / med(eager) / 1e12,
+            "graph_us_per_call": med(replay) * 1e6,
+            "graph_device_us_per_call": med(replay_dev) * 1e6,
+            "graph_tflops": flops / med(replay) / 1e12,
+            "single_launch_cold_l2_us": cold * 1e6}
+        del graph
+
     if do_gemm:
         del A, B, Ad, Bd, C
 
@@ -750,13 +808,15 @@ def main():
                          "launch's resident programs)")
     ap.add_argument("--no-dynamic", action="store_true")
     ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose", "mma_sync",
-                                       "tc_rate", "swizzle", "tf32", "cublas"],
+                                       "tc_rate", "swizzle", "tf32", "cublas", "launch"],
                     default="all",
                     help="gemm: headline steps only; sweep / swizzle: one cold launch per "
                          "order / operand swizzle span; "
                          "transpose: the transposes only; tf32: the TF32 8192^3 GEMM, "
                          "3 warm-up launches and one cold one; cublas: torch.matmul on the "
-                         "workload's shape for counter comparison (profiling modes)")
+                         "workload's shape for counter comparison (profiling modes); "
+                         "launch: 50 calls back to back, eager and replayed from a CUDA "
+                         "graph, per-call wall time")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -108,5 +108,5 @@ def test_workloads_and_capture_modes():
     # the capture modes the profiles' commands use are accepted
     src = open(bench.__file__).read()
     for mode in ("gemm", "sweep", "swizzle", "transpose", "mma_sync", "tc_rate", "tf32",
-                 "cublas"):
+                 "cublas", "launch"):
         assert f'"{mode}"' in src
