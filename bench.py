@@ -82,9 +82,11 @@ SWEEP = WORKLOADS["gemm8192_bf16_pair"]["sweep"]
 
 # SHA-256 prefixes of the gemm.cu sources the ncu figures below hold for:
 # the one they were captured on, then sources that differ from it only in
-# host code the measured launches do not run (4fa95a59d7bcf357: Stream-K
-# flags cleared on the stream when a call is recorded into a CUDA graph).
-NCU_SOURCES = ("32dfb91f838bdc4f", "4fa95a59d7bcf357")
+# host code of Stream-K launches, which the measured (static) launches do not
+# run: 4fa95a59d7bcf357 clears the Stream-K flags on the stream when a call
+# is recorded into a CUDA graph; 9a33811045633d4e also keeps every program
+# of a Stream-K launch that has fewer tiles than programs.
+NCU_SOURCES = ("32dfb91f838bdc4f", "4fa95a59d7bcf357", "9a33811045633d4e")
 
 # DRAM traffic of one launch of the headline GEMM from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
@@ -336,8 +338,8 @@ def run_swz(args):
         A, B = si.gemm_inputs(M, N, K, wl["dtype"], wl["dist"], seed=0)
         Ad, Bd = A.to(dev), B.to(dev)
         C = torch.empty((M, N), dtype=torch.float32, device=dev)
-        _, (_, _, _, _, programs) = swz.swz_gemm_plan(M, N, K, int(persistent),
-                                                      swz.make_opts(**cfg))
+        _, (_, _, _, _, programs) = swz.swz_gemm_plan(
+            M, N, K, int(persistent), swz.make_opts(stream_k=args.stream_k, **cfg))
         ws = None
         if args.stream_k:
             nws = swz.workspace_size(M, N, K, persistent, **cfg)

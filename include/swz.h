@@ -135,8 +135,10 @@ typedef struct swz_gemm_opts {
                         CTA owns 128 x tile_n of C) -- [CPS] Example 2;
                         0: single CTA                                        */
   int num_programs;  /* persistent only: CTAs to launch (a multiple of 2 with
-                        cta_pair, of 4 with shared_a); 0 = resident capacity,
-                        capped at the tile count                             */
+                        cta_pair, of 4 with shared_a); 0 = resident capacity;
+                        capped at the tile count (scheduler units) except
+                        with stream_k, where a launch with fewer units than
+                        programs splits each unit's K among programs      */
   int32_t* d_trace;  /* optional device array, 2 int32 per CTA tile, indexed
                         (cta_m * tiles_n + cta_n): {program (blockIdx.x),
                         iteration of that program's tile loop}               */
@@ -144,7 +146,8 @@ typedef struct swz_gemm_opts {
   uint32_t timeout_ms;  /* bound of every device wait; 0 = 2000 ms           */
   int stream_k;      /* persistent only: 1 = share the last, partial wave of
                         tiles among all programs by splitting those tiles'
-                        K iterations into equal contiguous ranges (Stream-K);
+                        K iterations into equal contiguous ranges (Stream-K;
+                        with fewer tiles than programs every tile is split);
                         needs d_workspace of swz_gemm_workspace_size bytes   */
   void* d_workspace; /* device scratch for stream_k: partial accumulators and
                         per-piece flags.  Zero-fill it once before its first

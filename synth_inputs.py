@@ -80,3 +80,12 @@ def sample_indices(M: int, N: int, per_tile_m: int, per_tile_n: int,
     jj.append(np.array([0, N - 1, 0, N - 1]))
     return (np.concatenate(ii).astype(np.int64),
             np.concatenate(jj).astype(np.int64))
+
+
+def device_words(M: int, N: int, seed: int = 0, device: str = "cuda") -> torch.Tensor:
+    """M x N int32 tensor of random words in [0, 2^31) drawn on `device` by
+    torch's generator for that device (for sizes too large to draw on the
+    host); reproducible for a given seed on one kind of device."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return torch.empty((M, N), dtype=torch.int32, device=device).random_(generator=g)

@@ -94,6 +94,28 @@ def test_plan_without_device(swz):
     assert swz.swz_gemm_plan(1024, 1024, 512, 0, o)[0] == swz.SWZ_EINVAL
 
 
+def test_stream_k_plan_keeps_every_program(swz):
+    # Stream-K shares the tail among all programs: with fewer scheduler units
+    # than programs every program stays (each unit's K is split), while the
+    # other schedules cap the programs at the units.
+    for cfg, units in ((dict(cta_pair=True), 1), (dict(tile_n=128), 4)):
+        o = swz.make_opts(num_programs=152, **cfg)
+        rc, plan = swz.swz_gemm_plan(256, 256, 1 << 20, 1, o)
+        assert rc == swz.SWZ_OK and plan[4] == units * (2 if cfg.get("cta_pair") else 1)
+        assert swz.swz_gemm_workspace_size(256, 256, 1 << 20, 1, o) == (swz.SWZ_OK, 0)
+        o = swz.make_opts(num_programs=152, stream_k=True, **cfg)
+        rc, plan = swz.swz_gemm_plan(256, 256, 1 << 20, 1, o)
+        assert rc == swz.SWZ_OK and plan[4] == 152
+        rc, n = swz.swz_gemm_workspace_size(256, 256, 1 << 20, 1, o)
+        # flags of 152 CTAs (4 words each, 256-byte aligned) + one 128 x tile_n
+        # FP32 partial per CTA
+        tn = 256 if cfg.get("cta_pair") else 128
+        assert rc == swz.SWZ_OK and n == 2560 + 152 * 128 * tn * 4
+    # evenly divided units need no Stream-K workspace
+    o = swz.make_opts(num_programs=8, stream_k=True, tile_n=128)
+    assert swz.swz_gemm_workspace_size(1024, 1024, 512, 1, o) == (swz.SWZ_OK, 0)
+
+
 def test_validation_before_device(swz):
     # these are rejected before any CUDA call is made
     E = swz.SWZ_EINVAL

@@ -1144,7 +1144,10 @@ static int make_plan(int M, int N, int persistent, const swz_gemm_opts& o, const
       if (rc != SWZ_OK) return rc;
     }
     const uint32_t units_cap = uint32_t(cap / cln);
-    pl->programs = int(pl->units < units_cap ? pl->units : units_cap) * cln;
+    // Stream-K shares the tail among all programs, so with fewer units than
+    // programs (the whole product is one partial wave) every program stays
+    // and each unit's K iterations are split among several of them.
+    pl->programs = int(pl->units < units_cap && !o.stream_k ? pl->units : units_cap) * cln;
   }
   return SWZ_OK;
 }
