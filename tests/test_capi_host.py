@@ -135,6 +135,13 @@ def test_validation_before_device(swz):
     assert swz.swz_transpose(0, 0, 0, 5, 0) == swz.SWZ_OK             # empty: no-op
     assert swz.swz_transpose(16, 32, 4, 4, 0) == E                    # overlapping
     assert swz.swz_transpose(18, 4096, 4, 4, 0) == E                  # misaligned
+    # maximum sizes: the transpose grid's y extent holds 65535 row tiles of
+    # 32 (M <= 2,097,120); a GEMM whose tile count does not fit int32 is refused
+    assert swz.swz_transpose(16, 1 << 40, 65535 * 32 + 1, 4, 0) == E
+    for cfg in (dict(), dict(cta_pair=True), dict(tile_n=128)):
+        assert swz.swz_gemm_plan(2**31 - 1, 2**31 - 8, 64, 0, swz.make_opts(**cfg))[0] == E
+    rc, plan = swz.swz_gemm_plan(2**20, 2**20, 64, 0, swz.make_opts())
+    assert rc == swz.SWZ_OK and plan == (8192, 4096, 8192, 4096, 33554432)
 
 
 def test_product_does_not_import_oracle():
