@@ -214,3 +214,60 @@ def persistent_trace(order, gm, gn, group, num_programs, cluster_m=1, cluster_n=
                     raise AssertionError(f"tile {key} visited twice")
                 trace[key] = (prog, it)
     return trace
+
+
+def stream_k_trace(order, gm, gn, group, num_programs, k_blocks, cluster_m=1):
+    """The persistent schedule with a Stream-K tail, CTA by CTA.
+
+    Not from the pages: the first page names dynamic balancing and Stream-K
+    only as what its static loop lacks.  This is the library's definition,
+    written out plainly.  With P clusters of cluster_m CTAs and U
+    scheduler units (cluster tiles, in tile-order sequence), the first
+    U - R units (R = U mod P) go out whole by work-index striding, as in
+    persistent_trace.  The K blocks of the R tail units are laid end to
+    end, I = R * k_blocks of them, and cluster c takes the contiguous range
+    [floor(I c / P), floor(I (c + 1) / P)).  A cluster's work items are its
+    whole units, then one item for each tail unit its range touches, in K
+    order.  A tail unit is finished (C written) by the cluster whose range
+    holds the unit's first K block.
+
+    Returns {(cta_m, cta_n): (program, item index)} over all CTA tiles, the
+    program and item that write each tile.
+    """
+    if gm % cluster_m:
+        raise ValueError("the cluster shape must divide the CTA-tile grid")
+    seq = tile_sequence(order, gm // cluster_m, gn, group)
+    P = num_programs // cluster_m
+    U = len(seq)
+    R = U % P
+    full = U - R
+    trace = {}
+
+    def put(unit, c, item):
+        m_idx, n_idx = seq[unit]
+        for r in range(cluster_m):
+            key = (m_idx * cluster_m + r, n_idx)
+            if key in trace:
+                raise AssertionError(f"tile {key} written twice")
+            trace[key] = (c * cluster_m + r, item)
+
+    for w in range(full):
+        put(w, w % P, w // P)
+    I = R * k_blocks
+    for c in range(P):
+        s, e = I * c // P, I * (c + 1) // P
+        item = len(range(c, full, P))
+        t = s // k_blocks
+        while s < e and t * k_blocks < e:
+            if t * k_blocks >= s:
+                put(full + t, c, item)
+            item += 1
+            t += 1
+    return trace
+
+
+def stream_k_ranges(num_clusters, tail_units, k_blocks):
+    """Each cluster's tail range [s, e) in the laid-end-to-end K blocks."""
+    I = tail_units * k_blocks
+    return [(I * c // num_clusters, I * (c + 1) // num_clusters)
+            for c in range(num_clusters)]

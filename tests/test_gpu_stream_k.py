@@ -8,6 +8,7 @@ import torch
 import synth_inputs as si
 from gpu_util import MAX_ABS, REL_FRO, errors, require_gpu
 from oracle import ref
+from oracle import tile_order as to
 
 pytestmark = pytest.mark.gpu
 
@@ -103,3 +104,35 @@ def test_stream_k_errors(swz):
     assert e.value.code == swz.SWZ_EUNSUPPORTED
     # evenly divisible tiles need no workspace and run whole tiles
     assert swz.workspace_size(768, 640, 128, True, tile_n=128, num_programs=6) == 0
+
+
+# (M, N, K, cfg, programs): whole units and a tail; more programs than tiles
+# (every tile split); CTA pairs with a tail; one cluster tile over 8 clusters
+TRACE_CASES = [
+    (768, 640, 1024, dict(tile_n=128), 7),
+    (768, 640, 384, dict(tile_n=128), 40),
+    (768, 640, 192, dict(tile_n=256), 5),
+    (1280, 1024, 576, dict(cta_pair=True), 6),
+    (256, 256, 4096, dict(cta_pair=True), 16),
+]
+
+
+@pytest.mark.parametrize("M,N,K,cfg,programs", TRACE_CASES)
+@pytest.mark.parametrize("order,g", [(to.PANEL, 2), (to.SERPENTINE, 3)])
+def test_stream_k_trace_matches_oracle(swz, M, N, K, cfg, programs, order, g):
+    # which program writes each tile, at which item of its loop: the
+    # schedule the oracle writes out from the Stream-K definition
+    rc, (tm, tn, _, _, P) = swz.swz_gemm_plan(
+        M, N, K, 1, swz.make_opts(stream_k=True, num_programs=programs, **cfg))
+    assert rc == swz.SWZ_OK and P == programs
+    kb = -(-K // (128 if cfg.get("tile_n") == 128 else 64))  # K blocks per stage
+    A, B = si.small_int_gemm_inputs(M, N, K, "bf16", lo=-3, hi=3, seed=K + programs)
+    ws, n = _ws(swz, M, N, K, num_programs=programs, **cfg)
+    trace = torch.full((tm * tn * 2,), -1, dtype=torch.int32, device="cuda")
+    C = swz.gemm(A.cuda(), B.cuda(), order, g, True, num_programs=programs, stream_k=True,
+                 workspace=ws, trace=trace, **cfg)
+    swz.check_status()
+    assert torch.equal(C.cpu().double(), ref.gemm_f64(A, B))
+    want = to.stream_k_trace(order, tm, tn, g, P, kb, cluster_m=2 if cfg.get("cta_pair") else 1)
+    got = trace.view(tm, tn, 2).cpu().tolist()
+    assert {(m, n): tuple(got[m][n]) for m in range(tm) for n in range(tn)} == want

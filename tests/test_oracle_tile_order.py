@@ -176,3 +176,61 @@ def test_persistent_trace_2x2_clusters():
     assert tr[(0, 3)] == (6, 0)   # rank 2 of cluster 1: row 0, column 1
     with pytest.raises(ValueError):
         to.persistent_trace(to.ROW, 6, 7, 1, 4, cluster_m=2, cluster_n=2)
+
+
+def test_stream_k_trace_hand_example():
+    # 1 x 3 tiles, 4 clusters, 4 K blocks a tile: all 3 tiles are the tail,
+    # I = 12 blocks split [0,3) [3,6) [6,9) [9,12).  Tile 0 starts at block 0
+    # (cluster 0, its first item); tile 1 at block 4, inside cluster 1's
+    # range, whose items are the end of tile 0 (item 0) and tile 1 (item 1);
+    # tile 2 at block 8, cluster 2's second item.  Cluster 3 only adds the
+    # end of tile 2.
+    assert to.stream_k_ranges(4, 3, 4) == [(0, 3), (3, 6), (6, 9), (9, 12)]
+    assert to.stream_k_trace(to.ROW, 1, 3, 1, 4, 4) == {
+        (0, 0): (0, 0), (0, 1): (1, 1), (0, 2): (2, 1)}
+    # the same with 2-CTA clusters: each cluster tile is two CTA tiles
+    assert to.stream_k_trace(to.ROW, 2, 3, 1, 8, 4, cluster_m=2) == {
+        (0, 0): (0, 0), (1, 0): (1, 0), (0, 1): (2, 1), (1, 1): (3, 1),
+        (0, 2): (4, 1), (1, 2): (5, 1)}
+    with pytest.raises(ValueError):
+        to.stream_k_trace(to.ROW, 3, 3, 1, 8, 4, cluster_m=2)
+
+
+@pytest.mark.parametrize("gm,gn,P,kb,cm", [(6, 5, 6, 4, 1), (6, 5, 7, 16, 1), (6, 5, 7, 3, 1),
+                                           (6, 5, 40, 3, 1), (2, 1, 152, 16384, 2),
+                                           (6, 5, 8, 9, 2), (10, 4, 6, 7, 2)])
+def test_stream_k_trace_against_brute_force(gm, gn, P, kb, cm):
+    order, g = to.PANEL, 2
+    tr = to.stream_k_trace(order, gm, gn, g, P, kb, cluster_m=cm)
+    assert len(tr) == gm * gn  # every CTA tile written once
+    clusters, U = P // cm, (gm // cm) * gn
+    R = U % clusters
+    if R == 0:
+        assert tr == to.persistent_trace(order, gm, gn, g, P, cluster_m=cm)
+        return
+    # whole units: as the static schedule
+    seq = to.tile_sequence(order, gm // cm, gn, g)
+    for w in range(U - R):
+        m, n = seq[w]
+        for r in range(cm):
+            assert tr[(m * cm + r, n)] == ((w % clusters) * cm + r, w // clusters)
+    # the tail, block by block: owner of block b = the cluster whose range
+    # holds it; ranges are contiguous, cover [0, R * kb) once and differ in
+    # length by at most one block
+    ranges = to.stream_k_ranges(clusters, R, kb)
+    assert ranges[0][0] == 0 and ranges[-1][1] == R * kb
+    assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
+    assert max(e - s for s, e in ranges) - min(e - s for s, e in ranges) <= 1
+    holder = {}
+    for c, (s, e) in enumerate(ranges):
+        for b in range(s, e):
+            holder[b] = c
+    for t in range(R):
+        c = holder[t * kb]
+        # the items of cluster c before this one: its whole units, then one
+        # per earlier tail unit its range touches
+        whole = len(range(c, U - R, clusters))
+        earlier = len({b // kb for b in range(*ranges[c]) if b // kb < t})
+        m, n = seq[U - R + t]
+        for r in range(cm):
+            assert tr[(m * cm + r, n)] == (c * cm + r, whole + earlier)
