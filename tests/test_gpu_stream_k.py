@@ -25,10 +25,11 @@ def _ws(swz, M, N, K, **kw):
 
 # (M, N, K, cfg, programs): programs chosen so that tiles % clusters != 0;
 # K values give tail ranges longer and shorter than one cluster (the latter
-# leaves some programs with an empty range).
+# leaves some programs with an empty range).  kb = K blocks of a tile: one
+# stage each, 64 elements of K (128 for 128-wide tiles, two-atom stages).
 CASES = [
-    (768, 640, 1024, dict(tile_n=128), 7),       # 30 tiles, R = 2, kb = 16
-    (768, 640, 192, dict(tile_n=128), 7),        # kb = 3: I = 6 < 7 programs
+    (768, 640, 1024, dict(tile_n=128), 7),       # 30 tiles, R = 2, kb = 8
+    (768, 640, 192, dict(tile_n=128), 7),        # kb = 2: I = 4 < 7 programs
     (768, 640, 64, dict(tile_n=128), 7),         # kb = 1: no split possible
     (1000, 1000, 520, dict(tile_n=256), 5),      # ragged M/N/K
     (768, 640, 1024, dict(cta_pair=True), 4),    # 9 cluster tiles, 2 clusters, R = 1
