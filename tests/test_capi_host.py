@@ -111,6 +111,11 @@ def test_stream_k_plan_keeps_every_program(swz):
         # FP32 partial per CTA
         tn = 256 if cfg.get("cta_pair") else 128
         assert rc == swz.SWZ_OK and n == 2560 + 152 * 128 * tn * 4
+    # the same through the Python helper
+    assert swz.gemm_plan(256, 256, 1 << 20, True, cta_pair=True, num_programs=152) == (
+        2, 1, 1, 1, 2)
+    assert swz.gemm_plan(256, 256, 1 << 20, True, cta_pair=True, num_programs=152,
+                         stream_k=True) == (2, 1, 1, 1, 152)
     # evenly divided units need no Stream-K workspace
     o = swz.make_opts(num_programs=8, stream_k=True, tile_n=128)
     assert swz.swz_gemm_workspace_size(1024, 1024, 512, 1, o) == (swz.SWZ_OK, 0)

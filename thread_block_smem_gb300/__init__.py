@@ -335,11 +335,12 @@ def make_opts(dtype=SWZ_F16, tile_n=0, cta_pair=False, num_programs=0, trace=Non
 
 
 def gemm_plan(M, N, K, persistent=False, tile_n=0, cta_pair=False, num_programs=0,
-              shared_a=False):
-    """(tiles_m, tiles_n, sched_m, sched_n, programs) of a GEMM launch."""
+              shared_a=False, stream_k=False):
+    """(tiles_m, tiles_n, sched_m, sched_n, programs) of a GEMM launch
+    (with ``stream_k`` the program count is not capped at the tile count)."""
     rc, v = swz_gemm_plan(M, N, K, int(bool(persistent)),
                           make_opts(tile_n=tile_n, cta_pair=cta_pair, num_programs=num_programs,
-                                    shared_a=shared_a))
+                                    shared_a=shared_a, stream_k=stream_k))
     _check(rc, "swz_gemm_plan")
     return v
 
