@@ -11,7 +11,6 @@
 * edge cases: ragged M/N/K, K = 0, tiny shapes, non-bijective Morton/XOR.
 Tolerance: max |C - Cref| <= 1e-2 and relative Frobenius error <= 1e-3.
 """
-import numpy as np
 import pytest
 import torch
 
