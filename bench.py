@@ -59,19 +59,6 @@ WORKLOADS = {
                                                  ("panel", 8), ("panel", 16),
                                                  ("serpentine", 4), ("serpentine", 8),
                                                  ("serpentine", 16)]),
-    # shared A: 4-CTA clusters of two 128-wide pairs (CTA tiles 128 x 128).  The L2
-    # model sees it at the cluster tile: per 256 x 256 cluster tile A and B are
-    # each requested from L2 once (A by multicast, B in per-CTA quarters) --
-    # the request pattern of the model's 2-CTA cluster of 128 x 256 tiles,
-    # with half as many model CTAs in flight as launched CTAs
-    "gemm6144x10240x4096_fp16_shared_a": dict(M=6144, N=10240, K=4096, dtype="fp16",
-                                              dist="uniform",
-                                              cfg=dict(cta_pair=True, shared_a=True),
-                                              tile=(128, 256), cluster_m=2, tk=128, conc_div=2,
-                                              sweep=[("row", 1), ("col", 1), ("panel", 4),
-                                                     ("panel", 8), ("panel", 16),
-                                                     ("serpentine", 4), ("serpentine", 8),
-                                                     ("serpentine", 16)]),
     "gemm1024x1024x512_fp16": dict(M=1024, N=1024, K=512, dtype="fp16", dist="uniform",
                                    cfg=dict(tile_n=128), tile=(128, 128), cluster_m=1,
                                    sweep=[("row", 1), ("col", 1), ("panel", 4), ("morton", 1),
@@ -432,7 +419,7 @@ def run_swz(args):
             for sp in (128, 64, 32):
                 gemm_once(head_order, head_group, sp)
             torch.cuda.synchronize()
-        elif args.only == "all" and not args.no_swizzle and not cfg.get("shared_a"):
+        elif args.only == "all" and not args.no_swizzle:
             for sp in (128, 64, 32):
                 t = timed(lambda: gemm_once(head_order, head_group, sp), max(5, args.steps // 4),
                           3)
@@ -440,8 +427,7 @@ def run_swz(args):
                 spans.append({"span_bytes": sp, "ms": med, "tflops": flops / med / 1e9})
         # ---- static (work_idx striding) vs dynamic (atomic counter) -------
         sched = {}
-        if (args.only == "all" and not args.no_dynamic and persistent and not args.stream_k
-                and not cfg.get("shared_a")):  # shared A runs the static schedule only
+        if args.only == "all" and not args.no_dynamic and persistent and not args.stream_k:
             dws = torch.zeros(256, dtype=torch.uint8, device=dev)
             for name, kw in (("static", {}), ("dynamic", dict(dynamic=True, workspace=dws))):
                 fn = lambda: swz.gemm(Ad, Bd, head_order, head_group, True, out=C, **kw, **cfg)
@@ -548,9 +534,6 @@ def run_swz(args):
                     t.append(e0.elapsed_time(e1) / n_calls)
             return statistics.median(t)  # host memory is shared: one slow rep must not decide
 
-        # growing-square blocks (swz_gemm_host_tiled): C leaves while A and B
-        # arrive; the row-slab pipeline (swz_gemm_host) is reported beside it
-        ms_tiled = e2e_time(blocks=args.e2e_blocks)
         ms_slabs = e2e_time(slabs=args.e2e_slabs)
         n_calls = max(args.steps, 4)
         ms_job = e2e_streamed(n_calls, slabs=args.e2e_slabs)
@@ -560,10 +543,7 @@ def run_swz(args):
                        "api": f"swz_gemm_host, {args.e2e_slabs} row slabs, pinned host "
                               f"buffers; a job of {n_calls} GEMMs on two alternating "
                               "streams, each call with its own copies in and out",
-                       "single_call": {"value": world * flops / ms_tiled / 1e9,
-                                       "api": f"swz_gemm_host_tiled, {args.e2e_blocks}x"
-                                              f"{args.e2e_blocks} blocks, one call timed alone"},
-                       "row_slabs": {"value": world * flops / ms_slabs / 1e9,
+                       "single_call": {"value": world * flops / ms_slabs / 1e9,
                                      "api": f"swz_gemm_host, {args.e2e_slabs} row slabs, "
                                             "one call timed alone"}}
         del hA, hB, hC
@@ -797,8 +777,6 @@ def main():
     ap.add_argument("--stream-k", action="store_true", help="Stream-K tail (persistent only)")
     ap.add_argument("--non-persistent", action="store_true", help="one CTA (pair) per tile")
     ap.add_argument("--e2e-slabs", type=int, default=8, help="row slabs of the host pipeline")
-    ap.add_argument("--e2e-blocks", type=int, default=4,
-                    help="blocks per side of the tiled host pipeline (e2e headline)")
     ap.add_argument("--no-mma-sync", action="store_true")
     ap.add_argument("--no-tf32", action="store_true")
     ap.add_argument("--no-tc-rate", action="store_true")

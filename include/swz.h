@@ -135,7 +135,7 @@ typedef struct swz_gemm_opts {
                         CTA owns 128 x tile_n of C) -- [CPS] Example 2;
                         0: single CTA                                        */
   int num_programs;  /* persistent only: CTAs to launch (a multiple of 2 with
-                        cta_pair, of 4 with shared_a); 0 = resident capacity;
+                        cta_pair); 0 = resident capacity;
                         capped at the tile count (scheduler units) except
                         with stream_k, where a launch with fewer units than
                         programs splits each unit's K among programs      */
@@ -158,12 +158,6 @@ typedef struct swz_gemm_opts {
   uint64_t workspace_bytes; /* size of d_workspace                           */
   int b_layout;      /* SWZ_B_KN (default): B is K x N row-major; SWZ_B_NK: B
                         is stored transposed, N x K row-major (K contiguous)  */
-  int split_tail;    /* persistent only, not with stream_k: when the R tiles
-                        left for the last wave number at most half the
-                        programs (clusters), split each into two halves of
-                        tile_n / 2 columns so that 2R programs finish the last
-                        wave in half the time; no workspace.  A split tile's
-                        trace entry records one of its two halves.           */
   int smem_swizzle;  /* span in bytes of the TMA / tensor-core shared-memory
                         swizzle of the operand stages ([SBC] "Hopper TMA 的
                         swizzling": the 16-byte chunk index of an address is
@@ -172,30 +166,17 @@ typedef struct swz_gemm_opts {
                         bytes in every mode; with 64 and 32 a 128-byte row of
                         a stage is split into 2 or 4 column groups of the
                         span's width.  The C staging keeps the 128-byte span. */
-  int dynamic;       /* persistent only, not with stream_k or split_tail, span
-                        128 only: tiles are claimed at run time instead of
-                        dealt out by work_idx striding.  1: program c takes
-                        work index c first, then P + the value of an atomic
-                        counter it increments (P = programs, or clusters with
-                        cta_pair), until the indices run out.  2: program c
-                        takes c, c + P, ... for the floor(U / P) full waves
-                        (U = scheduler units) and claims only the last,
-                        partial wave: index floor(U / P) * P + the counter.
-                        Each index goes through the tile order as usual.  The counter lives at
-                        the start of d_workspace (256-byte aligned, at least
+  int dynamic;       /* persistent only, not with stream_k, span 128 only:
+                        tiles are claimed at run time instead of dealt out by
+                        work_idx striding.  1: program c takes work index c
+                        first, then P + the value of an atomic counter it
+                        increments (P = programs, or clusters with cta_pair),
+                        until the indices run out.  Each index goes through
+                        the tile order as usual.  The counter lives at the
+                        start of d_workspace (256-byte aligned, at least
                         swz_gemm_workspace_size bytes = 256) and is cleared on
                         `stream` before the launch; launches sharing a
                         workspace must not overlap.                          */
-  int shared_a;      /* 1: with cta_pair and tile_n 128 (0 picks 128), 4-CTA
-                        clusters made of two CTA pairs side by side in N
-                        (cluster tile 256 x 256, scheduler grid ceil(M/256) x
-                        ceil(N/256), tile order applied to it).  The two CTAs
-                        that need the same 128 rows of A each load 64 of them
-                        and multicast them to both (TMA .multicast::cluster),
-                        halving A's L2 -> SM traffic.  fp16 / bf16 only, span
-                        128, static schedule (not with stream_k, split_tail
-                        or dynamic: SWZ_EUNSUPPORTED); num_programs a multiple
-                        of 4.  0: off                                        */
 } swz_gemm_opts;
 
 /* debug_flags: withhold the first operand load so that the consumer's
@@ -205,18 +186,13 @@ typedef struct swz_gemm_opts {
 
 /* swz_gemm with explicit tile shape, dtype, 2-CTA mode, program count, trace,
  * wait bound and Stream-K tail.  opts may be NULL (= swz_gemm).  Extra
- * errors: SWZ_EUNSUPPORTED for tile_n not in {0,128,256}, split_tail with
- * cta_pair, tile_n 128 and B as K x N, or stream_k with more programs than
- * can be resident at
- * once (its pieces wait on one another); SWZ_EINVAL for stream_k without
- * persistent or with a missing, misaligned (256 B) or too small workspace,
- * and for smem_swizzle not in {0, 32, 64, 128}; for dynamic the same
- * workspace rules, SWZ_EINVAL for a value other than 0, 1 or 2, without
- * persistent or with stream_k or split_tail, SWZ_EUNSUPPORTED with a span
- * other than 128; for shared_a
- * SWZ_EINVAL for a value other than 0 or 1, SWZ_EUNSUPPORTED without cta_pair,
- * with tile_n 256, TF32, a span other than 128, stream_k, split_tail or
- * dynamic.
+ * errors: SWZ_EUNSUPPORTED for tile_n not in {0,128,256}, or stream_k
+ * with more programs than can be resident at once (its pieces wait on one
+ * another); SWZ_EINVAL for stream_k without persistent or with a missing,
+ * misaligned (256 B) or too small workspace, and for smem_swizzle not in
+ * {0, 32, 64, 128}; for dynamic the same workspace rules, SWZ_EINVAL for a
+ * value other than 0 or 1, without persistent or with stream_k,
+ * SWZ_EUNSUPPORTED with a span other than 128.
  * In Stream-K mode the trace records, for a split tile, the program that
  * wrote it. */
 int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N, int K,
@@ -246,25 +222,6 @@ int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N, int K,
 int swz_gemm_host(const void* h_A, const void* h_B, float* h_C, int M, int N, int K,
                   int order, int group, const swz_gemm_opts* opts, void* d_A, void* d_B,
                   float* d_C, int slabs, void* stream);
-
-/*
- * swz_gemm_host_tiled -- swz_gemm_host with C cut into blocks x blocks
- * blocks (0 = 4; at most 8; block edges multiples of 256) finished in a
- * growing square: row slab t of A and column panel t of B are copied in
- * (A0, B0, A1, B1, ...), and as soon as both are resident blocks (t, 0..t)
- * and (0..t-1, t) are multiplied (swz_gemm_ex, persistent = 1, order/group
- * within the block) and copied out.  C thus leaves while A and B are still
- * arriving; every C row of swz_gemm_host waits for all of B.  Column panels
- * of a K x N B are gathered into d_B by pitched copies (packed K x n_j
- * panels); with opts->b_layout = SWZ_B_NK (required for TF32) the panels
- * are contiguous rows of B.  d_C holds the blocks packed, not C's layout;
- * h_C receives C row-major (pitched copies).  Buffers, streams, ordering and
- * errors as swz_gemm_host.  The result equals swz_gemm_host's bit for bit (a
- * tile's K loop does not depend on the block it is computed in).
- */
-int swz_gemm_host_tiled(const void* h_A, const void* h_B, float* h_C, int M, int N, int K,
-                        int order, int group, const swz_gemm_opts* opts, void* d_A,
-                        void* d_B, float* d_C, int blocks, void* stream);
 
 /* Bytes of d_workspace a launch with these arguments needs (0 when
  * stream_k is off, the launch is not persistent or the tiles divide evenly

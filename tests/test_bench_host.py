@@ -94,12 +94,8 @@ def test_resolve_workload_custom_and_group_sizes():
 def test_workloads_and_capture_modes():
     import argparse
     base = dict(m=0, n=0, k=0, dtype="fp16", tile_n=0, pair=False, group_sizes="")
-    # shared A is modelled at the cluster tile: 128 x 256 model tiles, K steps
-    # of 128, half as many model CTAs as launched ones
     wl = bench.resolve_workload(argparse.Namespace(
-        **dict(base, workload="gemm6144x10240x4096_fp16_shared_a")))
-    assert wl["cfg"] == dict(cta_pair=True, shared_a=True)
-    assert wl["tile"] == (128, 256) and wl["tk"] == 128 and wl["conc_div"] == 2
+        **dict(base, workload="gemm6144x10240x4096_fp16_pair")))
     assert ("morton", 1) not in wl["sweep"] and ("xor", 1) not in wl["sweep"]
     # every named workload resolves, with a non-empty order sweep
     for name in bench.WORKLOADS:

@@ -72,26 +72,6 @@ def test_plan_without_device(swz):
     assert swz.gemm_plan(1024, 1024, 512, cta_pair=True, tile_n=128) == (8, 8, 4, 8, 64)
     rc, _ = swz.swz_gemm_plan(1024, 1024, 512, 1, swz.make_opts(cta_pair=True, num_programs=7))
     assert rc == swz.SWZ_EINVAL
-    # shared A: 4-CTA clusters of two 128-wide pairs, cluster tiles 256 x 256
-    # over a grid of 24 x 40; CTA tiles stay 128 x 128 (48 x 80 of them)
-    assert swz.gemm_plan(6144, 10240, 4096, cta_pair=True, shared_a=True) == (48, 80, 24, 40, 3840)
-    assert swz.gemm_plan(6144, 10240, 4096, True, cta_pair=True, shared_a=True,
-                         num_programs=144) == (48, 80, 24, 40, 144)
-    # ragged: 257 rows -> 2 cluster rows; 264 columns -> 2 cluster columns
-    assert swz.gemm_plan(257, 264, 64, cta_pair=True, tile_n=128, shared_a=True) == (
-        4, 4, 2, 2, 16)
-    assert swz.gemm_plan(300, 392, 64, True, cta_pair=True, shared_a=True,
-                         num_programs=1000) == (4, 4, 2, 2, 16)
-    rc, _ = swz.swz_gemm_plan(1024, 1024, 512, 1,  # not a multiple of 4
-                              swz.make_opts(cta_pair=True, num_programs=6, shared_a=True))
-    assert rc == swz.SWZ_EINVAL
-    for bad in (dict(cta_pair=True, tile_n=256, shared_a=True),       # 256-wide pairs
-                dict(cta_pair=False, shared_a=True)):                 # needs the pair
-        rc, _ = swz.swz_gemm_plan(1024, 1024, 512, 0, swz.make_opts(**bad))
-        assert rc == swz.SWZ_EUNSUPPORTED, bad
-    o = swz.make_opts(cta_pair=True)
-    o.shared_a = 2
-    assert swz.swz_gemm_plan(1024, 1024, 512, 0, o)[0] == swz.SWZ_EINVAL
 
 
 def test_stream_k_plan_keeps_every_program(swz):

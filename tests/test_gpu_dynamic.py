@@ -144,7 +144,6 @@ def test_errors(swz):
     assert call(workspace=ws[:128]) == swz.SWZ_EINVAL                # too small
     assert call(workspace=ws[16:]) == swz.SWZ_EINVAL                 # misaligned
     assert call(workspace=ws, stream_k=True) == swz.SWZ_EINVAL
-    assert call(workspace=ws, split_tail=True) == swz.SWZ_EINVAL
     assert call(workspace=ws, smem_swizzle=64) == swz.SWZ_EUNSUPPORTED
     assert swz.workspace_size(256, 256, 64, True, stream_k=False, dynamic=True) == 256
     assert swz.workspace_size(256, 256, 64, False, stream_k=False, dynamic=True) == 0
@@ -165,88 +164,8 @@ def test_withheld_load_times_out_cleanly(swz, cfg):
     assert torch.equal(C, swz.gemm(Ad, Bd, "row", 1, True, **cfg))
 
 
-# dynamic = 2: the full waves by work-index striding, the last, partial wave
-# claimed through the counter
-
-@pytest.mark.parametrize("shape", [(768, 640, 576), (300, 392, 200), (1100, 1304, 136)])
-@pytest.mark.parametrize("cfg", CFGS)
-@pytest.mark.parametrize("programs", [0, 4, 6])
-def test_tail_claim_exact(swz, shape, cfg, programs):
-    M, N, K = shape
-    A, B = si.small_int_gemm_inputs(M, N, K, "bf16", lo=-4, hi=4, seed=N + programs)
-    C = swz.gemm(A.cuda(), B.cuda(), "panel", 2, True, num_programs=programs, dynamic=2,
-                 workspace=_ws(), **cfg)
-    swz.check_status()
-    assert torch.equal(C.cpu().double(), ref.gemm_f64(A, B))
-
-
-@pytest.mark.parametrize("cfg", CFGS)
-def test_tail_claim_bit_identical_to_static(swz, cfg):
-    A, B = si.gemm_inputs(2048, 2048, 1024, "bf16", "normal", seed=6)
-    Ad, Bd = A.cuda(), B.cuda()
-    C0 = swz.gemm(Ad, Bd, "serpentine", 4, True, num_programs=6, **cfg)
-    ws = _ws()
-    for _ in range(2):
-        C1 = swz.gemm(Ad, Bd, "serpentine", 4, True, num_programs=6, dynamic=2, workspace=ws,
-                      **cfg)
-        swz.check_status()
-        assert torch.equal(C0, C1)
-
-
-def _check_tail_trace(trace, gm, gn, order, g, programs, cluster_m):
-    got = trace.view(gm, gn, 2).cpu().tolist()
-    cgm = gm // cluster_m
-    P = programs // cluster_m
-    S = (cgm * gn) // P  # full waves
-    ids = to.id_table(order, cgm, gn, g)
-    static = to.persistent_trace(order, gm, gn, g, programs, cluster_m=cluster_m)
-    per_prog = {}
-    for m in range(gm):
-        for n in range(gn):
-            prog, it = got[m][n]
-            w = ids[m // cluster_m][n]
-            assert prog % cluster_m == m % cluster_m
-            if w < S * P:
-                assert (prog, it) == static[(m, n)], (m, n)  # the full waves are static
-            else:
-                assert it >= S and 0 <= prog < programs, (m, n, prog, it)
-            per_prog.setdefault(prog, {})
-            assert it not in per_prog[prog]
-            per_prog[prog][it] = w
-    for prog, seq in per_prog.items():
-        its = sorted(seq)
-        assert its == list(range(len(its)))
-        tail = [seq[i] for i in its if i >= S]
-        assert all(a < b for a, b in zip(tail, tail[1:]))  # claimed from one counter
-    if cluster_m == 2:
-        for prog in range(0, programs, 2):
-            assert per_prog.get(prog) == per_prog.get(prog + 1)
-
-
-@pytest.mark.parametrize("order,g", [(to.ROW, 1), (to.PANEL, 4), (to.SERPENTINE, 2)])
-@pytest.mark.parametrize("programs", [7, 4])
-def test_tail_claim_trace_single_cta(swz, order, g, programs):
-    A, B = si.gemm_inputs(768, 640, 128, "fp16", "uniform", seed=3)
-    trace = torch.full((6 * 5 * 2,), -1, dtype=torch.int32, device="cuda")
-    C = swz.gemm(A.cuda(), B.cuda(), order, g, True, tile_n=128, num_programs=programs,
-                 trace=trace, dynamic=2, workspace=_ws())
-    swz.check_status()
-    _check_tail_trace(trace, 6, 5, order, g, programs, 1)
-    assert torch.equal(C, swz.gemm(A.cuda(), B.cuda(), order, g, True, tile_n=128))
-
-
-@pytest.mark.parametrize("programs", [4, 6])
-def test_tail_claim_trace_pair(swz, programs):
-    A, B = si.gemm_inputs(1536, 1280, 192, "bf16", "uniform", seed=2)
-    trace = torch.full((12 * 5 * 2,), -1, dtype=torch.int32, device="cuda")
-    swz.gemm(A.cuda(), B.cuda(), to.SERPENTINE, 2, True, cta_pair=True, num_programs=programs,
-             trace=trace, dynamic=2, workspace=_ws())
-    swz.check_status()
-    _check_tail_trace(trace, 12, 5, to.SERPENTINE, 2, programs, 2)
-
-
 def test_dynamic_mode_range(swz):
     A, B = si.gemm_inputs(256, 256, 64, "fp16", "uniform", seed=0)
     with pytest.raises(swz.SwzError) as e:
-        swz.gemm(A.cuda(), B.cuda(), "row", 1, True, dynamic=3, workspace=_ws())
+        swz.gemm(A.cuda(), B.cuda(), "row", 1, True, dynamic=2, workspace=_ws())
     assert e.value.code == swz.SWZ_EINVAL

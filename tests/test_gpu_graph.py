@@ -39,8 +39,8 @@ def _replays(swz, g, Ad, Bd, C, M, N, K, dtype, seeds):
 STATIC = [
     (768, 640, 1024, "bf16", dict(cta_pair=True)),
     (1000, 1000, 520, "fp16", dict(tile_n=256)),
-    (768, 640, 512, "fp16", dict(tile_n=128, split_tail=True, num_programs=7)),
-    (1024, 1024, 512, "bf16", dict(cta_pair=True, tile_n=128, shared_a=True, num_programs=8)),
+    (768, 640, 512, "fp16", dict(tile_n=128, num_programs=7)),
+    (1024, 1024, 512, "bf16", dict(cta_pair=True, tile_n=128, num_programs=8)),
 ]
 
 
@@ -79,10 +79,9 @@ def test_graph_stream_k_workspace(swz, M, N, K, cfg):
     assert torch.equal(C.cpu().double(), ref.gemm_f64(A, B))
 
 
-@pytest.mark.parametrize("mode", [1, 2])
-def test_graph_dynamic(swz, mode):
+def test_graph_dynamic(swz):
     M, N, K = 1280, 1024, 576
-    cfg = dict(cta_pair=True, num_programs=6, dynamic=mode)
+    cfg = dict(cta_pair=True, num_programs=6, dynamic=True)
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     Ad = torch.zeros((M, K), dtype=torch.float16, device="cuda")
     Bd = torch.zeros((K, N), dtype=torch.float16, device="cuda")

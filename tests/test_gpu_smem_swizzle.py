@@ -64,8 +64,7 @@ def test_tails(swz, cfg, programs, span):
     A, B = si.small_int_gemm_inputs(M, N, K, "bf16", lo=-3, hi=3, seed=programs + span)
     want = ref.gemm_f64(A, B)
     Ad, Bd = A.cuda(), B.cuda()
-    C = swz.gemm(Ad, Bd, "panel", 2, True, num_programs=programs, split_tail=True,
-                 smem_swizzle=span, **cfg)
+    C = swz.gemm(Ad, Bd, "panel", 2, True, num_programs=programs, smem_swizzle=span, **cfg)
     swz.check_status()
     assert torch.equal(C.cpu().double(), want)
     n = swz.workspace_size(M, N, K, True, num_programs=programs, **cfg)

@@ -51,8 +51,7 @@ def test_b_transposed_tails(swz, cfg, programs):
     A, B = si.small_int_gemm_inputs(M, N, K, "bf16", lo=-3, hi=3, seed=programs)
     Bt = B.t().contiguous().cuda()
     want = ref.gemm_f64(A, B)
-    C = swz.gemm(A.cuda(), Bt, "panel", 2, True, num_programs=programs, split_tail=True,
-                 b_transposed=True, **cfg)
+    C = swz.gemm(A.cuda(), Bt, "panel", 2, True, num_programs=programs, b_transposed=True, **cfg)
     swz.check_status()
     assert torch.equal(C.cpu().double(), want)
     n = swz.workspace_size(M, N, K, True, num_programs=programs, **cfg)

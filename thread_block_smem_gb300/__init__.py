@@ -37,7 +37,7 @@ EXPORTS = ["swz_tile_map", "swz_is_bijective", "swz_gemm", "swz_gemm_ex", "swz_g
            "swz_device_info", "swz_l2_model", "swz_gemm_workspace_size",
            "swz_gemm_streamk_noalloc", "swz_gemm_host", "swz_gemm_mma_sync", "swz_tc_rate",
            "swz_tc_rate_ex",
-           "swz_l2_model_bytes", "swz_gemm_host_tiled"]
+           "swz_l2_model_bytes"]
 
 
 class SwzError(RuntimeError):
@@ -53,8 +53,7 @@ class swz_gemm_opts(ctypes.Structure):
                 ("debug_flags", ctypes.c_uint32), ("timeout_ms", ctypes.c_uint32),
                 ("stream_k", ctypes.c_int), ("d_workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_uint64), ("b_layout", ctypes.c_int),
-                ("split_tail", ctypes.c_int), ("smem_swizzle", ctypes.c_int),
-                ("dynamic", ctypes.c_int), ("shared_a", ctypes.c_int)]
+                ("smem_swizzle", ctypes.c_int), ("dynamic", ctypes.c_int)]
 
 
 _lib = None
@@ -91,7 +90,6 @@ def lib() -> ctypes.CDLL:
                                                ctypes.POINTER(swz_gemm_opts), vp]
         L.swz_gemm_host.argtypes = [vp, vp, vp, i, i, i, i, i, ctypes.POINTER(swz_gemm_opts),
                                     vp, vp, vp, i, vp]
-        L.swz_gemm_host_tiled.argtypes = L.swz_gemm_host.argtypes
         L.swz_gemm_mma_sync.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, i, i, vp]
         L.swz_tc_rate.argtypes = [i, i, vp, vp, i, i, vp, vp, vp]
         L.swz_tc_rate_ex.argtypes = [i, i, i, i, vp, vp, i, i, vp, vp, vp]
@@ -149,13 +147,6 @@ def swz_gemm_host(hA, hB, hC, M, N, K, order, group, opts, dA, dB, dC, slabs=0, 
     return lib().swz_gemm_host(hA, hB, hC, M, N, K, order, group,
                                ctypes.byref(opts) if opts is not None else None,
                                dA, dB, dC, slabs, stream)
-
-
-def swz_gemm_host_tiled(hA, hB, hC, M, N, K, order, group, opts, dA, dB, dC, blocks=0,
-                        stream=0):
-    return lib().swz_gemm_host_tiled(hA, hB, hC, M, N, K, order, group,
-                                     ctypes.byref(opts) if opts is not None else None,
-                                     dA, dB, dC, blocks, stream)
 
 
 def swz_gemm_mma_sync(A, B, C, M, N, K, dtype, vec, per_phase, max_phase, pad, order, group,
@@ -312,14 +303,12 @@ def tile_map(order, grid_m, grid_n, group=1, device="cuda", stream=None):
 
 
 def make_opts(dtype=SWZ_F16, tile_n=0, cta_pair=False, num_programs=0, trace=None,
-              debug_flags=0, timeout_ms=0, stream_k=False, workspace=None, split_tail=False,
-              b_layout=SWZ_B_KN, smem_swizzle=0, dynamic=False, shared_a=False):
+              debug_flags=0, timeout_ms=0, stream_k=False, workspace=None,
+              b_layout=SWZ_B_KN, smem_swizzle=0, dynamic=False):
     o = swz_gemm_opts()
-    o.shared_a = 1 if shared_a else 0
     o.smem_swizzle = smem_swizzle
-    o.dynamic = int(dynamic)  # False / True, or 1 / 2 (2: only the last wave claimed)
+    o.dynamic = int(dynamic)
     o.b_layout = b_layout
-    o.split_tail = 1 if split_tail else 0
     o.stream_k = 1 if stream_k else 0
     if workspace is not None:
         o.d_workspace = workspace.data_ptr()
@@ -335,12 +324,12 @@ def make_opts(dtype=SWZ_F16, tile_n=0, cta_pair=False, num_programs=0, trace=Non
 
 
 def gemm_plan(M, N, K, persistent=False, tile_n=0, cta_pair=False, num_programs=0,
-              shared_a=False, stream_k=False):
+              stream_k=False):
     """(tiles_m, tiles_n, sched_m, sched_n, programs) of a GEMM launch
     (with ``stream_k`` the program count is not capped at the tile count)."""
     rc, v = swz_gemm_plan(M, N, K, int(bool(persistent)),
                           make_opts(tile_n=tile_n, cta_pair=cta_pair, num_programs=num_programs,
-                                    shared_a=shared_a, stream_k=stream_k))
+                                    stream_k=stream_k))
     _check(rc, "swz_gemm_plan")
     return v
 
@@ -368,8 +357,8 @@ def _dtype_code(t):
 
 def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
          cta_pair=False, num_programs=0, trace=None, debug_flags=0, timeout_ms=0,
-         stream_k=False, workspace=None, split_tail=False, b_transposed=False, smem_swizzle=0,
-         dynamic=False, shared_a=False, stream=None):
+         stream_k=False, workspace=None, b_transposed=False, smem_swizzle=0,
+         dynamic=False, stream=None):
     """C = A @ B (fp32) through swz_gemm_ex.  A: M x K; B: K x N, or N x K
     when ``b_transposed`` (B stored transposed); both fp16, both bf16, or both
     fp32 (multiplied as TF32); row-major contiguous CUDA tensors.  fp32 inputs
@@ -379,10 +368,7 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
     ``smem_swizzle``: swizzle span of the operand stages, 128 (0), 64 or 32.
     ``dynamic``: claim tiles at run time through an atomic counter kept in
     ``workspace`` (a CUDA tensor of at least workspace_size(..., dynamic=True)
-    bytes); persistent launches only.  ``dynamic=2``: the full waves by
-    work-index striding and only the last, partial wave claimed.  ``shared_a`` (with ``cta_pair``):
-    4-CTA clusters of two 128-wide pairs that load each A tile once and
-    multicast it to both."""
+    bytes); persistent launches only."""
     import torch
     if A.dtype != B.dtype:
         raise TypeError("A and B must have the same dtype")
@@ -400,23 +386,21 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
         raise ValueError("inner dimensions differ")
     C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=A.device)
     opts = make_opts(code, tile_n, cta_pair, num_programs, trace, debug_flags, timeout_ms,
-                     stream_k, workspace, split_tail, SWZ_B_NK if b_transposed else SWZ_B_KN,
-                     smem_swizzle, dynamic, shared_a)
+                     stream_k, workspace, SWZ_B_NK if b_transposed else SWZ_B_KN,
+                     smem_swizzle, dynamic)
     _check(swz_gemm_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _order(order),
                        group, int(bool(persistent)), opts, _stream(stream)), "swz_gemm_ex")
     return C
 
 
 def gemm_host(hA, hB, hC, dA, dB, dC, order="panel", group=8, *, tile_n=0, cta_pair=False,
-              num_programs=0, stream_k=False, workspace=None, split_tail=False, slabs=0,
-              b_transposed=False, blocks=None, shared_a=False, stream=None):
+              num_programs=0, stream_k=False, workspace=None, slabs=0,
+              b_transposed=False, stream=None):
     """C = A @ B from host tensors through swz_gemm_host.  hA (M x K), hB
     (K x N, or N x K when ``b_transposed``; always N x K for fp32 / TF32): CPU
     fp16/bf16/fp32 tensors (pinned for overlap); hC: CPU fp32 M x N;
     dA, dB, dC: CUDA tensors of the same shapes used as staging.  Asynchronous
-    on `stream`; synchronise before reading hC.  With ``blocks`` (0 = 4, at
-    most 8) the call goes through swz_gemm_host_tiled: C in blocks x blocks
-    blocks finished in a growing square, so C leaves while A and B arrive."""
+    on `stream`; synchronise before reading hC."""
     import torch
     M, K = hA.shape
     N = hB.shape[0] if (b_transposed or hA.dtype == torch.float32) else hB.shape[1]
@@ -427,14 +411,7 @@ def gemm_host(hA, hB, hC, dA, dB, dC, order="panel", group=8, *, tile_n=0, cta_p
         raise TypeError("A and B must have the same dtype")
     code = _dtype_code(hA.dtype)
     opts = make_opts(code, tile_n, cta_pair, num_programs, None, 0, 0, stream_k, workspace,
-                     split_tail, SWZ_B_NK if (b_transposed or code == SWZ_TF32) else SWZ_B_KN,
-                     shared_a=shared_a)
-    if blocks is not None:  # the growing-square pipeline (swz_gemm_host_tiled)
-        _check(swz_gemm_host_tiled(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K,
-                                   _order(order), group, opts, dA.data_ptr(), dB.data_ptr(),
-                                   dC.data_ptr(), blocks, _stream(stream)),
-               "swz_gemm_host_tiled")
-        return hC
+                     SWZ_B_NK if (b_transposed or code == SWZ_TF32) else SWZ_B_KN)
     _check(swz_gemm_host(hA.data_ptr(), hB.data_ptr(), hC.data_ptr(), M, N, K, _order(order),
                          group, opts, dA.data_ptr(), dB.data_ptr(), dC.data_ptr(), slabs,
                          _stream(stream)), "swz_gemm_host")

@@ -31,19 +31,9 @@
 //   * CTA pair (PAIR): 2-CTA cluster, tcgen05 cta_group::2, MMA 256 x BN.
 //     Each CTA loads its own 128 rows of A and its half of B's columns;
 //     the leader issues the MMAs and its commits are multicast to both CTAs.
-//   * Shared A (MCA, with PAIR, 128-wide tiles, 128-byte span): 4-CTA
-//     clusters of two pairs side by side in N (cluster tile 256 x 256).  The
-//     two CTAs that need the same 128 rows of A (cluster ranks r and r + 2)
-//     each load 64 of them and multicast them to both, so each A byte leaves
-//     L2 once per cluster instead of twice (a 128-wide tile needs 1.5x the
-//     operand bytes per FLOP of a 256-wide one).  A stage is refilled only
-//     when both pairs' MMAs have released it (every leader's commit reaches
-//     all four CTAs).  It halves A's L2 reads but not the bytes each SM
-//     receives, and measures no faster than the plain 128-wide pair.
 //   * Work items come from the static schedule (Schedule: work_idx striding,
-//     optional Stream-K tail or split tail) or, with DYN, from an atomic
-//     counter published one item ahead to all roles through a shared-memory
-//     ring.  A Stream-K tile's owner streams its peers' partial sums into a
+//     optional Stream-K tail) or, with DYN, from an atomic counter published
+//     one item ahead to all roles through a shared-memory ring.  A Stream-K tile's owner streams its peers' partial sums into a
 //     ring of slots in its idle operand stages with bulk copies.
 //   * Every wait is bounded (globaltimer); on expiry the kernel records
 //     SWZ_ETIMEOUT in a device status word, drains what it issued, frees TMEM
@@ -134,23 +124,20 @@ struct Params {
   int order, group;
   uint32_t sched_m, sched_n;  // scheduler grid (cluster tiles with PAIR)
   uint32_t num_kb;            // ceil(K / BK)
-  uint32_t idesc;       // full-width MMA (N = BN)
-  uint32_t idesc_half;  // half-width MMA (N = BN/2) for split tail tiles
+  uint32_t idesc;       // MMA instruction descriptor (N = BN)
   uint32_t b3d;         // B's share of a full-width tile in one 3-D box (N % span == 0)
   uint32_t b_kmajor;    // B given as N x K (K contiguous): K-major operand
   uint32_t a3d;         // A's stage in one 3-D box (span < 128 and K % span == 0)
   int32_t* trace;
   uint32_t debug_flags;
   uint64_t timeout_ns;
-  // tail policies (persistent launches only; both 0 = whole tiles everywhere)
-  uint32_t split_tail;  // halve the N width of the tiles of the last wave
+  // tail policy (persistent launches only; 0 = whole tiles everywhere)
   uint32_t stream_k;
   uint32_t epoch;      // value a finished partial's flag takes in this launch
   uint32_t* sk_flags;  // [cluster][rank][lane quarter]
   float4* sk_ws;       // [cluster][rank][BN/4 column groups][128 rows] float4
   uint32_t* dyn_counter;  // dynamic scheduler: work indices claimed beyond the first wave
   uint32_t epi_pace_ns;   // gap between an epilogue warp's chunk stores (tiles with a successor)
-  uint32_t dyn_static;    // dynamic: items each cluster takes by striding before claiming
 };
 
 enum ItemKind : int { kWhole = 0, kFirst = 1, kPartial = 2 };
@@ -166,33 +153,24 @@ enum ItemKind : int { kWhole = 0, kFirst = 1, kPartial = 2 };
 // (R < P), so it holds at most two pieces: a piece that starts inside a tile
 // (a partial, written to the workspace) and a piece that starts a tile (its
 // first piece: the cluster owning it adds the other pieces and writes C).
-// With split_tail, when the R = U mod P tail units would leave most clusters
-// idle in the last wave and 2R <= P, each tail unit is cut into two halves of
-// N width BN/2 (left half, right half) and cluster h takes half-unit h: the
-// last wave then runs on 2R clusters for half as long, with no data exchanged
-// between clusters.
 struct Schedule {
   uint32_t c, P, U, kb;
   uint32_t dp_end;  // units below this are whole tiles
   uint32_t n_dp;    // whole tiles of this cluster
-  uint32_t n_half;  // 1 if this cluster takes a half-width tail tile
   uint64_t I;       // Stream-K tail iterations
   uint64_t s, e;    // this cluster's Stream-K tail range [s, e)
   uint64_t Iq;      // I / P and I % P: range starts are stepped from one
   uint32_t Ir;      // cluster to the next by addition (64-bit division is slow)
 
   __device__ __forceinline__ void init(uint32_t c_, uint32_t P_, uint32_t U_, uint32_t kb_,
-                                       bool sk, bool split) {
+                                       bool sk) {
     c = c_;
     P = P_;
     U = U_;
     kb = kb_;
-    uint32_t R = U % P;
-    const bool halves = !sk && split && R > 0 && 2 * R <= P;
-    if (!sk && !halves) R = 0;
+    const uint32_t R = sk ? U % P : 0u;
     dp_end = U - R;
     n_dp = c < dp_end ? (dp_end - c + P - 1) / P : 0u;
-    n_half = halves && c < 2 * R ? 1u : 0u;
     I = sk ? uint64_t(R) * kb : 0u;
     s = range_start(c);
     e = range_start(c + 1);
@@ -219,11 +197,9 @@ struct Schedule {
     }
     ++k.cc;
   }
-  // The i-th piece of work: unit, K-block range [k0, k1), kind, and which
-  // half of the N width (-1: the whole width).
+  // The i-th piece of work: unit, K-block range [k0, k1) and kind.
   __device__ __forceinline__ bool item(uint32_t i, uint32_t& unit, uint32_t& k0, uint32_t& k1,
-                                       int& kind, int& half) const {
-    half = -1;
+                                       int& kind) const {
     if (i < n_dp) {
       unit = c + i * P;
       k0 = 0;
@@ -232,15 +208,6 @@ struct Schedule {
       return true;
     }
     i -= n_dp;
-    if (n_half) {
-      if (i != 0) return false;
-      unit = dp_end + c / 2;
-      half = int(c & 1u);
-      k0 = 0;
-      k1 = kb;
-      kind = kWhole;
-      return true;
-    }
     if (s >= e) return false;
     const uint64_t t = s / kb + i;
     const uint64_t t0 = t * kb;
@@ -315,18 +282,15 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
   while (ptx::global_timer_ns() - t0 < ns) __nanosleep(1000);
 }
 
-template <int BN, bool PAIR, int KIND, int SW, bool DYN, bool MCA = false>
+template <int BN, bool PAIR, int KIND, int SW, bool DYN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA3,
                 const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmB3,
                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ Params p) {
   constexpr int KA = SW == 128 ? stage_atoms(BN) : 1;
   using K_ = Cfg<BN, PAIR, KA>;
-  constexpr int CL = K_::CG;
-  constexpr int NP = MCA ? 2 : 1;  // CTA pairs per cluster, side by side in N
-  constexpr int CLN = CL * NP;     // CTAs per cluster
+  constexpr int CL = K_::CG;  // CTAs per cluster
   constexpr int STAGES = K_::STAGES;
-  static_assert(!MCA || (PAIR && BN == 128 && SW == 128 && !DYN), "shared-A configuration");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -348,23 +312,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile uint32_t* ring_w = tmem_slot + 2;
 
   const uint32_t warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const uint32_t crank = PAIR ? ptx::cluster_ctarank() : 0u;  // rank in the cluster
-  const uint32_t rank = crank & 1u;   // rank in the CTA pair: which 128 rows of the pair's tile
-  const uint32_t pidx = crank >> 1;   // pair index (MCA): which 128 columns of the cluster tile
-  const uint32_t lead = crank & ~1u;  // cluster rank of the pair's leader
+  // rank in the CTA pair: which 128 rows of the pair's tile (the leader, rank
+  // 0, issues the MMAs)
+  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;
   const bool leader = rank == 0;
 
   if (threadIdx.x == 0) {
     ptx::prefetch_tensormap(&tmA);
-    if constexpr (SW != 128 || MCA) {
-      if (MCA || p.a3d) ptx::prefetch_tensormap(&tmA3);
+    if constexpr (SW != 128) {
+      if (p.a3d) ptx::prefetch_tensormap(&tmA3);
     }
     ptx::prefetch_tensormap(&tmB);
     if (p.b3d) ptx::prefetch_tensormap(&tmB3);
     ptx::prefetch_tensormap(&tmC);
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(full_bar(s), 1);
-      ptx::mbar_init(empty_bar(s), NP);  // one commit from each pair's leader
+      ptx::mbar_init(empty_bar(s), 1);  // the leader's MMA commit
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(tfull_bar(a), 1);
@@ -395,15 +358,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   Ctl ctl;
   ctl.abort_flag = abort_flag;
-  ctl.n_peers = CLN - 1;
-  for (uint32_t j = 1; j < uint32_t(CLN); ++j)
-    ctl.peer_abort[j - 1] = ptx::map_to_rank(ptx::smem_u32(abort_flag), crank ^ j);
+  ctl.n_peers = CL - 1;
+  if constexpr (PAIR) ctl.peer_abort[0] = ptx::map_to_rank(ptx::smem_u32(abort_flag), rank ^ 1u);
   ctl.timeout_ns = p.timeout_ns;
 
   const uint32_t units = p.sched_m * p.sched_n;
   Schedule sch;
-  sch.init(blockIdx.x / CLN, gridDim.x / CLN, units, p.num_kb, p.stream_k != 0,
-           p.split_tail != 0);
+  sch.init(blockIdx.x / CL, gridDim.x / CL, units, p.num_kb, p.stream_k != 0);
   bool aborted = false;
 
   // Dynamic scheduler (DYN): the producer of the leader CTA claims work
@@ -438,24 +399,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t dyn_published = 0;  // the claiming producer: items published so far
   bool dyn_ended = false;
   auto next_item = [&](uint32_t i, bool fetch, uint32_t& w, uint32_t& kbeg, uint32_t& kend,
-                       int& kind, int& half) -> bool {
+                       int& kind) -> bool {
     if constexpr (!DYN) {
-      return sch.item(i, w, kbeg, kend, kind, half);
+      return sch.item(i, w, kbeg, kend, kind);
     } else {
       kbeg = 0;
       kend = p.num_kb;
       kind = kWhole;
-      half = -1;
       if (fetch) {
         // Published one item ahead: the peer CTA's producer learns its next
         // tile from the ring, and publishing only when this producer starts
         // that tile's loads delayed the peer's loads, and with them the
-        // pair's MMAs, at every tile boundary.  The first dyn_static items
-        // come by work-index striding, the rest are claimed.
+        // pair's MMAs, at every tile boundary.  The first item is the
+        // cluster's own index, the rest are claimed.
         while (!dyn_ended && dyn_published <= i + 1u) {
           const uint32_t k = dyn_published;
-          uint32_t wk = k < p.dyn_static ? sch.c + k * sch.P
-                                         : p.dyn_static * sch.P + atomicAdd(p.dyn_counter, 1u);
+          uint32_t wk = k == 0 ? sch.c : sch.P + atomicAdd(p.dyn_counter, 1u);
           if (wk >= units) wk = kNoWork;
           if (!ring_put(k, wk)) { aborted = true; return false; }
           ++dyn_published;
@@ -471,10 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
   // warp-wide form for the epilogue warps: lane 0 reads the ring
-  auto next_item_warp = [&](uint32_t i, uint32_t& w, uint32_t& kbeg, uint32_t& kend, int& kind,
-                            int& half) -> bool {
+  auto next_item_warp = [&](uint32_t i, uint32_t& w, uint32_t& kbeg, uint32_t& kend,
+                            int& kind) -> bool {
     if constexpr (!DYN) {
-      return sch.item(i, w, kbeg, kend, kind, half);
+      return sch.item(i, w, kbeg, kend, kind);
     } else {
       uint32_t wl = 0;
       int ok = 1;
@@ -484,7 +443,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       kbeg = 0;
       kend = p.num_kb;
       kind = kWhole;
-      half = -1;
       if (!ok) { aborted = true; return false; }
       return w != kNoWork;
     }
@@ -496,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0;
       bool skip = (p.debug_flags & SWZ_DEBUG_SKIP_FIRST_LOAD) != 0;
       uint32_t w, kbeg, kend;
-      int kind, half;
+      int kind;
       // Swizzle span sw: a stage's 128-byte rows are split into 128/sw
       // column groups of sw bytes (xe elements), each a TMA box of its own
       // (or one 3-D box for all of them); a group holds all rows of the
@@ -509,22 +467,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int xe = int(sw) / (KIND == 0 ? 2 : 4);
       const int xn = int(sw) / 2;
       const uint32_t b_box_bytes = uint32_t(BK) * sw;
-      for (uint32_t i = 0; !aborted && next_item(i, leader, w, kbeg, kend, kind, half); ++i) {
+      for (uint32_t i = 0; !aborted && next_item(i, leader, w, kbeg, kend, kind); ++i) {
         const TileCoord t = tile_of(p.order, w, p.sched_m, p.sched_n, uint32_t(p.group));
         const int32_t m0 = int32_t((t.m * CL + rank) * BM);
-        // B columns this CTA loads: its share of the tile (or of one half)
-        const int local = half < 0 ? K_::BN_LOCAL : K_::BN_LOCAL / 2;
-        const int32_t n0 = int32_t((t.n * NP + pidx) * BN + (half < 0 ? 0 : half * (BN / 2)) +
-                                   rank * local);
-        const int boxes = local / xn;  // xn = 64 when sw == 128
-        const uint32_t tx = uint32_t(CL) * uint32_t(K_::A_BYTES + local * 128 * KA);
+        // B columns this CTA loads: its share of the tile
+        constexpr int local = K_::BN_LOCAL;
+        const int32_t n0 = int32_t(t.n * BN + rank * local);
+        constexpr int boxes = local / xn;  // xn = 64 when sw == 128
+        constexpr uint32_t tx = K_::TX_BYTES;
         for (uint32_t kb = kbeg; kb < kend; ++kb) {
           if (!wait(empty_bar(stage), phase ^ 1u, ctl)) { aborted = true; break; }
           if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), tx);
           if (skip) {
             skip = false;
           } else {
-            const uint32_t fb = PAIR ? ptx::map_to_rank(full_bar(stage), lead) : full_bar(stage);
+            const uint32_t fb = PAIR ? ptx::map_to_rank(full_bar(stage), 0) : full_bar(stage);
             const int32_t k0 = int32_t(kb * bk_elems<KIND>() * KA);
             const uint32_t a_dst = sA + stage * K_::A_BYTES, b_dst = sB + stage * K_::B_BYTES;
             // A: one box of 128 rows per column group, or one 3-D box
@@ -533,32 +490,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             // `boxes` column groups) when the map allows it, else one 2-D box
             // per group; the shared-memory layout is the same either way.
             // B, K-major (N x K given): per column group one 2-D box of
-            // `local` rows (tmB: full width, tmB3: half width).
-            const bool one_box = p.b3d && half < 0;
+            // `local` rows.
+            const bool one_box = p.b3d != 0;
             if constexpr (SW == 128) {
               // K-major operands: one box per 128-byte atom (KA of them);
               // N-major B: boxes of 64 columns x BK * KA rows
               constexpr int ke = bk_elems<KIND>();
               if constexpr (PAIR) {
-                if constexpr (MCA) {
-                  // rows 64*pidx .. +63 of this CTA's A block, multicast to
-                  // this CTA and the one at rank ^ 2 (same rows, other pair);
-                  // tmA3 holds the 64-row box
-                  const uint16_t mask = uint16_t(0x5u << rank);
 #pragma unroll
-                  for (int g = 0; g < KA; ++g)
-                    ptx::tma_load_2d_pair_mc(a_dst + g * (BM * 128) + pidx * (64 * 128), &tmA3, fb,
-                                             k0 + g * ke, m0 + int32_t(pidx * 64), mask);
-                } else {
-#pragma unroll
-                  for (int g = 0; g < KA; ++g)
-                    ptx::tma_load_2d_pair(a_dst + g * (BM * 128), &tmA, fb, k0 + g * ke, m0);
-                }
+                for (int g = 0; g < KA; ++g)
+                  ptx::tma_load_2d_pair(a_dst + g * (BM * 128), &tmA, fb, k0 + g * ke, m0);
                 if (p.b_kmajor)
 #pragma unroll
                   for (int g = 0; g < KA; ++g)
-                    ptx::tma_load_2d_pair(b_dst + g * local * 128, half < 0 ? &tmB : &tmB3, fb,
-                                          k0 + g * ke, n0);
+                    ptx::tma_load_2d_pair(b_dst + g * local * 128, &tmB, fb, k0 + g * ke, n0);
                 else if (one_box)
                   ptx::tma_load_3d_pair(b_dst, &tmB3, fb, 0, k0, n0 / 64);
                 else
@@ -571,8 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.b_kmajor)
 #pragma unroll
                   for (int g = 0; g < KA; ++g)
-                    ptx::tma_load_2d(b_dst + g * local * 128, half < 0 ? &tmB : &tmB3, fb,
-                                     k0 + g * ke, n0);
+                    ptx::tma_load_2d(b_dst + g * local * 128, &tmB, fb, k0 + g * ke, n0);
                 else if (one_box)
                   ptx::tma_load_3d(b_dst, &tmB3, fb, 0, k0, n0 / 64);
                 else
@@ -587,8 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   ptx::tma_load_2d_pair(a_dst + g * BM * sw, &tmA, fb, k0 + g * xe, m0);
               if (p.b_kmajor)
                 for (int g = 0; g < groups; ++g)
-                  ptx::tma_load_2d_pair(b_dst + g * local * sw, half < 0 ? &tmB : &tmB3, fb,
-                                        k0 + g * xe, n0);
+                  ptx::tma_load_2d_pair(b_dst + g * local * sw, &tmB, fb, k0 + g * xe, n0);
               else if (one_box)
                 ptx::tma_load_3d_pair(b_dst, &tmB3, fb, 0, k0, n0 / xn);
               else
@@ -602,8 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   ptx::tma_load_2d(a_dst + g * BM * sw, &tmA, fb, k0 + g * xe, m0);
               if (p.b_kmajor)
                 for (int g = 0; g < groups; ++g)
-                  ptx::tma_load_2d(b_dst + g * local * sw, half < 0 ? &tmB : &tmB3, fb,
-                                   k0 + g * xe, n0);
+                  ptx::tma_load_2d(b_dst + g * local * sw, &tmB, fb, k0 + g * xe, n0);
               else if (one_box)
                 ptx::tma_load_3d(b_dst, &tmB3, fb, 0, k0, n0 / xn);
               else
@@ -630,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool issued = false;
       uint32_t w, kbeg, kend;
-      int kind, half;
+      int kind;
       // Operand layouts of a stage for swizzle span sw (see the producer).
       // K-major block of R rows: 8-row groups 8*sw bytes apart (stride byte
       // offset); MMA k-slice kk (32 bytes of each row) starts at column
@@ -645,12 +587,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto kmajor_off = [&](int kk, uint32_t rows) {
         return uint64_t(((uint32_t(kk) * 32u / sw) * rows * sw + (uint32_t(kk) * 32u) % sw) >> 4);
       };
-      for (uint32_t i = 0; !aborted && next_item(i, false, w, kbeg, kend, kind, half); ++i) {
+      const uint32_t idesc = p.idesc;
+      constexpr uint32_t b_rows = uint32_t(K_::BN_LOCAL);
+      for (uint32_t i = 0; !aborted && next_item(i, false, w, kbeg, kend, kind); ++i) {
         if (!wait(tempty_bar(acc), acc_phase ^ 1u, ctl)) { aborted = true; break; }
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
-        const uint32_t idesc = half < 0 ? p.idesc : p.idesc_half;
-        const uint32_t b_rows = uint32_t(half < 0 ? K_::BN_LOCAL : K_::BN_LOCAL / 2);
         uint64_t a_step[4] = {}, b_step[4] = {};
         if constexpr (SW != 128) {
 #pragma unroll
@@ -690,9 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::mma<CL, KIND>(d, adesc + a_step[kk], bdesc + b_step[kk], idesc, 1u);
           }
           issued = true;
-          // the stage is free once every pair that reads it is done: MCA
-          // stages also hold A that the other pair's CTAs loaded
-          if constexpr (PAIR) ptx::mma_commit_pair(empty_bar(st), MCA ? 0xF : 0x3);
+          // the stage is free (in both CTAs of a pair) once these MMAs are done
+          if constexpr (PAIR) ptx::mma_commit_pair(empty_bar(st), 0x3);
           else ptx::mma_commit(empty_bar(st));
         };
         // The issuing thread is the critical path: an MMA takes nearly as
@@ -711,14 +652,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (aborted) break;
-        if constexpr (PAIR) ptx::mma_commit_pair(tfull_bar(acc), uint16_t(0x3u << lead));
+        if constexpr (PAIR) ptx::mma_commit_pair(tfull_bar(acc), 0x3);
         else ptx::mma_commit(tfull_bar(acc));
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       if (aborted && issued) {
         // drain: wait (bounded) until every MMA issued so far has completed
-        if constexpr (PAIR) ptx::mma_commit_pair(drain_bar, uint16_t(1u << lead));
+        if constexpr (PAIR) ptx::mma_commit_pair(drain_bar, 0x1);
         else ptx::mma_commit(drain_bar);
         const uint64_t t0 = ptx::global_timer_ns();
         while (!ptx::mbar_try_wait(drain_bar, 0) && ptx::global_timer_ns() - t0 < p.timeout_ns) {
@@ -736,13 +677,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t q = warp & 3u;
     uint32_t acc = 0, acc_phase = 0;
     uint32_t w, kbeg, kend;
-    int kind, half;
-    for (uint32_t i = 0; next_item_warp(i, w, kbeg, kend, kind, half); ++i) {
+    int kind;
+    for (uint32_t i = 0; next_item_warp(i, w, kbeg, kend, kind); ++i) {
       const bool ok = wait(tfull_bar(acc), acc_phase, ctl);
       if (!__all_sync(0xFFFFFFFFu, ok)) { aborted = true; break; }
       ptx::tc_fence_after();
       const TileCoord t = tile_of(p.order, w, p.sched_m, p.sched_n, uint32_t(p.group));
-      const uint32_t cta_m = t.m * CL + rank, cta_n = t.n * NP + pidx;
+      const uint32_t cta_m = t.m * CL + rank, cta_n = t.n;
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + acc * BN;
       if (kind == kPartial) {
         // workspace slot of this CTA: per warp and 32-column chunk one
@@ -765,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), lead));
+          if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
           else ptx::mbar_arrive(tempty_bar(acc));
           ptx::st_release_gpu(p.sk_flags + (sch.c * CL + rank) * 4u + q, p.epoch);
         }
@@ -854,8 +795,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 8 different bank groups) -> TMA store (full 128-byte lines; parts
         // beyond M or N are clipped by the tensor map).
         const int32_t row0 = int32_t(cta_m * BM + q * 32u);
-        const int width = half < 0 ? BN : BN / 2;
-        const int32_t col0 = int32_t(cta_n) * BN + (half < 0 ? 0 : half * (BN / 2));
+        constexpr int width = BN;
+        const int32_t col0 = int32_t(cta_n) * BN;
         const uint32_t stg_warp = sStg + (warp - 2u) * 2u * K_::STG_BOX_BYTES;
         // A tile's C leaves as 4 x width/32 TMA stores of 4 KB; issued in one
         // burst they share the TMA unit with the operand loads of the next
@@ -866,8 +807,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t pace_ns = 0;
         if constexpr (!DYN) {
           uint32_t w2, b2, e2;
-          int k2, h2;
-          if (p.epi_pace_ns && sch.item(i + 1, w2, b2, e2, k2, h2)) pace_ns = p.epi_pace_ns;
+          int k2;
+          if (p.epi_pace_ns && sch.item(i + 1, w2, b2, e2, k2)) pace_ns = p.epi_pace_ns;
         } else {
           // the ring's next slot, if the producer has published it already
           // (it claims a tile before loading it, so usually long before);
@@ -941,10 +882,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), lead));
+          if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
           else ptx::mbar_arrive(tempty_bar(acc));
           if (warp == 2 && p.trace) {
-            const uint64_t idx = uint64_t(cta_m) * (p.sched_n * NP) + cta_n;
+            const uint64_t idx = uint64_t(cta_m) * p.sched_n + cta_n;
             p.trace[2 * idx] = int32_t(blockIdx.x);
             p.trace[2 * idx + 1] = int32_t(i);
           }
@@ -1048,15 +989,14 @@ static int encode_groups(CUtensorMap* map, int dtype, const void* base, uint64_t
 struct Plan {
   int bn;
   bool pair;
-  bool mca;  // 4-CTA clusters of two pairs sharing A
   uint32_t tiles_m, tiles_n, sched_m, sched_n, units;
   int programs;
 };
 
-template <int BN, bool PAIR, int KIND, bool MCA = false>
+template <int BN, bool PAIR, int KIND>
 static int kernel_capacity(const DeviceInfo& dev, int* programs) {
   constexpr int SW = 128;
-  constexpr int CLN = (PAIR ? 2 : 1) * (MCA ? 2 : 1);
+  constexpr int CLN = PAIR ? 2 : 1;
   using K_ = Cfg<BN, PAIR, stage_atoms(BN)>;
   static std::mutex mu;
   static int cache[64] = {};
@@ -1067,13 +1007,13 @@ static int kernel_capacity(const DeviceInfo& dev, int* programs) {
       return SWZ_OK;
     }
   }
-  auto kern = gemm_kernel<BN, PAIR, KIND, SW, false, MCA>;
+  auto kern = gemm_kernel<BN, PAIR, KIND, SW, false>;
   SWZ_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     K_::SMEM_BYTES));
   int cap = 0;
   if constexpr (PAIR) {
-    // clusters of CLN CTAs fit a GPC only whole: with 4 the count can leave
-    // SMs idle (GPCs whose SM count is not a multiple of 4)
+    // clusters fit a GPC only whole: ask the occupancy API how many can be
+    // resident at once
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(CLN * dev.num_sms);
     cfg.blockDim = dim3(kThreads);
@@ -1104,7 +1044,6 @@ static int kernel_capacity(const DeviceInfo& dev, int* programs) {
 static int capacity_for(const Plan& pl, const DeviceInfo& dev, int* cap) {
   // the three configurations share their shared-memory footprint across
   // kinds, so the f16 kernels' residency stands for both
-  if (pl.mca) return kernel_capacity<128, true, 0, true>(dev, cap);
   if (pl.pair) {
     if (pl.bn == 128) return kernel_capacity<128, true, 0>(dev, cap);
     return kernel_capacity<256, true, 0>(dev, cap);
@@ -1116,22 +1055,16 @@ static int capacity_for(const Plan& pl, const DeviceInfo& dev, int* cap) {
 static int make_plan(int M, int N, int persistent, const swz_gemm_opts& o, const DeviceInfo* dev,
                      Plan* pl) {
   if (o.tile_n != 0 && o.tile_n != 128 && o.tile_n != 256) return SWZ_EUNSUPPORTED;
-  if (o.shared_a != 0 && o.shared_a != 1) return SWZ_EINVAL;
   pl->pair = o.cta_pair != 0;
-  pl->mca = o.shared_a != 0;
-  // shared A: two 128-wide pairs per cluster
-  if (pl->mca && (!pl->pair || o.tile_n == 256)) return SWZ_EUNSUPPORTED;
-  pl->bn = o.tile_n ? o.tile_n : (pl->mca ? 128 : pl->pair || N > 128 ? 256 : 128);
-  const int np = pl->mca ? 2 : 1;       // pairs side by side in N
-  const int cl = pl->pair ? 2 : 1;      // CTAs of a pair, stacked in M
-  const int cln = cl * np;              // CTAs per cluster
-  const uint64_t sm = (uint64_t(M) + BM * cl - 1) / (BM * cl);
-  const uint64_t sn = (uint64_t(N) + uint64_t(pl->bn) * np - 1) / (uint64_t(pl->bn) * np);
+  pl->bn = o.tile_n ? o.tile_n : (pl->pair || N > 128 ? 256 : 128);
+  const int cln = pl->pair ? 2 : 1;  // CTAs per cluster (a pair is stacked in M)
+  const uint64_t sm = (uint64_t(M) + BM * cln - 1) / (BM * cln);
+  const uint64_t sn = (uint64_t(N) + uint64_t(pl->bn) - 1) / uint64_t(pl->bn);
   if (sm * sn * cln > uint64_t(INT32_MAX)) return SWZ_EINVAL;
   pl->sched_m = uint32_t(sm);
   pl->sched_n = uint32_t(sn);
-  pl->tiles_m = uint32_t(sm * cl);
-  pl->tiles_n = uint32_t(sn * np);
+  pl->tiles_m = uint32_t(sm * cln);
+  pl->tiles_n = uint32_t(sn);
   pl->units = uint32_t(sm * sn);
   if (o.num_programs < 0 || (o.num_programs % cln) != 0) return SWZ_EINVAL;
   if (!persistent) {
@@ -1173,14 +1106,14 @@ static SkLayout sk_layout(const Plan& pl, int persistent, const swz_gemm_opts& o
   return L;
 }
 
-template <int BN, bool PAIR, int KIND, int SW, bool DYN, bool MCA = false>
+template <int BN, bool PAIR, int KIND, int SW, bool DYN>
 static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& ta3,
                   const CUtensorMap& tb, const CUtensorMap& tb3, const CUtensorMap& tc,
                   const Params& prm, cudaStream_t stream) {
   using K_ = Cfg<BN, PAIR, SW == 128 ? stage_atoms(BN) : 1>;
   static std::mutex mu;
   static bool attr_set[64] = {};
-  auto kern = gemm_kernel<BN, PAIR, KIND, SW, DYN, MCA>;
+  auto kern = gemm_kernel<BN, PAIR, KIND, SW, DYN>;
   int dev = 0;
   SWZ_CUDA_TRY(cudaGetDevice(&dev));
   {
@@ -1199,7 +1132,7 @@ static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& ta3,
   cudaLaunchAttribute attr[1];
   if constexpr (PAIR) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = MCA ? 4 : 2;
+    attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -1220,10 +1153,6 @@ template <int SW, bool DYN>
 static int dispatch(const Plan& pl, bool tf32, const CUtensorMap& ta, const CUtensorMap& ta3,
                     const CUtensorMap& tb, const CUtensorMap& tb3, const CUtensorMap& tc,
                     const Params& prm, cudaStream_t s) {
-  if constexpr (SW == 128 && !DYN) {
-    if (pl.mca) return launch<128, true, 0, SW, DYN, true>(pl, ta, ta3, tb, tb3, tc, prm, s);
-  }
-  if (pl.mca) return SWZ_EUNSUPPORTED;
   if (tf32) {
     if (pl.pair && pl.bn == 128)
       return launch<128, true, 1, SW, DYN>(pl, ta, ta3, tb, tb3, tc, prm, s);
@@ -1358,9 +1287,6 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   if (o.dtype == SWZ_TF32 && o.b_layout != SWZ_B_NK) return SWZ_EUNSUPPORTED;
   const bool tf32 = o.dtype == SWZ_TF32;
   const uint32_t span = o.smem_swizzle ? uint32_t(o.smem_swizzle) : 128u;
-  // shared A: 16-bit operands, the 128-byte span, the static whole-tile schedule
-  if (pl.mca && (tf32 || span != 128 || o.stream_k || o.split_tail || o.dynamic))
-    return SWZ_EUNSUPPORTED;
   const uint32_t esize = tf32 ? 4u : 2u;
   const uint32_t bke = 128u / esize;  // K elements per 128-byte stage row
   const uint32_t xe = span / esize;   // elements per swizzle span
@@ -1378,18 +1304,13 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   if (a3d) {
     rc = encode_groups(&ta3, o.dtype, A, uint64_t(M), uint64_t(K), xe, BM, 128 / span, span);
     if (rc != SWZ_OK) return rc;
-  } else if (pl.mca) {
-    // shared A: each CTA loads half of a 128-row block (64-row boxes)
-    rc = encode_2d(&ta3, o.dtype, A, uint64_t(M), uint64_t(K), xe, BM / 2, span);
-    if (rc != SWZ_OK) return rc;
   }
   bool b3d = false;
   if (b_kmajor) {
-    // B given as N x K: like A, boxes of `local` (tb) or local/2 (tb3) rows
+    // B given as N x K: like A, boxes of `local` rows
     rc = encode_2d(&tb, o.dtype, B, uint64_t(N), uint64_t(K), xe, local, span);
     if (rc != SWZ_OK) return rc;
-    rc = encode_2d(&tb3, o.dtype, B, uint64_t(N), uint64_t(K), xe, local / 2, span);
-    if (rc != SWZ_OK) return rc;
+    tb3 = tb;
   } else {
     const uint32_t xn = span / 2;  // B columns per span (16-bit elements)
     rc = encode_2d(&tb, o.dtype, B, uint64_t(K), uint64_t(N), xn, BK * ka, span);
@@ -1418,19 +1339,11 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   prm.sched_n = pl.sched_n;
   prm.num_kb = uint32_t((uint32_t(K) + bke * ka - 1) / (bke * ka));
   prm.idesc = make_idesc(o.dtype, pl.pair ? 256 : 128, pl.bn, !b_kmajor);
-  prm.idesc_half = make_idesc(o.dtype, pl.pair ? 256 : 128, pl.bn / 2, !b_kmajor);
   prm.b_kmajor = b_kmajor ? 1u : 0u;
   prm.a3d = a3d ? 1u : 0u;
-  if (o.split_tail) {
-    if (!persistent || o.stream_k) return SWZ_EINVAL;
-    // a half tile of a 128-wide pair leaves each CTA 32 columns of B: less
-    // than one N-major box of the span
-    if (pl.pair && pl.bn == 128 && !b_kmajor) return SWZ_EUNSUPPORTED;
-    prm.split_tail = 1;
-  }
-  if (o.dynamic < 0 || o.dynamic > 2) return SWZ_EINVAL;
+  if (o.dynamic < 0 || o.dynamic > 1) return SWZ_EINVAL;
   if (o.dynamic) {
-    if (!persistent || o.stream_k || o.split_tail) return SWZ_EINVAL;
+    if (!persistent || o.stream_k) return SWZ_EINVAL;
     const uintptr_t ws = reinterpret_cast<uintptr_t>(o.d_workspace);
     if (!ws || (ws & 255u) || o.workspace_bytes < kDynWorkspaceBytes) return SWZ_EINVAL;
     if (span != 128) return SWZ_EUNSUPPORTED;
@@ -1480,10 +1393,6 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   if (o.dynamic) {
     // the counter of claimed work indices starts at zero in every launch
     prm.dyn_counter = static_cast<uint32_t*>(o.d_workspace);
-    // 1: each cluster's first work index by striding, then claims; 2: the
-    // full waves by striding, only the last, partial wave claimed
-    const uint32_t clusters = uint32_t(pl.programs) / (pl.pair ? (pl.mca ? 4u : 2u) : 1u);
-    prm.dyn_static = o.dynamic == 2 ? pl.units / clusters : 1u;
     SWZ_CUDA_TRY(cudaMemsetAsync(prm.dyn_counter, 0, sizeof(uint32_t), s));
     return dispatch<128, true>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
   }

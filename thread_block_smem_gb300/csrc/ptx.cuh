@@ -133,19 +133,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// Same, multicast: the box lands at offset `dst` of every CTA in `cta_mask`
-// (cluster ranks), and each destination's bytes are signalled on the barrier
-// at `bar`'s offset in the leader (even rank) of that destination's pair.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const CUtensorMap* map,
-                                                    uint32_t bar, int32_t x, int32_t y,
-                                                    uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
-
 // Untiled bulk copy of `bytes` (a multiple of 16) from global `src` to this
 // CTA's shared memory at `dst` (both 16-byte aligned), completing the bytes
 // on the barrier `bar` of this CTA.
