@@ -8,19 +8,28 @@ twice its size) before every timed step and the step is timed alone with CUDA
 events on the launching stream.
 
 Also reported on the same JSON line:
-  orders       TFLOP/s and % of peak of every order of the sweep
+  sweep        every order of the headline configuration: TFLOP/s, fraction
+               of the measured peak, the offline L2 model's hit rate and DRAM
+               bytes (the first page's model and the two-die reading), and
+               the ncu figures recorded for this kernel source
+  configs      the same sweep for the specification's other configurations:
+               1024x1024x512 fp16, 4096^3 fp16 (1-CTA 128 x 256 tiles,
+               persistent and one CTA per tile), 6144x10240x4096 fp16
+               (128 x 128 CTA tiles)
   roofline     the GEMM kernel against the measured bf16 tensor peak
   e2e          the same GEMM through the public API from pinned host buffers,
                host->device and device->host copies inside the timed region
   transpose    swz_transpose 16384 x 32768 (naive / padded / xor) in GB/s
   cpu_baseline the CPU oracle (FP64, all host cores) on a bounded row sample
-  clocks       nvidia-smi samples taken during the measurements
+  clocks       nvidia-smi samples taken over the timed headline steps and one
+               second more of the same steps (clocks_whole_run: the whole run)
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl swz|reference]
 """
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -67,36 +76,61 @@ WORKLOADS = {
 HEADLINE = dict(order="serpentine", group=8, persistent=True)
 SWEEP = WORKLOADS["gemm8192_bf16_pair"]["sweep"]
 
-# SHA-256 prefixes of the gemm.cu sources the ncu figures below hold for:
-# the one they were captured on, then sources that differ from it only in
-# host code of Stream-K launches, which the measured (static) launches do not
-# run: 4fa95a59d7bcf357 clears the Stream-K flags on the stream when a call
-# is recorded into a CUDA graph; 9a33811045633d4e also keeps every program
-# of a Stream-K launch that has fewer tiles than programs.
-NCU_SOURCES = ("32dfb91f838bdc4f", "4fa95a59d7bcf357", "9a33811045633d4e")
+# The other configurations of the specification, timed in the default run
+# beside the headline, each in a sub-object of the line: (key, workload,
+# launch modes) and the orders each names.
+_G = (2, 4, 8, 16)
+CONFIG_SWEEPS = [
+    ("cfg1_1024x1024x512_fp16", "gemm1024x1024x512_fp16", (True,)),
+    ("cfg2_4096_fp16_tile128x256", "gemm4096_fp16", (True, False)),
+    ("cfg4_6144x10240x4096_fp16_tile128x128", "gemm6144x10240x4096_fp16_pair", (True,)),
+]
+CONFIG_ORDERS = {
+    "cfg1_1024x1024x512_fp16": [("row", 1), ("col", 1), ("panel", 4), ("morton", 1),
+                                ("xor", 1), ("serpentine", 2)],
+    "cfg2_4096_fp16_tile128x256": ([("row", 1), ("col", 1)] + [("panel", g) for g in _G]
+                                   + [("serpentine", g) for g in _G]
+                                   + [("morton", 1), ("xor", 1)]),
+    "cfg4_6144x10240x4096_fp16_tile128x128": ([("row", 1), ("col", 1)]
+                                              + [("panel", g) for g in (4, 8, 16)]
+                                              + [("serpentine", g) for g in (4, 8, 16)]),
+}
 
-# DRAM traffic of one launch of the headline GEMM from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum); valid only for the kernel
-# sources whose SHA-256 prefixes are recorded with it.
-TRAFFIC = {"bytes": 1307546112, "gemm_cu_sha256": NCU_SOURCES,
-           "workload": "gemm8192_bf16_pair", "profile": "profiles/gemm_8192_bf16_pair_ncu.md"}
+# ncu figures of the GEMM kernel, per workload: one cold launch per order
+# (`--only sweep`: the L2 hit rate lts__t_sector_hit_rate.pct and
+# dram__bytes_read.sum) and the DRAM traffic (read + write) of the headline
+# launch.  They are counters of a capture, not of this run, and hold only
+# for the gemm.cu source they were taken on (SHA-256 prefix); for any
+# other source they are left out of the line.
+NCU = {
+    "gemm8192_bf16_pair": {
+        "source": {"gemm_cu_sha256": "32dfb91f838bdc4f", "captured": "2026-12-02",
+                   "kernel": "gemm_kernel<256, 1, 0, 128, 0>",
+                   "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum,"
+                              "dram__bytes_write.sum --clock-control none -k regex:gemm_kernel "
+                              "python bench.py --only sweep --no-cpu"},
+        "traffic_bytes": 1307546112, "traffic_order": ("serpentine", 8),
+        "orders": {("row", 1): (62.56, 2054057728), ("col", 1): (61.44, 2054787840),
+                   ("panel", 4): (70.64, 1418204672), ("panel", 8): (71.18, 1098593024),
+                   ("panel", 16): (66.87, 1300169216), ("serpentine", 4): (70.25, 1277612288),
+                   ("serpentine", 8): (72.44, 1059105536),
+                   ("serpentine", 16): (69.65, 1270239744), ("morton", 1): (69.53, 1364993024),
+                   ("xor", 1): (63.88, 2055510528)}},
+}
 
 
-# L2 hit rate (lts__t_sector_hit_rate.pct) of one cold launch per order from
-# an ncu capture of `bench.py --only sweep`; valid for the recorded kernel
-# source only.
-L2_NCU = {"gemm_cu_sha256": NCU_SOURCES, "profile": "profiles/gemm_8192_bf16_orders_l2.md",
-          ("row", 1): 62.56, ("col", 1): 61.44, ("panel", 4): 70.64, ("panel", 8): 71.18,
-          ("panel", 16): 66.87, ("serpentine", 4): 70.25, ("serpentine", 8): 72.44,
-          ("serpentine", 16): 69.65, ("morton", 1): 69.53, ("xor", 1): 63.88}
+def _gemm_src_hash():
+    with open(os.path.join(ROOT, "thread_block_smem_gb300", "csrc", "gemm.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-# dram__bytes_read.sum of the same captures (one cold launch per order)
-L2_NCU_DRAM = {("row", 1): 2054057728, ("col", 1): 2054787840, ("panel", 4): 1418204672,
-               ("panel", 8): 1098593024, ("panel", 16): 1300169216,
-               ("serpentine", 4): 1277612288, ("serpentine", 8): 1059105536,
-               ("serpentine", 16): 1270239744, ("morton", 1): 1364993024,
-               ("xor", 1): 2055510528}
+def ncu_record(workload):
+    """The recorded ncu figures of `workload` if they were taken on the
+    current gemm.cu source, else None."""
+    rec = NCU.get(workload)
+    if rec is None or rec["source"]["gemm_cu_sha256"] != _gemm_src_hash():
+        return None
+    return rec
 
 
 def resolve_workload(args):
@@ -124,11 +158,6 @@ def resolve_workload(args):
     return wl
 
 
-def _gemm_src_hash():
-    with open(os.path.join(ROOT, "thread_block_smem_gb300", "csrc", "gemm.cu"), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
-
-
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -139,20 +168,28 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons while running."""
-    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clock, utilisation and throttle reasons while
+    running; mark(tag) labels the samples taken from then on (None: no
+    label), so that a summary can cover one phase of the run."""
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+         "clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
         self.proc = None
+        self.marks = []  # (time, tag)
+        self.rows = []
+
+    def mark(self, tag):
+        self.marks.append((time.time(), tag))
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -165,34 +202,44 @@ class ClockSampler:
         time.sleep(0.25)
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) >= 8:
-                self.rows.append(f)
+        rows = [[x.strip() for x in line.split(",")] for line in out.strip().splitlines()]
+        for r in rows:
+            if len(r) < 10:
+                continue
+            try:  # the sample's local wall time
+                t = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            r = r[1:]
+            tag = None
+            for tm, tg in self.marks:
+                if tm <= t:
+                    tag = tg
+            self.rows.append((tag, r))
 
-    def summary(self):
-        if not getattr(self, "rows", None):
+    def summary(self, *tags):
+        """Median SM clock over the samples of the phases `tags` (all samples
+        when none is given) taken while the GPU was busy (utilisation >= 50
+        %), the maximum clock and every throttle reason seen active."""
+        rows = [r for tg, r in self.rows if not tags or tg in tags]
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
         def num(x):
             try:
                 return float(x)
             except ValueError:
                 return None
-        sm = [num(r[0]) for r in self.rows if num(r[0])]
-        pw = [num(r[2]) for r in self.rows if num(r[2])]
-        # samples under load: power above the midpoint of the observed range
-        if pw:
-            cut = (min(pw) + max(pw)) / 2
-            loaded = [num(r[0]) for r in self.rows if num(r[2]) and num(r[2]) >= cut and num(r[0])]
-        else:
-            loaded = sm
+        busy = [r for r in rows if (num(r[3]) or 0) >= 50]
+        sm = [num(r[0]) for r in (busy or rows) if num(r[0])]
+        pw = [num(r[2]) for r in rows if num(r[2])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in self.rows for i in range(4)
-                          if r[4 + i].lower().startswith("active")})
-        return {"sm_mhz": statistics.median(loaded or sm) if (loaded or sm) else None,
-                "sm_max_mhz": max(num(r[1]) or 0 for r in self.rows),
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(num(r[1]) or 0 for r in rows),
                 "power_w_max": max(pw) if pw else None,
-                "reasons": reasons, "samples": len(self.rows)}
+                "reasons": reasons, "samples": len(rows), "samples_busy": len(busy)}
 
 
 def spearman(xs, ys):
@@ -352,17 +399,87 @@ def run_swz(args):
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in ev]
 
+    def model(order, g, w, conc, parts):
+        """The offline L2 model at the kernel's tiling: hit % and DRAM bytes."""
+        tk = 128 if w["tile"][1] == 128 else 64  # K per stage: two atoms for 128-wide tiles
+        return swz.l2_model_predict(order, g, w["M"], w["N"], w["K"], w["tile"][0], w["tile"][1],
+                                    tk, 2, model_l2, conc, w["cluster_m"], l2_partitions=parts)
+
+    model_l2 = int(args.l2_cache_mb * 2**20) if args.l2_cache_mb else l2_bytes
+
+    def sweep(name, w, persist, steps, warmup):
+        """Every order of workload `w`: median TFLOP/s of L2-flushed launches,
+        fraction of the measured peak, the L2 model (the first page's, and the
+        two-die reading) and, where recorded for this kernel source, ncu."""
+        wM, wN, wK = w["M"], w["N"], w["K"]
+        wf = 2.0 * wM * wN * wK
+        wA, wB = si.gemm_inputs(wM, wN, wK, w["dtype"], w["dist"], seed=0)
+        wA, wB = wA.to(dev), wB.to(dev)
+        wC = torch.empty((wM, wN), dtype=torch.float32, device=dev)
+        wcfg = dict(w["cfg"])
+        _, (_, _, _, _, progs) = swz.swz_gemm_plan(wM, wN, wK, int(persist), swz.make_opts(**wcfg))
+        # the model's wave: resident CTAs (the first page's min(tiles, capacity)),
+        # unless overridden (its --num-sms)
+        conc = args.num_sms if args.num_sms else progs
+        rec = ncu_record(name) if persist else None
+        out = []
+        for order, g in w["sweep"]:
+            fn = lambda: swz.gemm(wA, wB, order, g, persist, out=wC, **wcfg)
+            try:
+                t = timed(fn, steps, warmup)
+            except swz.SwzError as e:  # Morton / XOR on a grid they do not permute
+                out.append({"order": order, "group": g, "error": swz.strerror(e.code)})
+                continue
+            med = statistics.median(t)
+            hit, dram = model(order, g, w, conc, 1)
+            hit2, dram2 = model(order, g, w, conc, 2)
+            o = {"order": order, "group": g, "ms": med, "tflops": wf / med / 1e9,
+                 "frac_of_peak": wf / med / 1e9 / peaks["bf16_tflops"],
+                 "l2_model_hit_pct": hit, "l2_model_dram_read_bytes": dram,
+                 "l2_model_2die_hit_pct": hit2, "l2_model_2die_dram_read_bytes": dram2}
+            if rec and (order, g) in rec["orders"]:
+                nh, nd = rec["orders"][(order, g)]
+                o.update({"ncu_l2_hit_pct": nh, "ncu_dram_read_bytes": nd,
+                          "l2_model_2die_dram_err": (dram2 - nd) / nd})
+            out.append(o)
+        del wA, wB, wC
+        res = {"shape": [wM, wN, wK], "dtype": w["dtype"], "cfg": wcfg,
+               "persistent": persist, "programs": progs, "orders": out,
+               "model": {"l2_bytes": model_l2, "concurrency_ctas": conc}}
+        good = [o for o in out if "tflops" in o]
+        if len(good) > 1:
+            res["spearman_l2_model_vs_tflops"] = spearman(
+                [o["l2_model_hit_pct"] for o in good], [o["tflops"] for o in good])
+        meas = [o for o in good if "ncu_dram_read_bytes" in o]
+        if len(meas) > 1:
+            res["ncu_source"] = rec["source"]
+            res["spearman_model_dram_vs_ncu_dram"] = {
+                "full_l2": spearman([o["l2_model_dram_read_bytes"] for o in meas],
+                                    [o["ncu_dram_read_bytes"] for o in meas]),
+                "two_die": spearman([o["l2_model_2die_dram_read_bytes"] for o in meas],
+                                    [o["ncu_dram_read_bytes"] for o in meas])}
+            res["l2_model_2die_dram_abs_err_max"] = max(abs(o["l2_model_2die_dram_err"])
+                                                        for o in meas)
+        return res
+
     sampler = ClockSampler(local)
     ms = None
-    orders = []
     with sampler:
         if args.only in ("all", "gemm"):
             # ---- headline: K timed steps ------------------------------
             if world > 1:
                 tdist.barrier()
             torch.cuda.synchronize()
+            sampler.mark("timed")
             ms = timed(lambda: gemm_once(head_order, head_group), args.steps, args.warmup)
             torch.cuda.synchronize()
+            # the same steps again, untimed, for about a second: nvidia-smi
+            # samples every 50 ms, too coarse for the timed steps alone
+            sampler.mark("window")
+            t_end = time.time() + 1.0
+            while time.time() < t_end:
+                timed(lambda: gemm_once(head_order, head_group), 20, 0)
+            sampler.mark(None)
             if world > 1:
                 tdist.barrier()
         if args.only == "sweep":
@@ -371,48 +488,22 @@ def run_swz(args):
                 gemm_once(order, g)
             torch.cuda.synchronize()
             for order, g in wl["sweep"]:
-                t = timed(lambda: gemm_once(order, g), 1, 0)
-                orders.append({"order": order, "group": g, "ms": t[0]})
+                timed(lambda: gemm_once(order, g), 1, 0)
         elif args.only == "all" and not args.no_sweep:
-            for order, g in wl["sweep"]:
-                try:
-                    t = timed(lambda: gemm_once(order, g), max(5, args.steps // 4), 3)
-                except swz.SwzError as e:  # Morton / XOR on a grid they do not permute
-                    orders.append({"order": order, "group": g, "error": swz.strerror(e.code)})
-                    continue
-                med = statistics.median(t)
-                # the model at the kernel's tiling: K steps of 64 elements
-                # (two 128-byte atoms, 128 elements, for 128-wide tiles)
-                tk = wl.get("tk", 128 if wl["tile"][1] == 128 else 64)
-                # model parameters: the device's L2 and resident programs,
-                # unless overridden (the first page's --l2-cache-mb, --num-sms)
-                model_l2 = int(args.l2_cache_mb * 2**20) if args.l2_cache_mb else l2_bytes
-                model_conc = ((args.num_sms if args.num_sms else programs)  # CTAs in a wave
-                              // wl.get("conc_div", 1))
-                pred, pred_bytes = swz.l2_model_predict(order, g, M, N, K, wl["tile"][0],
-                                                        wl["tile"][1], tk, 2, model_l2,
-                                                        model_conc, wl["cluster_m"])
-                # the same model fed half the L2: GB300's L2 is two halves,
-                # one per die, and operand lines that SMs of both dies read
-                # can take room in both
-                pred_h, pred_h_bytes = swz.l2_model_predict(order, g, M, N, K, wl["tile"][0],
-                                                            wl["tile"][1], tk, 2, model_l2 // 2,
-                                                            model_conc, wl["cluster_m"])
-                ncu_ok = (_gemm_src_hash() in L2_NCU.get("gemm_cu_sha256", ())
-                          and args.workload == "gemm8192_bf16_pair" and persistent
-                          and not args.stream_k)
-                line["l2_model"] = {"l2_bytes": model_l2, "concurrency_ctas": model_conc,
-                                    "tile": [wl["tile"][0], wl["tile"][1], tk]}
-                orders.append({"order": order, "group": g, "ms": med,
-                               "tflops": flops / med / 1e9,
-                               "pct_peak": 100.0 * flops / med / 1e9 / peaks["bf16_tflops"],
-                               "l2_model_hit_pct": pred,
-                               "l2_model_dram_read_bytes": pred_bytes,
-                               "l2_model_half_hit_pct": pred_h,
-                               "l2_model_half_dram_read_bytes": pred_h_bytes,
-                               "l2_ncu_hit_pct": L2_NCU.get((order, g)) if ncu_ok else None,
-                               "dram_read_ncu_bytes": L2_NCU_DRAM.get((order, g))
-                               if ncu_ok else None})
+            line["sweep"] = sweep(args.workload, wl, persistent, max(5, args.steps // 4), 3)
+            # the other configurations of the specification, each in its own
+            # sub-object (order sweeps; the 4096^3 one also non-persistent)
+            if not args.no_configs:
+                cf = {}
+                for key, wname, modes in CONFIG_SWEEPS:
+                    if wname == args.workload:
+                        continue
+                    w = resolve_workload(argparse.Namespace(**{**vars(args), "workload": wname,
+                                                               "m": 0, "n": 0, "k": 0}))
+                    w["sweep"] = CONFIG_ORDERS[key]
+                    cf[key] = {("persistent" if p else "non_persistent"): sweep(wname, w, p, 5, 3)
+                               for p in modes}
+                line["configs"] = cf
         # ---- operand-stage swizzle span (TMA + tensor-core layout) ---------
         spans = []
         if args.only == "swizzle":  # one cold launch per span, for counter capture
@@ -434,7 +525,13 @@ def run_swz(args):
                 t = timed(fn, max(5, args.steps // 4), 3)
                 sched[name] = {"ms": statistics.median(t),
                                "tflops": flops / statistics.median(t) / 1e9}
-    clocks = sampler.summary()
+    # the clock of the headline: samples of the timed steps and of the
+    # second of the same steps after them; under sustained dense load the
+    # power cap (sw_power_cap) takes the clock down from its maximum within
+    # that second, so the median is a lower bound of the timed steps' clock
+    clocks = sampler.summary("timed", "window")
+    clocks["timed_steps"] = sampler.summary("timed")
+    clocks_all = sampler.summary()
     if spans:
         line["smem_swizzle_spans"] = spans
     if sched:
@@ -444,10 +541,9 @@ def run_swz(args):
         ms_step = max_over_ranks(statistics.mean(ms), dev)
         achieved = flops / statistics.mean(ms) / 1e9
         # the captured launch is the default workload's headline launch only
-        traffic = (TRAFFIC["bytes"] if _gemm_src_hash() in TRAFFIC["gemm_cu_sha256"]
-                   and args.workload == TRAFFIC["workload"] and persistent
-                   and not args.stream_k and (head_order, head_group) == ("serpentine", 8)
-                   else None)
+        rec = ncu_record(args.workload)
+        traffic = (rec["traffic_bytes"] if rec and persistent and not args.stream_k
+                   and (head_order, head_group) == rec["traffic_order"] else None)
         line.update({
             "value": world * flops / ms_step / 1e9, "ms_per_step": ms_step,
             "config": {"workload": f"{args.workload}: gemm {M}x{N}x{K} {wl['dtype']} "
@@ -464,24 +560,13 @@ def run_swz(args):
                        "device": {"sms": sms, "l2_bytes": l2_bytes, "cc": f"{ccmaj}.{ccmin}"}},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                         "traffic": traffic, "peak_source": f"bf16 burst, of {peak_src}"},
+                         "traffic": traffic,
+                         "traffic_source": rec["source"] if traffic is not None else None,
+                         "peak_source": f"bf16 burst, of {peak_src}"},
             "gpu_launches": args.steps,
         })
     line["clocks"] = clocks
-    if orders:
-        line["orders"] = orders
-        good = [o for o in orders if "tflops" in o]
-        if len(good) > 1:
-            line["spearman_l2_model_vs_tflops"] = spearman(
-                [o["l2_model_hit_pct"] for o in good], [o["tflops"] for o in good])
-        # predicted against measured DRAM reads, where the capture is for this source
-        meas = [o for o in orders if o.get("dram_read_ncu_bytes")]
-        if len(meas) > 1:
-            line["spearman_model_dram_vs_ncu_dram"] = {
-                "full_l2": spearman([o["l2_model_dram_read_bytes"] for o in meas],
-                                    [o["dram_read_ncu_bytes"] for o in meas]),
-                "half_l2": spearman([o["l2_model_half_dram_read_bytes"] for o in meas],
-                                    [o["dram_read_ncu_bytes"] for o in meas])}
+    line["clocks_whole_run"] = clocks_all
 
     # ---- end to end through the public API from pinned host buffers --------
     # swz_gemm_host: B in, then A in / GEMM / C out overlapped in row slabs;
@@ -655,11 +740,14 @@ def run_swz(args):
                                    b_transposed=True, cta_pair=True),
                   10 if args.only == "all" else 1, 3)
         med = statistics.median(t)
-        # the recipe's nominal dense ratio tf32 / bf16 = 1.1 / 2.25 PFLOP/s
-        peak_tf32 = peaks["bf16_tflops"] * 1.1 / 2.25
+        # the measured bf16 peak scaled by the TF32 / bf16 rate ratio of the
+        # library's own tcgen05 MMAs: 1/2 (4,095 vs 8,190 FLOP per clock per
+        # SM); replaced below by this run's ratio when tc_rate runs
+        peak_tf32 = peaks["bf16_tflops"] * 0.5
         line["tf32_8192"] = {"ms": med, "tflops": flops / med / 1e9,
                              "peak": peak_tf32, "frac": flops / med / 1e9 / peak_tf32,
-                             "peak_source": "measured bf16 x nominal 1.1/2.25"}
+                             "peak_source": "measured bf16 burst x the tcgen05 tf32/bf16 rate "
+                                            "ratio 1/2"}
         del A32, Bt32, C32
 
     # ---- tensor-core rate of the library's own tcgen05 code (swz_tc_rate) ----
@@ -720,8 +808,13 @@ def run_swz(args):
             tc["headline_frac_of_bf16_max_clock_peak"] = a / tc["bf16"]["peak_max_clock_tflops"]
             tc["headline_frac_of_bf16_loaded_peak"] = a / tc["bf16"]["peak_loaded_tflops"]
         if "tf32_8192" in line:
-            line["tf32_8192"]["frac_of_tf32_loaded_peak"] = (
-                line["tf32_8192"]["tflops"] / tc["tf32"]["peak_loaded_tflops"])
+            t32 = line["tf32_8192"]
+            ratio = tc["tf32"]["flop_per_clk_per_sm"] / tc["bf16"]["flop_per_clk_per_sm"]
+            t32["peak"] = peaks["bf16_tflops"] * ratio
+            t32["frac"] = t32["tflops"] / t32["peak"]
+            t32["peak_source"] = (f"measured bf16 burst x this run's tcgen05 tf32/bf16 rate "
+                                  f"ratio {ratio:.4f}")
+            t32["frac_of_tf32_loaded_peak"] = t32["tflops"] / tc["tf32"]["peak_loaded_tflops"]
         line["tc_rate"] = tc
 
     # ---- ldmatrix / mma.sync path: operand layout vs bank conflicts ---------
@@ -787,6 +880,8 @@ def main():
                     help="concurrent CTAs the offline model assumes, as SMs (default: the "
                          "launch's resident programs)")
     ap.add_argument("--no-dynamic", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations' order sweeps")
     ap.add_argument("--only", choices=["all", "gemm", "sweep", "transpose", "mma_sync",
                                        "tc_rate", "swizzle", "tf32", "cublas", "launch"],
                     default="all",

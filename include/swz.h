@@ -292,10 +292,16 @@ int swz_l2_model(int order, int group, int M, int N, int K, int tile_m, int tile
 /* swz_l2_model plus the bytes the misses bring in (each miss of an A tile
  * counts tile_m * tile_k * elem_bytes, of a B tile tile_k * tile_n *
  * elem_bytes): the model's prediction of the operand bytes read from DRAM.
- * Errors: SWZ_EINVAL (as swz_l2_model, or h_miss_bytes NULL). */
+ * l2_partitions = 1 is the [TBS] model.  l2_partitions = p > 1 models an L2
+ * split into p halves, one per die (GB300: 2), where every operand line is
+ * read by SMs of every die and each half keeps its own copy: each half
+ * replays the whole trace with l2_bytes / p of capacity, and the counts are
+ * those of one half.  This is a reading of the hardware, not the page's
+ * model.  Errors: SWZ_EINVAL (as swz_l2_model, l2_partitions < 1, or
+ * h_miss_bytes NULL). */
 int swz_l2_model_bytes(int order, int group, int M, int N, int K, int tile_m, int tile_n,
-                       int tile_k, int elem_bytes, int64_t l2_bytes, int concurrency,
-                       int cluster_m, int64_t* h_hits, int64_t* h_misses,
+                       int tile_k, int elem_bytes, int64_t l2_bytes, int l2_partitions,
+                       int concurrency, int cluster_m, int64_t* h_hits, int64_t* h_misses,
                        int64_t* h_miss_bytes);
 
 /*
@@ -310,7 +316,7 @@ int swz_l2_model_bytes(int order, int group, int M, int N, int K, int tile_m, in
  * it synchronises the device.  swz_gemm_ex with stream_k needs a
  * caller-provided workspace; this entry point instead uses a scratch area
  * built into the library: a statically sized device array of
- * SWZ_NOALLOC_SCRATCH_BYTES (24 MiB) that every GPU which loads the library
+ * SWZ_NOALLOC_SCRATCH_BYTES (40 MiB) that every GPU which loads the library
  * holds until the process exits.
  *
  * Computes exactly what swz_gemm_ex computes with persistent = 1, stream_k =
@@ -320,8 +326,10 @@ int swz_l2_model_bytes(int order, int group, int M, int N, int K, int tile_m, in
  *
  * Set-up: the first call on each device looks up the device address of the
  * scratch area (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture.  The call allocates and frees
- * nothing.  It clears the part of the scratch area that must start at zero
+ * first call before any stream capture.  The address is kept for the life of
+ * the process and does not survive cudaDeviceReset (or anything else that
+ * destroys the device's primary context): do not call this entry point on a
+ * device after resetting it.  The call allocates and frees nothing.  It clears the part of the scratch area that must start at zero
  * (the per-piece flags) on `stream` before the launch.
  *
  * All calls on a device share the one scratch area, which keeps the last
@@ -332,7 +340,7 @@ int swz_l2_model_bytes(int order, int group, int M, int N, int K, int tile_m, in
  * Errors: as swz_gemm_ex, plus SWZ_ESCRATCH when the launch needs more than
  * SWZ_NOALLOC_SCRATCH_BYTES of scratch (see swz_gemm_workspace_size).
  */
-#define SWZ_NOALLOC_SCRATCH_BYTES (24u * 1024u * 1024u)
+#define SWZ_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u)
 int swz_gemm_streamk_noalloc(const void* A, const void* B, float* C, int M, int N, int K,
                              int order, int group, const swz_gemm_opts* opts,
                              void* stream);

@@ -226,13 +226,14 @@ def stream_k_trace(order, gm, gn, group, num_programs, k_blocks, cluster_m=1):
     U - R units (R = U mod P) go out whole by work-index striding, as in
     persistent_trace.  The K blocks of the R tail units are laid end to
     end, I = R * k_blocks of them, and cluster c takes the contiguous range
-    [floor(I c / P), floor(I (c + 1) / P)).  A cluster's work items are its
-    whole units, then one item for each tail unit its range touches, in K
-    order.  A tail unit is finished (C written) by the cluster whose range
-    holds the unit's first K block.
+    [floor(I c / P), floor(I (c + 1) / P)).  A cluster's work items are
+    first one item for each tail unit its range touches, in K order, then
+    its whole units.  A tail unit is recorded for the cluster whose range
+    holds the unit's first K block, at that cluster's item for the unit.
 
-    Returns {(cta_m, cta_n): (program, item index)} over all CTA tiles, the
-    program and item that write each tile.
+    Returns {(cta_m, cta_n): (program, item index)} over all CTA tiles: the
+    program and item that write each whole tile, and for a tail tile the
+    program and item holding its first K block.
     """
     if gm % cluster_m:
         raise ValueError("the cluster shape must divide the CTA-tile grid")
@@ -251,18 +252,20 @@ def stream_k_trace(order, gm, gn, group, num_programs, k_blocks, cluster_m=1):
                 raise AssertionError(f"tile {key} written twice")
             trace[key] = (c * cluster_m + r, item)
 
-    for w in range(full):
-        put(w, w % P, w // P)
     I = R * k_blocks
+    pieces = []  # tail units each cluster's range touches
     for c in range(P):
         s, e = I * c // P, I * (c + 1) // P
-        item = len(range(c, full, P))
+        touched = []
         t = s // k_blocks
         while s < e and t * k_blocks < e:
             if t * k_blocks >= s:
-                put(full + t, c, item)
-            item += 1
+                put(full + t, c, len(touched))
+            touched.append(t)
             t += 1
+        pieces.append(len(touched))
+    for w in range(full):
+        put(w, w % P, pieces[w % P] + w // P)
     return trace
 
 

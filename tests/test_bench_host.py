@@ -106,3 +106,54 @@ def test_workloads_and_capture_modes():
     for mode in ("gemm", "sweep", "swizzle", "transpose", "mma_sync", "tc_rate", "tf32",
                  "cublas", "launch"):
         assert f'"{mode}"' in src
+
+
+def test_clock_sampler_summarises_one_phase():
+    # nvidia-smi rows are placed by their own timestamps; only the samples of
+    # the marked phase taken while the GPU was busy set the median clock
+    import datetime
+
+    def stamp(t):
+        return datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+
+    t0 = 1_800_000_000.0
+    rows = [(t0 + 0.1, 2070, 0, "Not Active"), (t0 + 1.1, 1950, 100, "Active"),
+            (t0 + 1.2, 1930, 100, "Active"), (t0 + 1.3, 2070, 10, "Not Active"),
+            (t0 + 2.5, 1800, 100, "Not Active")]
+    text = "\n".join(f"{stamp(t)}, {mhz}, 2070, 900.0, {util}, 0x0, Not Active, Not Active, "
+                     f"Not Active, {cap}" for t, mhz, util, cap in rows)
+
+    class FakeProc:
+        def terminate(self):
+            pass
+
+        def communicate(self, timeout=None):
+            return text, ""
+
+    s = bench.ClockSampler(0)
+    s.proc = FakeProc()
+    s.marks = [(t0 + 1.0, "headline"), (t0 + 2.0, None)]
+    s.__exit__(None, None, None)
+    h = s.summary("headline")
+    assert s.summary("headline", None)["samples"] == 5
+    assert h["samples"] == 3 and h["samples_busy"] == 2
+    assert h["sm_mhz"] == 1940 and h["reasons"] == ["sw_power_cap"]
+    assert s.summary()["samples"] == 5
+
+
+def test_config_sweeps_cover_the_specification():
+    # every configuration of the specification other than the headline is in
+    # the default line, with the orders it names
+    keys = {k for k, _, _ in bench.CONFIG_SWEEPS}
+    assert keys == set(bench.CONFIG_ORDERS)
+    for key, wname, modes in bench.CONFIG_SWEEPS:
+        assert wname in bench.WORKLOADS
+    o2 = bench.CONFIG_ORDERS["cfg2_4096_fp16_tile128x256"]
+    assert {g for o, g in o2 if o == "panel"} == {2, 4, 8, 16}
+    assert {g for o, g in o2 if o == "serpentine"} == {2, 4, 8, 16}
+    assert ("morton", 1) in o2 and ("xor", 1) in o2
+    o4 = bench.CONFIG_ORDERS["cfg4_6144x10240x4096_fp16_tile128x128"]
+    assert not {o for o, _ in o4} & {"morton", "xor"}  # not bijective on 48 x 80
+    assert len(bench.CONFIG_ORDERS["cfg1_1024x1024x512_fp16"]) == 6
+    assert dict((k, m) for k, _, m in bench.CONFIG_SWEEPS)["cfg2_4096_fp16_tile128x256"] == (
+        True, False)

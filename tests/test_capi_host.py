@@ -87,10 +87,10 @@ def test_stream_k_plan_keeps_every_program(swz):
         rc, plan = swz.swz_gemm_plan(256, 256, 1 << 20, 1, o)
         assert rc == swz.SWZ_OK and plan[4] == 152
         rc, n = swz.swz_gemm_workspace_size(256, 256, 1 << 20, 1, o)
-        # flags of 152 CTAs (4 words each, 256-byte aligned) + one 128 x tile_n
-        # FP32 partial per CTA
+        # two slots per CTA: flags (4 words each, 256-byte aligned) and one
+        # 128 x tile_n FP32 partial each
         tn = 256 if cfg.get("cta_pair") else 128
-        assert rc == swz.SWZ_OK and n == 2560 + 152 * 128 * tn * 4
+        assert rc == swz.SWZ_OK and n == 4864 + 2 * 152 * 128 * tn * 4
     # the same through the Python helper
     assert swz.gemm_plan(256, 256, 1 << 20, True, cta_pair=True, num_programs=152) == (
         2, 1, 1, 1, 2)

@@ -50,6 +50,18 @@ def test_native_model_matches_oracle(swz, case):
     assert rc == 0 and (h2, m2, b) == want
 
 
+@pytest.mark.parametrize("parts", [2, 3])
+@pytest.mark.parametrize("case", CASES[2:6])
+def test_partitioned_model_is_the_oracle_at_a_fraction_of_the_capacity(swz, case, parts):
+    # the two-die reading: each of `parts` halves replays the whole trace with
+    # 1/parts of the capacity (integer division of the byte budget)
+    rc, h, m, b = swz.swz_l2_model_bytes(*case, l2_partitions=parts)
+    assert rc == 0
+    c = list(case)
+    c[9] = case[9] // parts
+    assert (h, m, b) == _oracle_counts(*c)
+
+
 @pytest.mark.slow
 def test_native_model_reproduces_printed_rates(swz):
     rows = [ln for ln in read_lines("tbs_l2_model_8192.txt") if ln[0] not in ("config", "spearman")]
@@ -64,7 +76,8 @@ def test_native_miss_bytes_compulsory(swz):
     # a cache larger than every operand tile together: each tile is read once
     M, N, K, tm, tn, tk = 1000, 1200, 300, 128, 256, 64
     gm, gn, gk = math.ceil(M / tm), math.ceil(N / tn), math.ceil(K / tk)
-    rc, h, m, b = swz.swz_l2_model_bytes(to.SERPENTINE, 2, M, N, K, tm, tn, tk, 2, 1 << 40, 7, 1)
+    rc, h, m, b = swz.swz_l2_model_bytes(to.SERPENTINE, 2, M, N, K, tm, tn, tk, 2, 1 << 40, 7, 1,
+                                         l2_partitions=2)
     assert rc == 0 and m == gm * gk + gk * gn
     assert b == gm * gk * tm * tk * 2 + gk * gn * tk * tn * 2
 
@@ -73,3 +86,5 @@ def test_native_model_rejects_bad_args(swz):
     assert swz.swz_l2_model(9, 1, 64, 64, 64, 16, 16, 16, 2, 1024, 4, 1)[0] == swz.SWZ_EINVAL
     assert swz.swz_l2_model(to.PANEL, 0, 64, 64, 64, 16, 16, 16, 2, 1024, 4, 1)[0] == swz.SWZ_EINVAL
     assert swz.swz_l2_model(to.ROW, 1, 64, 64, 64, 16, 16, 16, 2, 1024, 0, 1)[0] == swz.SWZ_EINVAL
+    assert swz.swz_l2_model_bytes(to.ROW, 1, 64, 64, 64, 16, 16, 16, 2, 1024, 4, 1,
+                                  l2_partitions=0)[0] == swz.SWZ_EINVAL

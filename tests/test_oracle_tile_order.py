@@ -196,6 +196,24 @@ def test_stream_k_trace_hand_example():
         to.stream_k_trace(to.ROW, 3, 3, 1, 8, 4, cluster_m=2)
 
 
+def test_stream_k_trace_hand_example_with_whole_units():
+    # 1 x 5 tiles in row order, 3 clusters, 2 K blocks a tile.  Units 0-2 go
+    # out whole (one per cluster); units 3 and 4 are the tail: I = 4 blocks,
+    # ranges [0,1) [1,2) [2,4).  The tail pieces come first: cluster 0 holds
+    # block 0, the head of unit 3 (its item 0), cluster 1 block 1 (the end of
+    # unit 3), cluster 2 blocks 2-3, all of unit 4 (its item 0); each
+    # cluster's whole unit is its item 1.
+    assert to.stream_k_ranges(3, 2, 2) == [(0, 1), (1, 2), (2, 4)]
+    assert to.stream_k_trace(to.ROW, 1, 5, 1, 3, 2) == {
+        (0, 0): (0, 1), (0, 1): (1, 1), (0, 2): (2, 1), (0, 3): (0, 0), (0, 4): (2, 0)}
+    # 1 x 4 tiles, 3 clusters, 1 K block a tile: one tail unit, I = 1 block,
+    # ranges [0,0) [0,0) [0,1): clusters 0 and 1 have no tail piece, so their
+    # whole units are their items 0; cluster 2 takes the tail unit first
+    assert to.stream_k_ranges(3, 1, 1) == [(0, 0), (0, 0), (0, 1)]
+    assert to.stream_k_trace(to.ROW, 1, 4, 1, 3, 1) == {
+        (0, 0): (0, 0), (0, 1): (1, 0), (0, 2): (2, 1), (0, 3): (2, 0)}
+
+
 @pytest.mark.parametrize("gm,gn,P,kb,cm", [(6, 5, 6, 4, 1), (6, 5, 7, 16, 1), (6, 5, 7, 3, 1),
                                            (6, 5, 40, 3, 1), (2, 1, 152, 16384, 2),
                                            (6, 5, 8, 9, 2), (10, 4, 6, 7, 2)])
@@ -208,16 +226,18 @@ def test_stream_k_trace_against_brute_force(gm, gn, P, kb, cm):
     if R == 0:
         assert tr == to.persistent_trace(order, gm, gn, g, P, cluster_m=cm)
         return
-    # whole units: as the static schedule
-    seq = to.tile_sequence(order, gm // cm, gn, g)
-    for w in range(U - R):
-        m, n = seq[w]
-        for r in range(cm):
-            assert tr[(m * cm + r, n)] == ((w % clusters) * cm + r, w // clusters)
     # the tail, block by block: owner of block b = the cluster whose range
     # holds it; ranges are contiguous, cover [0, R * kb) once and differ in
     # length by at most one block
     ranges = to.stream_k_ranges(clusters, R, kb)
+    # whole units: as the static schedule, after the cluster's tail pieces
+    seq = to.tile_sequence(order, gm // cm, gn, g)
+    for w in range(U - R):
+        m, n = seq[w]
+        c = w % clusters
+        npieces = len({b // kb for b in range(*ranges[c])})
+        for r in range(cm):
+            assert tr[(m * cm + r, n)] == (c * cm + r, npieces + w // clusters)
     assert ranges[0][0] == 0 and ranges[-1][1] == R * kb
     assert all(a[1] == b[0] for a, b in zip(ranges, ranges[1:]))
     assert max(e - s for s, e in ranges) - min(e - s for s, e in ranges) <= 1
@@ -227,10 +247,9 @@ def test_stream_k_trace_against_brute_force(gm, gn, P, kb, cm):
             holder[b] = c
     for t in range(R):
         c = holder[t * kb]
-        # the items of cluster c before this one: its whole units, then one
-        # per earlier tail unit its range touches
-        whole = len(range(c, U - R, clusters))
+        # the items of cluster c before this one: one per earlier tail unit
+        # its range touches
         earlier = len({b // kb for b in range(*ranges[c]) if b // kb < t})
         m, n = seq[U - R + t]
         for r in range(cm):
-            assert tr[(m * cm + r, n)] == (c * cm + r, whole + earlier)
+            assert tr[(m * cm + r, n)] == (c * cm + r, earlier)

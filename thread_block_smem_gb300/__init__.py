@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libswz.so")
 SWZ_OK, SWZ_EINVAL, SWZ_ENOTBIJECTIVE, SWZ_EARCH, SWZ_ECUDA, SWZ_ETIMEOUT, SWZ_EUNSUPPORTED = (
     0, -1, -2, -3, -4, -5, -6)
 SWZ_ESCRATCH = -7
-SWZ_NOALLOC_SCRATCH_BYTES = 24 * 1024 * 1024
+SWZ_NOALLOC_SCRATCH_BYTES = 40 * 1024 * 1024
 SWZ_ROW, SWZ_COL, SWZ_PANEL, SWZ_MORTON, SWZ_XOR, SWZ_SERPENTINE = range(6)
 SWZ_F16, SWZ_BF16, SWZ_TF32 = 0, 1, 2
 SWZ_B_KN, SWZ_B_NK = 0, 1
@@ -82,8 +82,8 @@ def lib() -> ctypes.CDLL:
         L.swz_device_info.argtypes = [ip, ip, ip, ip]
         i64p = ctypes.POINTER(ctypes.c_int64)
         L.swz_l2_model.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.c_int64, i, i, i64p, i64p]
-        L.swz_l2_model_bytes.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.c_int64, i, i, i64p,
-                                         i64p, i64p]
+        L.swz_l2_model_bytes.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.c_int64, i, i, i,
+                                         i64p, i64p, i64p]
         L.swz_gemm_workspace_size.argtypes = [i, i, i, i, ctypes.POINTER(swz_gemm_opts),
                                               ctypes.POINTER(ctypes.c_uint64)]
         L.swz_gemm_streamk_noalloc.argtypes = [vp, vp, vp, i, i, i, i, i,
@@ -246,19 +246,22 @@ def swz_l2_model(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_b
 
 
 def swz_l2_model_bytes(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_bytes,
-                       concurrency, cluster_m=1):
+                       concurrency, cluster_m=1, l2_partitions=1):
     h, m, b = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
     rc = lib().swz_l2_model_bytes(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes,
-                                  l2_bytes, concurrency, cluster_m, ctypes.byref(h),
-                                  ctypes.byref(m), ctypes.byref(b))
+                                  l2_bytes, l2_partitions, concurrency, cluster_m,
+                                  ctypes.byref(h), ctypes.byref(m), ctypes.byref(b))
     return rc, h.value, m.value, b.value
 
 
 def l2_model_predict(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_bytes,
-                     concurrency, cluster_m=1):
-    """(predicted L2 hit rate in percent, predicted operand DRAM bytes)."""
+                     concurrency, cluster_m=1, l2_partitions=1):
+    """(predicted L2 hit rate in percent, predicted operand DRAM bytes);
+    ``l2_partitions`` = 2 is the two-die reading (each half of the L2 keeps
+    its own copy of the whole trace), 1 the first page's model."""
     rc, h, m, b = swz_l2_model_bytes(_order(order), group, M, N, K, tile_m, tile_n, tile_k,
-                                     elem_bytes, l2_bytes, concurrency, cluster_m)
+                                     elem_bytes, l2_bytes, concurrency, cluster_m,
+                                     l2_partitions)
     _check(rc, "swz_l2_model_bytes")
     return (100.0 * h / (h + m) if h + m else 0.0), b
 

@@ -43,6 +43,12 @@ bool order_is_bijective(int order, uint32_t gm, uint32_t gn, uint32_t group);
 int gemm_sk_workspace_split(int M, int N, int K, int persistent, const swz_gemm_opts& o,
                             uint64_t* flag_bytes, uint64_t* total_bytes);
 
+// swz_gemm_ex; with clear_sk_flags a Stream-K launch clears its piece flags
+// on the stream before it starts (always, not only under stream capture),
+// after every argument check has passed.
+int gemm_ex(const void* A, const void* B, float* C, int M, int N, int K, int order, int group,
+            int persistent, const swz_gemm_opts* opts, void* stream, bool clear_sk_flags);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 

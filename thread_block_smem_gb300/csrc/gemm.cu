@@ -150,13 +150,15 @@ enum ItemKind : int { kWhole = 0, kFirst = 1, kPartial = 2 };
 // tail units are laid end to end (R*kb iterations) and split into P
 // contiguous ranges, one per cluster, so the last wave is shared by every
 // cluster instead of running on R of them.  A range is shorter than one tile
-// (R < P), so it holds at most two pieces: a piece that starts inside a tile
-// (a partial, written to the workspace) and a piece that starts a tile (its
-// first piece: the cluster owning it adds the other pieces and writes C).
+// (R < P), so it holds at most two pieces: one in the tile where it starts
+// and the head of the next tile.  The pieces of a tile are added in K order
+// and the sum written to C by the tile's participants together, each taking
+// a share of its chunks (the epilogue).
 struct Schedule {
   uint32_t c, P, U, kb;
-  uint32_t dp_end;  // units below this are whole tiles
-  uint32_t n_dp;    // whole tiles of this cluster
+  uint32_t dp_end;    // units below this are whole tiles
+  uint32_t n_dp;      // whole tiles of this cluster
+  uint32_t n_pieces;  // tail tiles this cluster's range touches (0, 1 or 2)
   uint64_t I;       // Stream-K tail iterations
   uint64_t s, e;    // this cluster's Stream-K tail range [s, e)
   uint64_t Iq;      // I / P and I % P: range starts are stepped from one
@@ -174,6 +176,7 @@ struct Schedule {
     I = sk ? uint64_t(R) * kb : 0u;
     s = range_start(c);
     e = range_start(c + 1);
+    n_pieces = s < e ? uint32_t((e - 1) / kb - s / kb + 1) : 0u;
     Iq = I / P;
     Ir = uint32_t(I % P);
   }
@@ -197,27 +200,75 @@ struct Schedule {
     }
     ++k.cc;
   }
-  // The i-th piece of work: unit, K-block range [k0, k1) and kind.
+  // Participants of tail tile t (the clusters whose non-empty ranges meet
+  // its K blocks [t*kb, (t+1)*kb)), walked in K order with a cursor:
+  // first_part(t) is the cluster holding the tile's first block, and
+  // next_part moves to the next cluster with a non-empty range starting
+  // before `end` (cc = P when there is none).  A participant's piece of the
+  // tile sits in its workspace slot 1 when its range started in an earlier
+  // tile (the piece is the head of t), else in slot 0.
+  __device__ __forceinline__ uint32_t holder(uint64_t x) const {
+    return uint32_t(((x + 1) * P - 1) / I);  // largest cc with range_start(cc) <= x
+  }
+  __device__ __forceinline__ Cursor first_part(uint32_t t) const {
+    return cursor(holder(uint64_t(t) * kb));
+  }
+  __device__ __forceinline__ void next_part(Cursor& k, uint64_t end) const {
+    for (;;) {
+      step(k);
+      if (k.cc >= P || k.s >= end) {
+        k.cc = P;
+        return;
+      }
+      Cursor kn = k;
+      step(kn);
+      if (kn.s > k.s) return;  // non-empty range
+    }
+  }
+  // Tail tile t: its participants (n), how many of them reduce it (nred)
+  // and this cluster's index among the participants (j).  The reducers are
+  // the first nred participants: all of them, except the last one when its
+  // range runs on into tile t + 1 -- that cluster holds the head of t + 1
+  // and reduces that tile instead, so that every cluster reduces one tile.
+  struct Part {
+    uint32_t n, nred, j;
+  };
+  __device__ __forceinline__ Part participants(uint32_t t) const {
+    const uint64_t end = uint64_t(t + 1) * kb;
+    Part r{0u, 0u, 0u};
+    uint32_t last = 0;
+    for (Cursor k = first_part(t); k.cc < P; next_part(k, end)) {
+      if (k.cc == c) r.j = r.n;
+      last = k.cc;
+      ++r.n;
+    }
+    const bool last_goes_on = t + 1 < U - dp_end && holder(end) == last;
+    r.nred = r.n - (last_goes_on && r.n > 1 ? 1u : 0u);
+    return r;
+  }
+  // The i-th piece of work: unit, K-block range [k0, k1) and kind.  The
+  // pieces of the tail range come first (in K order), then the whole units:
+  // every cluster starts the tail at once, and the reduction of the split
+  // tiles runs in the epilogue warps while the MMAs of the whole units go on.
   __device__ __forceinline__ bool item(uint32_t i, uint32_t& unit, uint32_t& k0, uint32_t& k1,
                                        int& kind) const {
-    if (i < n_dp) {
-      unit = c + i * P;
-      k0 = 0;
-      k1 = kb;
-      kind = kWhole;
+    if (i < n_pieces) {
+      const uint64_t t = s / kb + i;
+      const uint64_t t0 = t * kb;
+      const uint32_t a = s > t0 ? uint32_t(s - t0) : 0u;
+      const uint32_t b = e < t0 + kb ? uint32_t(e - t0) : kb;
+      unit = dp_end + uint32_t(t);
+      k0 = a;
+      k1 = b;
+      kind = a > 0 ? kPartial : (b == kb ? kWhole : kFirst);
       return true;
     }
-    i -= n_dp;
-    if (s >= e) return false;
-    const uint64_t t = s / kb + i;
-    const uint64_t t0 = t * kb;
-    if (t0 >= e) return false;
-    const uint32_t a = s > t0 ? uint32_t(s - t0) : 0u;
-    const uint32_t b = e < t0 + kb ? uint32_t(e - t0) : kb;
-    unit = dp_end + uint32_t(t);
-    k0 = a;
-    k1 = b;
-    kind = a > 0 ? kPartial : (b == kb ? kWhole : kFirst);
+    i -= n_pieces;
+    if (i >= n_dp) return false;
+    unit = c + i * P;
+    k0 = 0;
+    k1 = kb;
+    kind = kWhole;
     return true;
   }
 };
@@ -669,15 +720,105 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------- epilogue: TMEM -> registers -> C ----------------
-    // Warp w owns TMEM lanes (rows) 32*(w%4) .. +31.  A partial piece goes to
-    // this cluster's workspace slot and is published per warp with a release
-    // flag; the owner of the tile's first piece waits, warp by warp, for the
-    // matching warps of the later pieces, streams their blocks into shared
-    // memory and adds them in K order.
+    // Warp w owns TMEM lanes (rows) 32*(w%4) .. +31 of the accumulator, in
+    // chunks of 32 columns.  A whole tile goes to C chunk by chunk.  A piece
+    // of a split Stream-K tile (the cluster's first items) is published
+    // instead: all its chunks go to this cluster's workspace slot, released
+    // per warp with a flag, and the accumulator is freed at once.  After its
+    // last piece, the warp reduces its share of the split tiles this cluster
+    // reduces -- every piece of a chunk added in K order -- and writes that
+    // share of C, while the MMA warp already works on the whole tiles.  So
+    // the partial sums of a split tile are spread over its participants, and
+    // their exchange overlaps the rest of the launch.
+    constexpr uint32_t NCH = uint32_t(BN / 32);  // chunks per warp and tile
     const uint32_t q = warp & 3u;
     uint32_t acc = 0, acc_phase = 0;
     uint32_t w, kbeg, kend;
     int kind;
+    const uint32_t stg_warp = sStg + (warp - 2u) * 2u * K_::STG_BOX_BYTES;
+    uint32_t nstored = 0;  // chunks stored so far (they alternate between two boxes)
+    // One 32 x 32 chunk: registers -> staging box (row r at r*128 bytes, its
+    // 16-byte piece j at slot j ^ (r mod 8): the 8 lanes of each 16-byte
+    // phase hit 8 different bank groups) -> TMA store at C (col, row), parts
+    // beyond M or N clipped by the tensor map.
+    auto store_chunk = [&](float (&f)[32], int32_t col, int32_t row) {
+      const uint32_t box = stg_warp + (nstored & 1u) * K_::STG_BOX_BYTES;
+      ++nstored;
+      // the store that last read this box (two chunks ago) must be done
+      if (lane == 0) ptx::bulk_wait_group_read<1>();
+      __syncwarp();
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const uint32_t dst = box + lane * 128u + ((uint32_t(v) ^ (lane & 7u)) << 4);
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(f[4 * v]),
+                     "f"(f[4 * v + 1]), "f"(f[4 * v + 2]), "f"(f[4 * v + 3])
+                     : "memory");
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_2d(&tmC, box, col, row);
+        ptx::bulk_commit_group();
+      }
+    };
+    // Stream-K workspace: per cluster two slots (its range's piece in the
+    // tile where the range starts, and the head of the next tile), per slot
+    // and CTA of the cluster one 4 KB block per warp and chunk (float4 of
+    // column group v and row r at v*32 + r) and one flag per warp.
+    auto sk_flag = [&](uint32_t cc, uint32_t slot) {
+      return p.sk_flags + ((cc * 2u + slot) * uint32_t(CL) + rank) * 4u + q;
+    };
+    auto sk_block = [&](uint32_t cc, uint32_t slot, uint32_t ch) {
+      return p.sk_ws + ((size_t(cc * 2u + slot) * CL + rank) * 4u + q) * (NCH * 256u) +
+             size_t(ch) * 256u;
+    };
+    // Reduces this warp's share of split tile `unit` (nothing if this
+    // cluster is not one of its reducers): chunk (q, ch) of a tile with nred
+    // reducers belongs to participant (q * NCH + ch) mod nred.  Waits for the
+    // participants' flags, then adds their blocks of each chunk in K order
+    // and stores the sum.
+    auto reduce_tile = [&](uint32_t unit) -> bool {
+      const uint32_t tt = unit - sch.dp_end;
+      const uint64_t t_beg = uint64_t(tt) * sch.kb, t_end = t_beg + sch.kb;
+      const Schedule::Part pt = sch.participants(tt);
+      if (pt.j >= pt.nred) return true;  // not a reducer of this tile
+      const uint32_t ch0 = (pt.j + pt.nred - (q * NCH) % pt.nred) % pt.nred;
+      if (ch0 >= NCH) return true;  // no chunk of this warp
+      bool got = true;
+      if (lane == 0) {
+        for (Schedule::Cursor k = sch.first_part(tt); k.cc < sch.P; sch.next_part(k, t_end))
+          if (!wait_flag(sk_flag(k.cc, k.s < t_beg ? 1u : 0u), p.epoch, ctl)) {
+            got = false;
+            break;
+          }
+      }
+      if (__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) == 0) return false;
+      __threadfence();  // the acquired partial sums before this warp's loads of them
+      const TileCoord tc = tile_of(p.order, unit, p.sched_m, p.sched_n, uint32_t(p.group));
+      const int32_t row0 = int32_t((tc.m * CL + rank) * BM + q * 32u);
+      const int32_t col0 = int32_t(tc.n) * BN;
+#pragma unroll 1
+      for (uint32_t ch = ch0; ch < NCH; ch += pt.nred) {
+        float f[32];
+        bool first = true;
+        for (Schedule::Cursor k = sch.first_part(tt); k.cc < sch.P; sch.next_part(k, t_end)) {
+          const float4* bx = sk_block(k.cc, k.s < t_beg ? 1u : 0u, ch);
+          float4 x[8];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) x[v] = __ldcg(bx + v * 32 + lane);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            f[4 * v] = first ? x[v].x : f[4 * v] + x[v].x;
+            f[4 * v + 1] = first ? x[v].y : f[4 * v + 1] + x[v].y;
+            f[4 * v + 2] = first ? x[v].z : f[4 * v + 2] + x[v].z;
+            f[4 * v + 3] = first ? x[v].w : f[4 * v + 3] + x[v].w;
+          }
+          first = false;
+        }
+        store_chunk(f, col0 + int32_t(ch * 32u), row0);
+      }
+      return true;
+    };
     for (uint32_t i = 0; next_item_warp(i, w, kbeg, kend, kind); ++i) {
       const bool ok = wait(tfull_bar(acc), acc_phase, ctl);
       if (!__all_sync(0xFFFFFFFFu, ok)) { aborted = true; break; }
@@ -685,20 +826,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const TileCoord t = tile_of(p.order, w, p.sched_m, p.sched_n, uint32_t(p.group));
       const uint32_t cta_m = t.m * CL + rank, cta_n = t.n;
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + acc * BN;
-      if (kind == kPartial) {
-        // workspace slot of this CTA: per warp and 32-column chunk one
-        // contiguous 4 KB block, float4 (column group v, row) at v*32 + row,
-        // so that the owner fetches a block with one bulk copy
-        float4* slot = p.sk_ws + size_t(sch.c * CL + rank) * (BN / 4) * BM +
-                       size_t(q) * (BN / 32) * 256;
+      if (kind != kWhole) {
+        // a piece of a split tile: publish all its chunks, free the accumulator
+        const uint32_t tt = w - sch.dp_end;
+        const uint32_t slot = sch.s < uint64_t(tt) * sch.kb ? 1u : 0u;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (uint32_t ch = 0; ch < NCH; ++ch) {
           uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c, r);
+          ptx::tmem_ld_32x32b_x32(taddr + ch * 32u, r);
           ptx::tmem_ld_wait();
+          float4* blk = sk_block(sch.c, slot, ch);
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            __stcg(slot + size_t(c / 32) * 256 + v * 32 + lane,
+            __stcg(blk + v * 32 + lane,
                    make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
                                __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
         }
@@ -708,97 +848,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           if constexpr (PAIR) ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
           else ptx::mbar_arrive(tempty_bar(acc));
-          ptx::st_release_gpu(p.sk_flags + (sch.c * CL + rank) * 4u + q, p.epoch);
+          ptx::st_release_gpu(sk_flag(sch.c, slot), p.epoch);
+          // the trace names the cluster holding the tile's first K block
+          if (warp == 2 && p.trace && kind == kFirst) {
+            const uint64_t idx = uint64_t(cta_m) * p.sched_n + cta_n;
+            p.trace[2 * idx] = int32_t(blockIdx.x);
+            p.trace[2 * idx + 1] = int32_t(i);
+          }
+        }
+        if (i + 1 == sch.n_pieces) {
+          // the last piece: reduce the split tiles (one of them, as a rule)
+          bool okr = true;
+#pragma unroll 1
+          for (uint32_t h = 0; h < sch.n_pieces && okr; ++h) {
+            uint32_t wh, bh, eh;
+            int kh;
+            sch.item(h, wh, bh, eh, kh);
+            okr = reduce_tile(wh);
+          }
+          if (!okr) { aborted = true; break; }
         }
       } else {
-        // owner of a tile's first piece: the later pieces come from clusters
-        // c+1, c+2, ... whose (non-empty) ranges start inside this tile
-        const uint64_t tile_end =
-            kind == kFirst ? uint64_t(w - sch.dp_end + 1) * sch.kb : uint64_t(0);
-        const Schedule::Cursor peer0 =
-            kind == kFirst ? sch.cursor(sch.c + 1) : Schedule::Cursor{0, 0, sch.P};
-        // advances k to the first cluster at or after it whose range is
-        // non-empty and starts inside this tile (k.cc == P: none left)
-        auto next_peer = [&](Schedule::Cursor& k) {
-          while (k.cc < sch.P && k.s < tile_end) {
-            Schedule::Cursor kn = k;
-            sch.step(kn);
-            if (k.s < kn.s) return;
-            k = kn;
-          }
-          k.cc = sch.P;
-        };
-        uint32_t npeers = 0;
-        if (kind == kFirst) {
-          bool got = true;
-          if (lane == 0) {
-            Schedule::Cursor k = peer0;
-            for (next_peer(k); k.cc < sch.P;) {
-              if (!wait_flag(p.sk_flags + (k.cc * CL + rank) * 4u + q, p.epoch, ctl)) {
-                got = false;
-                break;
-              }
-              ++npeers;
-              sch.step(k);
-              next_peer(k);
-            }
-          }
-          got = __shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0) != 0;
-          npeers = __shfl_sync(0xFFFFFFFFu, npeers, 0);
-          if (!got) { aborted = true; break; }
-          __threadfence();
-        }
-        // The peers' blocks (chunk by chunk, peers in K order) stream into a
-        // ring of 4 KB slots in this warp's quarter of the operand stages,
-        // idle now: this is the cluster's last item, its MMAs are complete
-        // and no load is pending.  Up to `kRing` bulk copies are in flight,
-        // where fetching block by block into registers would leave one
-        // dependent L2 round trip per chunk at the very end of the kernel.
-        constexpr uint32_t kRingWarp = uint32_t(STAGES * K_::STAGE_BYTES / 4) & ~4095u;
-        constexpr uint32_t kRing = kRingWarp / 4096u - 1u;  // the last 4 KB holds the barriers
-        static_assert(kRing >= 2, "fix-up ring");
-        const uint32_t ring = sA + (warp - 2u) * kRingWarp;
-        const uint32_t ring_bar0 = ring + kRing * 4096u;
-        const uint32_t nitems = npeers * uint32_t(BN / 32);
-        uint32_t issued = 0, consumed = 0, ic = 0;
-        Schedule::Cursor ik = peer0;
-        auto issue = [&]() {  // lane 0: the next block, chunk ic of peer ik
-          const uint32_t sl = issued % kRing;
-          const uint32_t bar = ring_bar0 + 8u * sl;
-          const float4* src = p.sk_ws + size_t(ik.cc * CL + rank) * (BN / 4) * BM +
-                              (size_t(q) * (BN / 32) + ic) * 256;
-          ptx::mbar_arrive_expect_tx(bar, 4096u);
-          ptx::bulk_load(ring + sl * 4096u, src, 4096u, bar);
-          ++issued;
-          sch.step(ik);
-          next_peer(ik);
-          if (ik.cc >= sch.P) {
-            ++ic;
-            ik = peer0;
-            next_peer(ik);
-          }
-        };
-        if (nitems > 0) {
-          if (lane == 0) {
-            for (uint32_t j = 0; j < kRing; ++j) ptx::mbar_init(ring_bar0 + 8u * j, 1);
-            ptx::fence_mbar_init();
-            ptx::fence_proxy_async_smem();
-            ptx::fence_proxy_async_global();  // the acquired partials, read by bulk copies
-            next_peer(ik);
-            while (issued < nitems && issued < kRing) issue();
-          }
-          __syncwarp();
-        }
-        // C tile rows of this warp: (cta_m*128 + q*32) .. +31.  Each 32-column
-        // chunk goes registers -> staging box (row r at r*128 bytes, its 16-byte
-        // piece j at slot j ^ (r mod 8): the 8 lanes of each 16-byte phase hit
-        // 8 different bank groups) -> TMA store (full 128-byte lines; parts
-        // beyond M or N are clipped by the tensor map).
         const int32_t row0 = int32_t(cta_m * BM + q * 32u);
-        constexpr int width = BN;
         const int32_t col0 = int32_t(cta_n) * BN;
-        const uint32_t stg_warp = sStg + (warp - 2u) * 2u * K_::STG_BOX_BYTES;
-        // A tile's C leaves as 4 x width/32 TMA stores of 4 KB; issued in one
+        // A tile's C leaves as 4 x BN/32 TMA stores of 4 KB; issued in one
         // burst they share the TMA unit with the operand loads of the next
         // tile's first stages, and the MMA thread stalls there.  When another
         // tile follows, the stores are spread out with a short gap (about a
@@ -820,64 +893,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             pace_ns = p.epi_pace_ns;
         }
 #pragma unroll 1
-        for (int c = 0; c < width; c += 32) {
+        for (uint32_t ch = 0; ch < NCH; ++ch) {
           uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c, r);
+          ptx::tmem_ld_32x32b_x32(taddr + ch * 32u, r);
           ptx::tmem_ld_wait();
           float f[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(r[j]);
-          for (uint32_t j = 0; j < npeers; ++j) {
-            const uint32_t sl = consumed % kRing;
-            const bool okb = wait(ring_bar0 + 8u * sl, (consumed / kRing) & 1u, ctl);
-            if (!__all_sync(0xFFFFFFFFu, okb)) { aborted = true; break; }
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              float4 x;
-              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                           : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
-                           : "r"(ring + sl * 4096u + uint32_t(v * 32 + lane) * 16u)
-                           : "memory");
-              f[4 * v] += x.x;
-              f[4 * v + 1] += x.y;
-              f[4 * v + 2] += x.z;
-              f[4 * v + 3] += x.w;
-            }
-            __syncwarp();
-            ++consumed;
-            if (lane == 0 && issued < nitems) {
-              ptx::fence_proxy_async_smem();  // this slot's reads before its next fill
-              issue();
-            }
-          }
-          if (aborted) break;
-          const uint32_t box = stg_warp + uint32_t((c / 32) & 1) * K_::STG_BOX_BYTES;
-          // the store that last read this box (two chunks ago) must be done
-          if (lane == 0) ptx::bulk_wait_group_read<1>();
-          __syncwarp();
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            const uint32_t dst = box + lane * 128u + ((uint32_t(v) ^ (lane & 7u)) << 4);
-            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "f"(f[4 * v]),
-                         "f"(f[4 * v + 1]), "f"(f[4 * v + 2]), "f"(f[4 * v + 3])
-                         : "memory");
-          }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_2d(&tmC, box, col0 + c, row0);
-            ptx::bulk_commit_group();
-          }
-          if (pace_ns && c + 32 < width) {
+          store_chunk(f, col0 + int32_t(ch * 32u), row0);
+          if (pace_ns && ch + 1 < NCH) {
             const uint64_t t0 = ptx::global_timer_ns();
             while (ptx::global_timer_ns() - t0 < pace_ns) __nanosleep(100);
           }
-        }
-        if (aborted) {
-          // a ring wait expired: let the copies already issued land first
-          if (lane == 0 && issued > consumed) spin_ns(50000);
-          __syncwarp();
-          break;
         }
         ptx::tc_fence_before();
         __syncwarp();
@@ -1085,8 +1112,9 @@ static int make_plan(int M, int N, int persistent, const swz_gemm_opts& o, const
   return SWZ_OK;
 }
 
-// Stream-K workspace: flags [clusters][CL][4] uint32 (256-byte aligned
-// block), then partial accumulators [clusters][CL][BN/4][128] float4.
+// Stream-K workspace: flags [clusters][2 slots][CL][4 warps] uint32 (a
+// 256-byte aligned block), then partial sums [clusters][2 slots][CL][4
+// warps][BN/32 chunks] of 4 KB blocks (32 rows x 32 fp32 columns).
 struct SkLayout {
   bool active;
   uint64_t flags_bytes, data_bytes;
@@ -1101,8 +1129,8 @@ static SkLayout sk_layout(const Plan& pl, int persistent, const swz_gemm_opts& o
   const uint32_t clusters = uint32_t(pl.programs) / cl;
   if (!o.stream_k || !persistent || clusters == 0 || pl.units % clusters == 0) return L;
   L.active = true;
-  L.flags_bytes = (uint64_t(clusters) * cl * 4u * 4u + 255u) & ~uint64_t(255);
-  L.data_bytes = uint64_t(clusters) * cl * BM * uint64_t(pl.bn) * 4u;
+  L.flags_bytes = (uint64_t(clusters) * 2u * cl * 4u * 4u + 255u) & ~uint64_t(255);
+  L.data_bytes = uint64_t(clusters) * 2u * cl * BM * uint64_t(pl.bn) * 4u;
   return L;
 }
 
@@ -1260,8 +1288,9 @@ extern "C" int swz_gemm_workspace_size(int M, int N, int K, int persistent,
   return SWZ_OK;
 }
 
-extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N, int K, int order,
-                           int group, int persistent, const swz_gemm_opts* opts, void* stream) {
+namespace swz {
+int gemm_ex(const void* A, const void* B, float* C, int M, int N, int K, int order, int group,
+            int persistent, const swz_gemm_opts* opts, void* stream, bool clear_sk_flags) {
   swz_gemm_opts o = {};
   if (opts) o = *opts;
   int rc = validate(A, B, C, M, N, K, order, group, o);
@@ -1380,7 +1409,7 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
       // runs in every replay; epochs are never 0).
       cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
       SWZ_CUDA_TRY(cudaStreamIsCapturing(s, &capturing));
-      if (capturing != cudaStreamCaptureStatusNone)
+      if (capturing != cudaStreamCaptureStatusNone || clear_sk_flags)
         SWZ_CUDA_TRY(cudaMemsetAsync(reinterpret_cast<void*>(ws), 0, size_t(L.flags_bytes), s));
       prm.stream_k = 1;
       prm.epoch = e;
@@ -1399,6 +1428,12 @@ extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N,
   if (span == 64) return dispatch<64, false>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
   if (span == 32) return dispatch<32, false>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
   return dispatch<128, false>(pl, tf32, ta, ta3, tb, tb3, tc, prm, s);
+}
+}  // namespace swz
+
+extern "C" int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N, int K, int order,
+                           int group, int persistent, const swz_gemm_opts* opts, void* stream) {
+  return swz::gemm_ex(A, B, C, M, N, K, order, group, persistent, opts, stream, false);
 }
 
 extern "C" int swz_gemm(const void* A, const void* B, float* C, int M, int N, int K, int order,

@@ -9,6 +9,12 @@
 // B tile (k, n).  With CTA clusters of `cluster_m` CTAs along M, the order
 // runs on cluster tiles and each cluster tile contributes its CTA tiles in
 // rank order (TVM TIRx "ClusterPersistentScheduler2D", Example 2).
+//
+// l2_partitions > 1 is not the page's model but a reading of a GPU whose L2
+// is split into that many halves (one per die, as on GB300): the SMs of
+// every die read every operand line of a wave, and each die's half keeps its
+// own copy of what its SMs read, so each half replays the whole trace with
+// 1 / l2_partitions of the capacity.  The prediction is that of one half.
 #include <stdint.h>
 
 #include <list>
@@ -61,11 +67,12 @@ inline uint64_t key_b(uint64_t k, uint64_t n) { return (uint64_t(1) << 63) | (n 
 
 extern "C" int swz_l2_model_bytes(int order, int group, int M, int N, int K, int tile_m,
                                   int tile_n, int tile_k, int elem_bytes, int64_t l2_bytes,
-                                  int concurrency, int cluster_m, int64_t* hits,
-                                  int64_t* misses, int64_t* miss_bytes) {
+                                  int l2_partitions, int concurrency, int cluster_m,
+                                  int64_t* hits, int64_t* misses, int64_t* miss_bytes) {
   if (!swz::order_is_valid(order) || (swz::order_uses_group(order) && group < 1)) return SWZ_EINVAL;
   if (M <= 0 || N <= 0 || K <= 0 || tile_m <= 0 || tile_n <= 0 || tile_k <= 0) return SWZ_EINVAL;
   if (elem_bytes <= 0 || l2_bytes < 0 || concurrency <= 0 || cluster_m <= 0) return SWZ_EINVAL;
+  if (l2_partitions < 1) return SWZ_EINVAL;
   if (!hits || !misses || !miss_bytes) return SWZ_EINVAL;
   const int64_t span_m = int64_t(tile_m) * cluster_m;
   const uint32_t sm = uint32_t((int64_t(M) + span_m - 1) / span_m);
@@ -84,7 +91,7 @@ extern "C" int swz_l2_model_bytes(int order, int group, int M, int N, int K, int
   }
   const int64_t a_bytes = int64_t(tile_m) * tile_k * elem_bytes;
   const int64_t b_bytes = int64_t(tile_k) * tile_n * elem_bytes;
-  LruBytes cache(l2_bytes);
+  LruBytes cache(l2_bytes / l2_partitions);
   for (size_t w0 = 0; w0 < seq.size(); w0 += size_t(concurrency)) {
     const size_t w1 = w0 + size_t(concurrency) < seq.size() ? w0 + size_t(concurrency) : seq.size();
     for (uint32_t k = 0; k < gk; ++k) {
@@ -106,5 +113,5 @@ extern "C" int swz_l2_model(int order, int group, int M, int N, int K, int tile_
   if (!hits || !misses) return SWZ_EINVAL;
   int64_t bytes = 0;
   return swz_l2_model_bytes(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_bytes,
-                            concurrency, cluster_m, hits, misses, &bytes);
+                            1, concurrency, cluster_m, hits, misses, &bytes);
 }

@@ -5,9 +5,12 @@
 // someone else, loops that must not call cudaMalloc because it synchronises
 // the device).  The source pages have no counterpart of this entry point.
 //
-// The array lives in this translation unit only, so the 24 MiB are held by a
+// The array lives in this translation unit only, so the 40 MiB are held by a
 // GPU once this file's code is loaded there (at the latest on the first call
-// of the entry point) and stay held until the process exits.
+// of the entry point) and stay held until the process exits.  That covers
+// the largest launch with the default program count on a GB300: two
+// workspace slots per program of 128 x 256 FP32 partial sums (1-CTA tiles,
+// 152 programs, or 76 CTA pairs), 38 MiB, and their flags.
 #include <mutex>
 
 #include "common.h"
@@ -20,7 +23,9 @@ namespace {
 static __device__ __align__(256) unsigned char noalloc_scratch[SWZ_NOALLOC_SCRATCH_BYTES];
 
 // Device address of noalloc_scratch on `device`, which must be current.
-// Looked up once per device and cached.
+// Looked up once per device and kept for the life of the process: it does
+// not survive cudaDeviceReset (the array is allocated anew in the next
+// context), so the entry point must not be called after a reset.
 int scratch_address(int device, void** out) {
   static std::mutex mu;
   static void* addr[64] = {};
@@ -60,13 +65,12 @@ extern "C" int swz_gemm_streamk_noalloc(const void* A, const void* B, float* C, 
       void* scratch = nullptr;
       rc = scratch_address(dev.device, &scratch);
       if (rc != SWZ_OK) return rc;
-      // The flags must not hold a value this launch could mistake for a
-      // finished piece: clear them (the partial sums need no clearing).
-      SWZ_CUDA_TRY(cudaMemsetAsync(scratch, 0, size_t(flag_bytes),
-                                   static_cast<cudaStream_t>(stream)));
       o.d_workspace = scratch;
       o.workspace_bytes = SWZ_NOALLOC_SCRATCH_BYTES;
     }
   }
-  return swz_gemm_ex(A, B, C, M, N, K, order, group, 1, &o, stream);
+  // The flags must not hold a value this launch could mistake for a
+  // finished piece: the launch clears them on the stream first (the partial
+  // sums need no clearing), once every argument check has passed.
+  return swz::gemm_ex(A, B, C, M, N, K, order, group, 1, &o, stream, true);
 }
