@@ -365,6 +365,9 @@ def run_swz(args):
     line = {"metric": METRIC, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": wl["dtype"], "data": "synthetic"}
+    if args.die_split:
+        dies = swz.calibrate()
+        line["die_calibration"] = {"sms_per_die": [dies.count(0), dies.count(1)]}
     head_order = args.order or HEADLINE["order"]
     head_group = args.group or HEADLINE["group"]
 
@@ -381,7 +384,7 @@ def run_swz(args):
 
     def gemm_once(order, group, span=0):
         swz.gemm(Ad, Bd, order, group, persistent, out=C, stream_k=args.stream_k,
-                 workspace=ws, smem_swizzle=span, **cfg)
+                 workspace=ws, smem_swizzle=span, die_split=args.die_split, **cfg)
 
     def timed(fn, steps, warmup):
         for _ in range(warmup):
@@ -868,6 +871,9 @@ def main():
                     default=None, help="headline tile order (default panel)")
     ap.add_argument("--group", type=int, default=None, help="G or S of the headline order")
     ap.add_argument("--stream-k", action="store_true", help="Stream-K tail (persistent only)")
+    ap.add_argument("--die-split", action="store_true",
+                    help="each die's clusters take their own share of the tiles (calibrates "
+                         "the device first; persistent only)")
     ap.add_argument("--non-persistent", action="store_true", help="one CTA (pair) per tile")
     ap.add_argument("--e2e-slabs", type=int, default=8, help="row slabs of the host pipeline")
     ap.add_argument("--no-mma-sync", action="store_true")

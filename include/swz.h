@@ -177,6 +177,25 @@ typedef struct swz_gemm_opts {
                         swz_gemm_workspace_size bytes = 256) and is cleared on
                         `stream` before the launch; launches sharing a
                         workspace must not overlap.                          */
+  int die_split;     /* persistent only, not with dynamic: 1 = split the work
+                        between the two dies of the package.  The clusters on
+                        die 0 take the first U0 scheduler units of the tile
+                        order and the clusters on die 1 the rest (U0 = the
+                        units times die 0's share of the clusters, rounded),
+                        each die striding (and with stream_k splitting its own
+                        tail) over its own clusters, so that most operand
+                        lines are read by the SMs of one die.  Needs
+                        swz_calibrate on the device first (SWZ_EUNSUPPORTED
+                        otherwise).  Applies to launches at the resident
+                        capacity (num_programs 0); other launches, and a
+                        device whose SMs all sit on one die, run the plain
+                        schedule.  The die of each cluster only decides which
+                        tiles it takes (see swz_gemm_die_plan): whole tiles
+                        are those of the plain schedule bit for bit; with
+                        stream_k each die splits its own tail, so other tiles
+                        are split at other K blocks than in the plain
+                        schedule (the same result up to FP32 summation order,
+                        deterministic from run to run).  0: off              */
 } swz_gemm_opts;
 
 /* debug_flags: withhold the first operand load so that the consumer's
@@ -192,7 +211,9 @@ typedef struct swz_gemm_opts {
  * misaligned (256 B) or too small workspace, and for smem_swizzle not in
  * {0, 32, 64, 128}; for dynamic the same workspace rules, SWZ_EINVAL for a
  * value other than 0 or 1, without persistent or with stream_k,
- * SWZ_EUNSUPPORTED with a span other than 128.
+ * SWZ_EUNSUPPORTED with a span other than 128; for die_split SWZ_EINVAL for
+ * a value other than 0 or 1, without persistent or with dynamic,
+ * SWZ_EUNSUPPORTED on a device swz_calibrate has not measured.
  * In Stream-K mode the trace records, for a split tile, the program that
  * wrote it. */
 int swz_gemm_ex(const void* A, const void* B, float* C, int M, int N, int K,
@@ -229,6 +250,42 @@ int swz_gemm_host(const void* h_A, const void* h_B, float* h_C, int M, int N, in
  * 0 (resident capacity). */
 int swz_gemm_workspace_size(int M, int N, int K, int persistent,
                             const swz_gemm_opts* opts, uint64_t* h_bytes);
+
+/*
+ * swz_calibrate -- finds, on the current device, which die of the package
+ * each SM sits on and where each persistent GEMM kernel shape places its
+ * CTAs, for the die_split schedule.  No source page has a counterpart: it
+ * is a GB300 property (two dies, each with half of the L2; a line one die's
+ * SM has read is a slower L2 hit for the other die's SMs).
+ *
+ * The die of an SM is found by timing: one CTA reads a buffer into its half
+ * of the L2, then one CTA per SM times a chain of dependent loads through
+ * its own slice; the SMs of the other die see the cross-die latency.  The
+ * placement is recorded by launching each kernel shape once at its resident
+ * capacity (the hardware places persistent CTAs the same way every time).
+ * The call is synchronous: it allocates and frees temporary device buffers
+ * (about 16 KB per SM), launches the probe kernels and waits for them.
+ * Results are kept per device for the life of the process; calling again
+ * repeats the measurement.
+ *   h_die_of_sm  host, max_sms ints (may be NULL with max_sms 0): the die
+ *                (0 or 1) of SM id s at [s]; all 0 on a single die
+ *   h_num_sms    host, optional: the device's SM count
+ * Errors: SWZ_EINVAL, SWZ_EARCH, SWZ_ECUDA, SWZ_EUNSUPPORTED (not every SM
+ * could be measured, e.g. while other work occupies the device).
+ */
+int swz_calibrate(int* h_die_of_sm, int max_sms, int* h_num_sms);
+
+/* The die split a persistent launch with these arguments would use
+ * (opts->die_split need not be set): for each cluster g (CTAs g*c .. g*c +
+ * c - 1, c = 2 with cta_pair) h_cluster_info[g] = die << 15 | rank of the
+ * cluster among its die's clusters, h_P0 = die 0's clusters, h_U0 = the
+ * scheduler units die 0 takes, h_clusters = the launch's clusters.  When the
+ * launch gets no split, every cluster reads as die 0 with rank g, P0 = the
+ * clusters and U0 = the units.  Errors: SWZ_EINVAL, SWZ_EUNSUPPORTED (device
+ * not calibrated), as swz_gemm_plan otherwise. */
+int swz_gemm_die_plan(int M, int N, int K, const swz_gemm_opts* opts,
+                      int32_t* h_cluster_info, int max_clusters, int* h_clusters,
+                      int* h_P0, int* h_U0);
 
 /* Grid and launch the GEMM would use, without launching: tiles_m, tiles_n
  * (CTA tiles), sched_m, sched_n (scheduler grid: cluster tiles in 2-CTA mode)

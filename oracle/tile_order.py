@@ -274,3 +274,63 @@ def stream_k_ranges(num_clusters, tail_units, k_blocks):
     I = tail_units * k_blocks
     return [(I * c // num_clusters, I * (c + 1) // num_clusters)
             for c in range(num_clusters)]
+
+
+def die_split_trace(order, gm, gn, group, cluster_die, k_blocks=None, cluster_m=1):
+    """The persistent schedule with its work split between two dies, CTA by CTA.
+
+    Not from the pages: the library's die split.  Cluster g (CTAs
+    g * cluster_m .. g * cluster_m + cluster_m - 1) sits on die
+    cluster_die[g] (0 or 1); its rank is the number of clusters before it on
+    the same die.  With P clusters, P0 of them on die 0, and U scheduler
+    units in tile-order sequence, die 0 takes units [0, U0) and die 1 units
+    [U0, U), where U0 = floor((U * P0 + floor(P / 2)) / P), that is U * P0 / P
+    rounded with halves going up.  Each die schedules its units over its own
+    clusters as a launch of that many clusters would: by work-index striding
+    (the die's unit i goes to its rank i mod P_d as that cluster's item
+    i div P_d), or, with k_blocks given, with a Stream-K tail of the die's
+    own R_d = U_d mod P_d units over its P_d clusters as in stream_k_trace
+    (a cluster's tail pieces first, then its whole units).  With every
+    cluster on one die the launch is not split.
+
+    Returns {(cta_m, cta_n): (program, item index)} as stream_k_trace.
+    """
+    if gm % cluster_m:
+        raise ValueError("the cluster shape must divide the CTA-tile grid")
+    P = len(cluster_die)
+    members = [[g for g in range(P) if cluster_die[g] == d] for d in (0, 1)]
+    if not members[0] or not members[1]:
+        if k_blocks is None:
+            return persistent_trace(order, gm, gn, group, P * cluster_m, cluster_m=cluster_m)
+        return stream_k_trace(order, gm, gn, group, P * cluster_m, k_blocks, cluster_m)
+    seq = tile_sequence(order, gm // cluster_m, gn, group)
+    U = len(seq)
+    U0 = (U * len(members[0]) + P // 2) // P
+    trace = {}
+
+    def put(unit, g, item):
+        m_idx, n_idx = seq[unit]
+        for r in range(cluster_m):
+            key = (m_idx * cluster_m + r, n_idx)
+            if key in trace:
+                raise AssertionError(f"tile {key} written twice")
+            trace[key] = (g * cluster_m + r, item)
+
+    for d, (lo, hi) in enumerate(((0, U0), (U0, U))):
+        Pd, Ud = len(members[d]), hi - lo
+        R = Ud % Pd if k_blocks is not None else 0
+        full = Ud - R
+        pieces = [0] * Pd
+        if R:
+            I = R * k_blocks
+            for r in range(Pd):
+                s, e = I * r // Pd, I * (r + 1) // Pd
+                t = s // k_blocks
+                while s < e and t * k_blocks < e:
+                    if t * k_blocks >= s:
+                        put(lo + full + t, members[d][r], pieces[r])
+                    pieces[r] += 1
+                    t += 1
+        for w in range(full):
+            put(lo + w, members[d][w % Pd], pieces[w % Pd] + w // Pd)
+    return trace

@@ -253,3 +253,43 @@ def test_stream_k_trace_against_brute_force(gm, gn, P, kb, cm):
         m, n = seq[U - R + t]
         for r in range(cm):
             assert tr[(m * cm + r, n)] == (c * cm + r, earlier)
+
+
+def test_die_split_trace_hand_example():
+    # 1 x 6 tiles in row order, 4 clusters on dies 0, 1, 1, 0: P0 = 2, so die
+    # 0 takes U0 = floor((6 * 2 + 2) / 4) = 3 units.  Die 0's clusters 0 and 3
+    # (ranks 0, 1) stride over units 0-2, die 1's clusters 1 and 2 over 3-5.
+    dies = [0, 1, 1, 0]
+    assert to.die_split_trace(to.ROW, 1, 6, 1, dies) == {
+        (0, 0): (0, 0), (0, 1): (3, 0), (0, 2): (0, 1),
+        (0, 3): (1, 0), (0, 4): (2, 0), (0, 5): (1, 1)}
+    # with a Stream-K tail, 2 K blocks a tile: each die has 3 units on 2
+    # clusters, so units 0, 1 (die 0) and 3, 4 (die 1) go out whole and units
+    # 2 and 5 are split block by block ([0,1) and [1,2)); the first block's
+    # cluster holds the head (its item 0), whole units come after the pieces
+    assert to.die_split_trace(to.ROW, 1, 6, 1, dies, k_blocks=2) == {
+        (0, 0): (0, 1), (0, 1): (3, 1), (0, 2): (0, 0),
+        (0, 3): (1, 1), (0, 4): (2, 1), (0, 5): (1, 0)}
+    # 2-CTA clusters: each cluster tile is two CTA tiles, programs 2g and 2g+1
+    tr = to.die_split_trace(to.ROW, 2, 6, 1, dies, cluster_m=2)
+    assert tr[(0, 1)] == (6, 0) and tr[(1, 1)] == (7, 0) and tr[(1, 5)] == (3, 1)
+
+
+@pytest.mark.parametrize("gm,gn,P,kb,cm", [(6, 5, 6, None, 1), (6, 5, 7, 4, 1), (8, 7, 10, 3, 2),
+                                           (4, 3, 9, 5, 1), (2, 1, 12, 64, 2)])
+def test_die_split_trace_covers_every_tile_once(gm, gn, P, kb, cm):
+    import random
+    rnd = random.Random(gm * 100 + P)
+    for _ in range(5):
+        dies = [rnd.randint(0, 1) for _ in range(P)]
+        tr = to.die_split_trace(to.SERPENTINE, gm, gn, 2, dies, k_blocks=kb, cluster_m=cm)
+        assert len(tr) == gm * gn
+        # a program's item indices are 0, 1, 2, ... without gaps over its whole
+        # units (its tail pieces come before, and only heads are recorded)
+        for prog in range(P * cm):
+            its = sorted(it for p, it in tr.values() if p == prog)
+            assert len(set(its)) == len(its)
+    # every cluster on one die: the plain schedules
+    assert to.die_split_trace(to.PANEL, 6, 5, 2, [0] * 7) == to.persistent_trace(to.PANEL, 6, 5, 2, 7)
+    assert to.die_split_trace(to.PANEL, 6, 5, 2, [1] * 7, k_blocks=3) == to.stream_k_trace(
+        to.PANEL, 6, 5, 2, 7, 3)

@@ -37,7 +37,7 @@ EXPORTS = ["swz_tile_map", "swz_is_bijective", "swz_gemm", "swz_gemm_ex", "swz_g
            "swz_device_info", "swz_l2_model", "swz_gemm_workspace_size",
            "swz_gemm_streamk_noalloc", "swz_gemm_host", "swz_gemm_mma_sync", "swz_tc_rate",
            "swz_tc_rate_ex",
-           "swz_l2_model_bytes"]
+           "swz_l2_model_bytes", "swz_calibrate", "swz_gemm_die_plan"]
 
 
 class SwzError(RuntimeError):
@@ -53,7 +53,8 @@ class swz_gemm_opts(ctypes.Structure):
                 ("debug_flags", ctypes.c_uint32), ("timeout_ms", ctypes.c_uint32),
                 ("stream_k", ctypes.c_int), ("d_workspace", ctypes.c_void_p),
                 ("workspace_bytes", ctypes.c_uint64), ("b_layout", ctypes.c_int),
-                ("smem_swizzle", ctypes.c_int), ("dynamic", ctypes.c_int)]
+                ("smem_swizzle", ctypes.c_int), ("dynamic", ctypes.c_int),
+                ("die_split", ctypes.c_int)]
 
 
 _lib = None
@@ -93,6 +94,9 @@ def lib() -> ctypes.CDLL:
         L.swz_gemm_mma_sync.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, i, i, i, vp]
         L.swz_tc_rate.argtypes = [i, i, vp, vp, i, i, vp, vp, vp]
         L.swz_tc_rate_ex.argtypes = [i, i, i, i, vp, vp, i, i, vp, vp, vp]
+        L.swz_calibrate.argtypes = [ip, i, ip]
+        L.swz_gemm_die_plan.argtypes = [i, i, i, ctypes.POINTER(swz_gemm_opts),
+                                        ctypes.POINTER(ctypes.c_int32), i, ip, ip, ip]
         for name in EXPORTS:
             if name != "swz_strerror":
                 getattr(L, name).restype = ctypes.c_int
@@ -141,6 +145,31 @@ def swz_gemm_streamk_noalloc(A, B, C, M, N, K, order, group, opts=None, stream=0
     return lib().swz_gemm_streamk_noalloc(A, B, C, M, N, K, order, group,
                                           ctypes.byref(opts) if opts is not None else None,
                                           stream)
+
+
+def swz_calibrate(max_sms=1024):
+    """(status, [die of SM id s for s < max_sms], SM count) -- see include/swz.h."""
+    dies = (ctypes.c_int * max_sms)()
+    n = ctypes.c_int(0)
+    rc = lib().swz_calibrate(dies, max_sms, ctypes.byref(n))
+    return rc, list(dies[: n.value]), n.value
+
+
+def swz_gemm_die_plan(M, N, K, opts=None, max_clusters=256):
+    """(status, [die << 15 | rank per cluster], P0, U0) of a persistent launch."""
+    info = (ctypes.c_int32 * max_clusters)()
+    nc, p0, u0 = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().swz_gemm_die_plan(M, N, K, ctypes.byref(opts) if opts is not None else None,
+                                 info, max_clusters, ctypes.byref(nc), ctypes.byref(p0),
+                                 ctypes.byref(u0))
+    return rc, list(info[: nc.value]), p0.value, u0.value
+
+
+def calibrate():
+    """Runs swz_calibrate on the current device; the die of every SM id."""
+    rc, dies, _ = swz_calibrate()
+    _check(rc, "swz_calibrate")
+    return dies
 
 
 def swz_gemm_host(hA, hB, hC, M, N, K, order, group, opts, dA, dB, dC, slabs=0, stream=0):
@@ -307,8 +336,9 @@ def tile_map(order, grid_m, grid_n, group=1, device="cuda", stream=None):
 
 def make_opts(dtype=SWZ_F16, tile_n=0, cta_pair=False, num_programs=0, trace=None,
               debug_flags=0, timeout_ms=0, stream_k=False, workspace=None,
-              b_layout=SWZ_B_KN, smem_swizzle=0, dynamic=False):
+              b_layout=SWZ_B_KN, smem_swizzle=0, dynamic=False, die_split=False):
     o = swz_gemm_opts()
+    o.die_split = 1 if die_split else 0
     o.smem_swizzle = smem_swizzle
     o.dynamic = int(dynamic)
     o.b_layout = b_layout
@@ -361,7 +391,7 @@ def _dtype_code(t):
 def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
          cta_pair=False, num_programs=0, trace=None, debug_flags=0, timeout_ms=0,
          stream_k=False, workspace=None, b_transposed=False, smem_swizzle=0,
-         dynamic=False, stream=None):
+         dynamic=False, die_split=False, stream=None):
     """C = A @ B (fp32) through swz_gemm_ex.  A: M x K; B: K x N, or N x K
     when ``b_transposed`` (B stored transposed); both fp16, both bf16, or both
     fp32 (multiplied as TF32); row-major contiguous CUDA tensors.  fp32 inputs
@@ -371,7 +401,8 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
     ``smem_swizzle``: swizzle span of the operand stages, 128 (0), 64 or 32.
     ``dynamic``: claim tiles at run time through an atomic counter kept in
     ``workspace`` (a CUDA tensor of at least workspace_size(..., dynamic=True)
-    bytes); persistent launches only."""
+    bytes); persistent launches only.  ``die_split``: each die's clusters take
+    their own share of the tiles (after ``calibrate()`` on the device)."""
     import torch
     if A.dtype != B.dtype:
         raise TypeError("A and B must have the same dtype")
@@ -390,7 +421,7 @@ def gemm(A, B, order="panel", group=8, persistent=False, *, out=None, tile_n=0,
     C = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=A.device)
     opts = make_opts(code, tile_n, cta_pair, num_programs, trace, debug_flags, timeout_ms,
                      stream_k, workspace, SWZ_B_NK if b_transposed else SWZ_B_KN,
-                     smem_swizzle, dynamic)
+                     smem_swizzle, dynamic, die_split)
     _check(swz_gemm_ex(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _order(order),
                        group, int(bool(persistent)), opts, _stream(stream)), "swz_gemm_ex")
     return C

@@ -19,7 +19,7 @@ ROOT = os.path.dirname(HERE)
 SRC_DIR = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libswz.so")
-SOURCES = ["capi.cu", "transpose.cu", "gemm.cu", "l2_model.cpp", "noalloc.cu",
+SOURCES = ["capi.cu", "transpose.cu", "gemm.cu", "l2_model.cpp", "noalloc.cu", "die.cu",
            "host_pipeline.cu", "gemm_mma_sync.cu", "tc_rate.cu"]
 HEADERS = ["common.h", "ptx.cuh", "tile_order.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

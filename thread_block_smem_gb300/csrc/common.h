@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "swz.h"
 
 namespace swz {
@@ -48,6 +50,15 @@ int gemm_sk_workspace_split(int M, int N, int K, int persistent, const swz_gemm_
 // after every argument check has passed.
 int gemm_ex(const void* A, const void* B, float* C, int M, int N, int K, int order, int group,
             int persistent, const swz_gemm_opts* opts, void* stream, bool clear_sk_flags);
+
+// The die of every SM of the current device (indexed by SM id; 0 or 1,
+// all 0 on a single die), found by timing L2 hits: SWZ_OK, SWZ_ECUDA, or
+// SWZ_EUNSUPPORTED when not every SM could be measured.
+int die_of_sms(int num_sms, std::vector<uint8_t>* die_of_sm);
+
+// The SM id of every CTA of one launch of `grid` CTAs in clusters of
+// `cluster` with `threads` threads and `smem` bytes of dynamic shared memory.
+int placement(int cluster, int threads, int smem, int grid, std::vector<uint32_t>* sm_of_cta);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }

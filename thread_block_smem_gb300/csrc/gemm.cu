@@ -39,7 +39,10 @@
 //     SWZ_ETIMEOUT in a device status word, drains what it issued, frees TMEM
 //     and returns.
 #include <atomic>
+#include <map>
 #include <mutex>
+#include <tuple>
+#include <vector>
 
 #include "common.h"
 #include "ptx.cuh"
@@ -138,6 +141,11 @@ struct Params {
   float4* sk_ws;       // [cluster][rank][BN/4 column groups][128 rows] float4
   uint32_t* dyn_counter;  // dynamic scheduler: work indices claimed beyond the first wave
   uint32_t epi_pace_ns;   // gap between an epilogue warp's chunk stores (tiles with a successor)
+  // die split (static schedules): cluster g sits on die cl_info[g] >> 15 with
+  // rank cl_info[g] & 0x7FFF among that die's clusters; die 0's P0 clusters
+  // take the units [0, U0) of the tile order, die 1's the rest
+  uint32_t die_split, P0, U0;
+  uint16_t cl_info[256];
 };
 
 enum ItemKind : int { kWhole = 0, kFirst = 1, kPartial = 2 };
@@ -159,6 +167,8 @@ struct Schedule {
   uint32_t dp_end;    // units below this are whole tiles
   uint32_t n_dp;      // whole tiles of this cluster
   uint32_t n_pieces;  // tail tiles this cluster's range touches (0, 1 or 2)
+  uint32_t ubase;     // the units of this schedule are ubase .. ubase + U - 1 of the order
+  uint32_t wsbase;    // first Stream-K workspace cluster slot of this schedule's clusters
   uint64_t I;       // Stream-K tail iterations
   uint64_t s, e;    // this cluster's Stream-K tail range [s, e)
   uint64_t Iq;      // I / P and I % P: range starts are stepped from one
@@ -170,6 +180,8 @@ struct Schedule {
     P = P_;
     U = U_;
     kb = kb_;
+    ubase = 0;
+    wsbase = 0;
     const uint32_t R = sk ? U % P : 0u;
     dp_end = U - R;
     n_dp = c < dp_end ? (dp_end - c + P - 1) / P : 0u;
@@ -257,7 +269,7 @@ struct Schedule {
       const uint64_t t0 = t * kb;
       const uint32_t a = s > t0 ? uint32_t(s - t0) : 0u;
       const uint32_t b = e < t0 + kb ? uint32_t(e - t0) : kb;
-      unit = dp_end + uint32_t(t);
+      unit = ubase + dp_end + uint32_t(t);
       k0 = a;
       k1 = b;
       kind = a > 0 ? kPartial : (b == kb ? kWhole : kFirst);
@@ -265,7 +277,7 @@ struct Schedule {
     }
     i -= n_pieces;
     if (i >= n_dp) return false;
-    unit = c + i * P;
+    unit = ubase + c + i * P;
     k0 = 0;
     k1 = kb;
     kind = kWhole;
@@ -415,7 +427,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t units = p.sched_m * p.sched_n;
   Schedule sch;
-  sch.init(blockIdx.x / CL, gridDim.x / CL, units, p.num_kb, p.stream_k != 0);
+  if (p.die_split) {
+    // this cluster's die takes its own share of the units (and of the
+    // Stream-K workspace), with the clusters of that die only
+    const uint32_t info = p.cl_info[blockIdx.x / CL];
+    const bool d1 = (info >> 15) != 0;
+    const uint32_t P1 = gridDim.x / CL - p.P0;
+    sch.init(info & 0x7FFFu, d1 ? P1 : p.P0, d1 ? units - p.U0 : p.U0, p.num_kb,
+             p.stream_k != 0);
+    sch.ubase = d1 ? p.U0 : 0u;
+    sch.wsbase = d1 ? p.P0 : 0u;
+  } else {
+    sch.init(blockIdx.x / CL, gridDim.x / CL, units, p.num_kb, p.stream_k != 0);
+  }
   bool aborted = false;
 
   // Dynamic scheduler (DYN): the producer of the leader CTA claims work
@@ -766,10 +790,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // and CTA of the cluster one 4 KB block per warp and chunk (float4 of
     // column group v and row r at v*32 + r) and one flag per warp.
     auto sk_flag = [&](uint32_t cc, uint32_t slot) {
-      return p.sk_flags + ((cc * 2u + slot) * uint32_t(CL) + rank) * 4u + q;
+      return p.sk_flags + (((sch.wsbase + cc) * 2u + slot) * uint32_t(CL) + rank) * 4u + q;
     };
     auto sk_block = [&](uint32_t cc, uint32_t slot, uint32_t ch) {
-      return p.sk_ws + ((size_t(cc * 2u + slot) * CL + rank) * 4u + q) * (NCH * 256u) +
+      return p.sk_ws + ((size_t((sch.wsbase + cc) * 2u + slot) * CL + rank) * 4u + q) * (NCH * 256u) +
              size_t(ch) * 256u;
     };
     // Reduces this warp's share of split tile `unit` (nothing if this
@@ -778,7 +802,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // participants' flags, then adds their blocks of each chunk in K order
     // and stores the sum.
     auto reduce_tile = [&](uint32_t unit) -> bool {
-      const uint32_t tt = unit - sch.dp_end;
+      const uint32_t tt = unit - sch.ubase - sch.dp_end;
       const uint64_t t_beg = uint64_t(tt) * sch.kb, t_end = t_beg + sch.kb;
       const Schedule::Part pt = sch.participants(tt);
       if (pt.j >= pt.nred) return true;  // not a reducer of this tile
@@ -828,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t taddr = tmem_base + ((q * 32u) << 16) + acc * BN;
       if (kind != kWhole) {
         // a piece of a split tile: publish all its chunks, free the accumulator
-        const uint32_t tt = w - sch.dp_end;
+        const uint32_t tt = w - sch.ubase - sch.dp_end;
         const uint32_t slot = sch.s < uint64_t(tt) * sch.kb ? 1u : 0u;
 #pragma unroll 1
         for (uint32_t ch = 0; ch < NCH; ++ch) {
@@ -1134,6 +1158,65 @@ static SkLayout sk_layout(const Plan& pl, int persistent, const swz_gemm_opts& o
   return L;
 }
 
+// ---- die split ----------------------------------------------------------
+// What swz_calibrate found on each device: the die of every SM, and the SM
+// of every CTA of each persistent kernel shape (clusters, shared memory,
+// CTAs) launched at its resident capacity.
+struct DieCalibration {
+  bool have = false;
+  std::vector<uint8_t> die_of_sm;
+  std::map<std::tuple<int, int, int>, std::vector<uint32_t>> placement;
+};
+static std::mutex g_die_mu;
+static DieCalibration g_die_cal[64];
+
+// dynamic shared memory of the kernel a launch of this plan and span uses
+static int kernel_smem(const Plan& pl, uint32_t span) {
+  const bool ka2 = span == 128 && pl.bn == 128;
+  if (pl.pair) {
+    if (pl.bn == 256) return Cfg<256, true, 1>::SMEM_BYTES;
+    return ka2 ? Cfg<128, true, 2>::SMEM_BYTES : Cfg<128, true, 1>::SMEM_BYTES;
+  }
+  if (pl.bn == 256) return Cfg<256, false, 1>::SMEM_BYTES;
+  return ka2 ? Cfg<128, false, 2>::SMEM_BYTES : Cfg<128, false, 1>::SMEM_BYTES;
+}
+
+struct DieSplit {
+  bool on;            // both dies have clusters of this launch
+  uint32_t P0, U0;    // clusters on die 0, units die 0 takes
+  std::vector<uint16_t> info;  // per cluster: die << 15 | rank on that die
+};
+
+// The die split of a persistent launch of plan `pl` (span `span`) on
+// device `dev`: SWZ_EUNSUPPORTED when the device was not calibrated.  A
+// launch whose shape calibration did not place (a program count other than
+// the resident capacity) gets no split (ds->on false).
+static int die_split_of(const Plan& pl, uint32_t span, int dev, DieSplit* ds) {
+  const int cl = pl.pair ? 2 : 1;
+  const uint32_t clusters = uint32_t(pl.programs) / uint32_t(cl);
+  std::lock_guard<std::mutex> lock(g_die_mu);
+  if (dev < 0 || dev >= 64 || !g_die_cal[dev].have) return SWZ_EUNSUPPORTED;
+  ds->on = false;
+  ds->P0 = clusters;
+  ds->U0 = pl.units;
+  ds->info.clear();
+  const DieCalibration& cal = g_die_cal[dev];
+  const auto it = cal.placement.find(std::make_tuple(cl, kernel_smem(pl, span), pl.programs));
+  if (it == cal.placement.end() || clusters == 0 || clusters > 256) return SWZ_OK;
+  ds->info.assign(clusters, 0);
+  uint32_t n[2] = {0, 0};
+  for (uint32_t g = 0; g < clusters; ++g) {
+    const uint32_t sm = it->second[size_t(g) * cl];
+    const uint32_t d = sm < cal.die_of_sm.size() ? cal.die_of_sm[sm] : 0u;
+    ds->info[g] = uint16_t((d << 15) | n[d]++);
+  }
+  ds->on = n[0] > 0 && n[1] > 0;
+  ds->P0 = n[0];
+  // each die takes units in proportion to its clusters
+  ds->U0 = uint32_t((uint64_t(pl.units) * n[0] + clusters / 2) / clusters);
+  return SWZ_OK;
+}
+
 template <int BN, bool PAIR, int KIND, int SW, bool DYN>
 static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& ta3,
                   const CUtensorMap& tb, const CUtensorMap& tb3, const CUtensorMap& tc,
@@ -1237,6 +1320,65 @@ extern "C" int swz_gemm_plan(int M, int N, int K, int persistent, const swz_gemm
   if (sched_m) *sched_m = int(pl.sched_m);
   if (sched_n) *sched_n = int(pl.sched_n);
   if (programs) *programs = pl.programs;
+  return SWZ_OK;
+}
+
+extern "C" int swz_calibrate(int* h_die_of_sm, int max_sms, int* h_num_sms) {
+  DeviceInfo dev{};
+  int rc = current_device(&dev);
+  if (rc != SWZ_OK) return rc;
+  if (max_sms < 0 || (max_sms > 0 && !h_die_of_sm)) return SWZ_EINVAL;
+  DieCalibration cal;
+  rc = die_of_sms(dev.num_sms, &cal.die_of_sm);
+  if (rc != SWZ_OK) return rc;
+  // the placement of every persistent kernel shape at its resident capacity
+  for (int pair = 0; pair < 2; ++pair)
+    for (int bn : {128, 256})
+      for (uint32_t span : {128u, 64u}) {
+        Plan pl{};
+        pl.pair = pair != 0;
+        pl.bn = bn;
+        int cap = 0;
+        rc = capacity_for(pl, dev, &cap);
+        if (rc != SWZ_OK) return rc;
+        const auto key = std::make_tuple(pair ? 2 : 1, kernel_smem(pl, span), cap);
+        if (cal.placement.count(key)) continue;
+        std::vector<uint32_t> sm;
+        rc = placement(pair ? 2 : 1, kThreads, kernel_smem(pl, span), cap, &sm);
+        if (rc != SWZ_OK) return rc;
+        cal.placement[key] = sm;
+      }
+  cal.have = true;
+  if (h_num_sms) *h_num_sms = dev.num_sms;
+  for (int s = 0; s < max_sms; ++s)
+    h_die_of_sm[s] = s < int(cal.die_of_sm.size()) ? cal.die_of_sm[size_t(s)] : 0;
+  std::lock_guard<std::mutex> lock(g_die_mu);
+  if (dev.device >= 0 && dev.device < 64) g_die_cal[dev.device] = cal;
+  return SWZ_OK;
+}
+
+extern "C" int swz_gemm_die_plan(int M, int N, int K, const swz_gemm_opts* opts,
+                                 int32_t* h_cluster_info, int max_clusters, int* h_clusters,
+                                 int* h_P0, int* h_U0) {
+  swz_gemm_opts o = {};
+  if (opts) o = *opts;
+  if (M <= 0 || N <= 0 || K < 0 || max_clusters < 0 || (max_clusters && !h_cluster_info))
+    return SWZ_EINVAL;
+  DeviceInfo dev{};
+  int rc = current_device(&dev);
+  if (rc != SWZ_OK) return rc;
+  Plan pl{};
+  rc = make_plan(M, N, 1, o, &dev, &pl);
+  if (rc != SWZ_OK) return rc;
+  DieSplit ds{};
+  rc = die_split_of(pl, o.smem_swizzle ? uint32_t(o.smem_swizzle) : 128u, dev.device, &ds);
+  if (rc != SWZ_OK) return rc;
+  const int clusters = pl.programs / (pl.pair ? 2 : 1);
+  if (h_clusters) *h_clusters = clusters;
+  if (h_P0) *h_P0 = ds.on ? int(ds.P0) : clusters;
+  if (h_U0) *h_U0 = ds.on ? int(ds.U0) : int(pl.units);
+  for (int g = 0; g < max_clusters && g < clusters; ++g)
+    h_cluster_info[g] = ds.on ? int32_t(ds.info[size_t(g)]) : int32_t(g);
   return SWZ_OK;
 }
 
@@ -1419,6 +1561,18 @@ int gemm_ex(const void* A, const void* B, float* C, int M, int N, int K, int ord
   }
 
   prm.b3d = b3d ? 1u : 0u;
+  if (o.die_split) {
+    if (o.die_split != 1 || !persistent || o.dynamic) return SWZ_EINVAL;
+    DieSplit ds{};
+    rc = die_split_of(pl, span, dev.device, &ds);
+    if (rc != SWZ_OK) return rc;
+    if (ds.on) {
+      prm.die_split = 1;
+      prm.P0 = ds.P0;
+      prm.U0 = ds.U0;
+      for (size_t g = 0; g < ds.info.size(); ++g) prm.cl_info[g] = ds.info[g];
+    }
+  }
   if (o.dynamic) {
     // the counter of claimed work indices starts at zero in every launch
     prm.dyn_counter = static_cast<uint32_t*>(o.d_workspace);
