@@ -52,7 +52,8 @@ WORKLOADS = {
                                cfg=dict(cta_pair=True), tile=(128, 256), cluster_m=2,
                                sweep=[o for o in _ALL if o != ("panel", 2)]),
     "gemm4096_fp16": dict(M=4096, N=4096, K=4096, dtype="fp16", dist="uniform",
-                          cfg=dict(tile_n=256), tile=(128, 256), cluster_m=1, sweep=_ALL),
+                          cfg=dict(tile_n=256), tile=(128, 256), cluster_m=1,
+                          sweep=_ALL + [("serpentine", 2)]),
     "gemm4096_fp16_pair": dict(M=4096, N=4096, K=4096, dtype="fp16", dist="uniform",
                                cfg=dict(cta_pair=True), tile=(128, 256), cluster_m=2,
                                sweep=_ALL),
@@ -371,6 +372,12 @@ def run_swz(args):
     head_order = args.order or HEADLINE["order"]
     head_group = args.group or HEADLINE["group"]
 
+    if do_gemm and args.stream_k is None:
+        # by default Stream-K where the launch has a full wave of tiles (see sweep())
+        _, (_, _, sm_, sn_, cap) = swz.swz_gemm_plan(M, N, K, 1,
+                                                    swz.make_opts(stream_k=True, **cfg))
+        args.stream_k = persistent and sm_ * sn_ >= cap // (2 if cfg.get("cta_pair") else 1)
+    args.stream_k = bool(args.stream_k) and persistent
     if do_gemm:
         A, B = si.gemm_inputs(M, N, K, wl["dtype"], wl["dist"], seed=0)
         Ad, Bd = A.to(dev), B.to(dev)
@@ -421,6 +428,16 @@ def run_swz(args):
         wC = torch.empty((wM, wN), dtype=torch.float32, device=dev)
         wcfg = dict(w["cfg"])
         _, (_, _, _, _, progs) = swz.swz_gemm_plan(wM, wN, wK, int(persist), swz.make_opts(**wcfg))
+        _, (_, _, sm_, sn_, cap) = swz.swz_gemm_plan(wM, wN, wK, 1,
+                                                    swz.make_opts(stream_k=True, **wcfg))
+        cl = 2 if wcfg.get("cta_pair") else 1
+        # the headline's scheduler, Stream-K, where the launch has a full wave
+        # of tiles to overlap its exchange with (with fewer tiles than
+        # programs every tile would be split and the exchange is exposed)
+        if persist and args.stream_k is not False and sm_ * sn_ >= cap // cl:
+            nws = swz.workspace_size(wM, wN, wK, True, **wcfg)
+            wcfg.update(stream_k=True,
+                        workspace=torch.zeros(max(nws, 256), dtype=torch.uint8, device=dev))
         # the model's wave: resident CTAs (the first page's min(tiles, capacity)),
         # unless overridden (its --num-sms)
         conc = args.num_sms if args.num_sms else progs
@@ -446,7 +463,8 @@ def run_swz(args):
                           "l2_model_2die_dram_err": (dram2 - nd) / nd})
             out.append(o)
         del wA, wB, wC
-        res = {"shape": [wM, wN, wK], "dtype": w["dtype"], "cfg": wcfg,
+        res = {"shape": [wM, wN, wK], "dtype": w["dtype"],
+               "cfg": {k: v for k, v in wcfg.items() if k != "workspace"},
                "persistent": persist, "programs": progs, "orders": out,
                "model": {"l2_bytes": model_l2, "concurrency_ctas": conc}}
         good = [o for o in out if "tflops" in o]
@@ -503,7 +521,6 @@ def run_swz(args):
                         continue
                     w = resolve_workload(argparse.Namespace(**{**vars(args), "workload": wname,
                                                                "m": 0, "n": 0, "k": 0}))
-                    w["sweep"] = CONFIG_ORDERS[key]
                     cf[key] = {("persistent" if p else "non_persistent"): sweep(wname, w, p, 5, 3)
                                for p in modes}
                 line["configs"] = cf
@@ -521,9 +538,12 @@ def run_swz(args):
                 spans.append({"span_bytes": sp, "ms": med, "tflops": flops / med / 1e9})
         # ---- static (work_idx striding) vs dynamic (atomic counter) -------
         sched = {}
-        if args.only == "all" and not args.no_dynamic and persistent and not args.stream_k:
+        if args.only == "all" and not args.no_dynamic and persistent:
             dws = torch.zeros(256, dtype=torch.uint8, device=dev)
-            for name, kw in (("static", {}), ("dynamic", dict(dynamic=True, workspace=dws))):
+            nws = swz.workspace_size(M, N, K, True, **cfg)
+            sws = torch.zeros(max(nws, 256), dtype=torch.uint8, device=dev)
+            for name, kw in (("static", {}), ("stream_k", dict(stream_k=True, workspace=sws)),
+                             ("dynamic", dict(dynamic=True, workspace=dws))):
                 fn = lambda: swz.gemm(Ad, Bd, head_order, head_group, True, out=C, **kw, **cfg)
                 t = timed(fn, max(5, args.steps // 4), 3)
                 sched[name] = {"ms": statistics.median(t),
@@ -545,7 +565,8 @@ def run_swz(args):
         achieved = flops / statistics.mean(ms) / 1e9
         # the captured launch is the default workload's headline launch only
         rec = ncu_record(args.workload)
-        traffic = (rec["traffic_bytes"] if rec and persistent and not args.stream_k
+        traffic = (rec["traffic_bytes"] if rec and persistent
+                   and bool(args.stream_k) == rec["source"].get("stream_k", False)
                    and (head_order, head_group) == rec["traffic_order"] else None)
         line.update({
             "value": world * flops / ms_step / 1e9, "ms_per_step": ms_step,
@@ -870,7 +891,10 @@ def main():
     ap.add_argument("--order", choices=["row", "col", "panel", "morton", "xor", "serpentine"],
                     default=None, help="headline tile order (default panel)")
     ap.add_argument("--group", type=int, default=None, help="G or S of the headline order")
-    ap.add_argument("--stream-k", action="store_true", help="Stream-K tail (persistent only)")
+    ap.add_argument("--stream-k", action=argparse.BooleanOptionalAction, default=None,
+                    help="Stream-K tail of persistent launches (default: on when the launch "
+                         "has a full wave of tiles; --no-stream-k: whole tiles only, the plain "
+                         "work-index stride; --stream-k: always)")
     ap.add_argument("--die-split", action="store_true",
                     help="each die's clusters take their own share of the tiles (calibrates "
                          "the device first; persistent only)")
@@ -900,6 +924,8 @@ def main():
                          "graph, per-call wall time")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
+    if args.non_persistent:
+        args.stream_k = False  # Stream-K shares the tail of a persistent launch
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -157,3 +157,6 @@ def test_config_sweeps_cover_the_specification():
     assert len(bench.CONFIG_ORDERS["cfg1_1024x1024x512_fp16"]) == 6
     assert dict((k, m) for k, _, m in bench.CONFIG_SWEEPS)["cfg2_4096_fp16_tile128x256"] == (
         True, False)
+    # the capture mode (--only sweep) of each workload covers the same orders
+    for key, wname, _ in bench.CONFIG_SWEEPS:
+        assert set(bench.WORKLOADS[wname]["sweep"]) == set(bench.CONFIG_ORDERS[key]), key
