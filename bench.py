@@ -105,18 +105,43 @@ CONFIG_ORDERS = {
 # other source they are left out of the line.
 NCU = {
     "gemm8192_bf16_pair": {
-        "source": {"gemm_cu_sha256": "32dfb91f838bdc4f", "captured": "2026-12-02",
-                   "kernel": "gemm_kernel<256, 1, 0, 128, 0>",
+        "source": {"gemm_cu_sha256": "096ad46accffb076", "captured": "2026-12-02",
+                   "kernel": "gemm_kernel<256, 1, 0, 128, 0>", "stream_k": True,
                    "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum,"
                               "dram__bytes_write.sum --clock-control none -k regex:gemm_kernel "
-                              "python bench.py --only sweep --no-cpu"},
-        "traffic_bytes": 1307546112, "traffic_order": ("serpentine", 8),
-        "orders": {("row", 1): (62.56, 2054057728), ("col", 1): (61.44, 2054787840),
-                   ("panel", 4): (70.64, 1418204672), ("panel", 8): (71.18, 1098593024),
-                   ("panel", 16): (66.87, 1300169216), ("serpentine", 4): (70.25, 1277612288),
-                   ("serpentine", 8): (72.44, 1059105536),
-                   ("serpentine", 16): (69.65, 1270239744), ("morton", 1): (69.53, 1364993024),
-                   ("xor", 1): (63.88, 2055510528)}},
+                              "-s 10 -c 10 python bench.py --only sweep --no-cpu; traffic: ncu "
+                              "--set full -k regex:gemm_kernel -s 3 -c 1 python bench.py --only "
+                              "gemm --steps 1 --warmup 3 --no-cpu"},
+        "traffic_bytes": 1067531008 + 277865472, "traffic_order": ("serpentine", 8),
+        "orders": {("row", 1): (62.92, 2059461120), ("col", 1): (61.23, 2063038464),
+                   ("panel", 4): (69.3, 1434872320), ("panel", 8): (71.85, 1117402880),
+                   ("panel", 16): (68.19, 1321885952), ("serpentine", 4): (69.35, 1280536576),
+                   ("serpentine", 8): (73.31, 1067172352),
+                   ("serpentine", 16): (68.18, 1291457280), ("morton", 1): (67.04, 1387209984),
+                   ("xor", 1): (64.04, 2061828608)}},
+    "gemm4096_fp16": {
+        "source": {"gemm_cu_sha256": "096ad46accffb076", "captured": "2026-12-02",
+                   "kernel": "gemm_kernel<256, 0, 0, 128, 0>", "stream_k": True,
+                   "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum "
+                              "--clock-control none -k regex:gemm_kernel -s 12 -c 12 python "
+                              "bench.py --workload gemm4096_fp16 --only sweep --no-cpu"},
+        "orders": {("row", 1): (80.88, 87051008), ("col", 1): (74.59, 94524672),
+                   ("panel", 2): (79.88, 91400448), ("panel", 4): (80.43, 97858304),
+                   ("panel", 8): (76.39, 96978944), ("panel", 16): (75.2, 110340608),
+                   ("serpentine", 4): (78.73, 96502272), ("serpentine", 8): (77.4, 99362048),
+                   ("serpentine", 16): (79.73, 87741440), ("morton", 1): (73.27, 111463168),
+                   ("xor", 1): (76.17, 109999104), ("serpentine", 2): (75.41, 96200448)}},
+    "gemm6144x10240x4096_fp16_pair": {
+        "source": {"gemm_cu_sha256": "096ad46accffb076", "captured": "2026-12-02",
+                   "kernel": "gemm_kernel<128, 1, 0, 128, 0>", "stream_k": True,
+                   "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum "
+                              "--clock-control none -k regex:gemm_kernel -s 8 -c 8 python "
+                              "bench.py --workload gemm6144x10240x4096_fp16_pair --only sweep "
+                              "--no-cpu"},
+        "orders": {("row", 1): (67.3, 1091503616), ("col", 1): (82.36, 289594368),
+                   ("panel", 4): (77.85, 559854080), ("panel", 8): (83.94, 321771264),
+                   ("panel", 16): (85.1, 252550144), ("serpentine", 4): (80.51, 426306816),
+                   ("serpentine", 8): (82.17, 359916544), ("serpentine", 16): (83.81, 305609472)}},
 }
 
 
@@ -565,7 +590,7 @@ def run_swz(args):
         achieved = flops / statistics.mean(ms) / 1e9
         # the captured launch is the default workload's headline launch only
         rec = ncu_record(args.workload)
-        traffic = (rec["traffic_bytes"] if rec and persistent
+        traffic = (rec["traffic_bytes"] if rec and "traffic_bytes" in rec and persistent
                    and bool(args.stream_k) == rec["source"].get("stream_k", False)
                    and (head_order, head_group) == rec["traffic_order"] else None)
         line.update({
