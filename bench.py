@@ -56,7 +56,7 @@ WORKLOADS = {
                           sweep=_ALL + [("serpentine", 2)]),
     "gemm4096_fp16_pair": dict(M=4096, N=4096, K=4096, dtype="fp16", dist="uniform",
                                cfg=dict(cta_pair=True), tile=(128, 256), cluster_m=2,
-                               sweep=_ALL),
+                               sweep=_ALL + [("serpentine", 2)]),
     "gemm6144x10240x4096_fp16": dict(M=6144, N=10240, K=4096, dtype="fp16", dist="uniform",
                                      cfg=dict(tile_n=128), tile=(128, 128), cluster_m=1,
                                      sweep=[("row", 1), ("col", 1), ("panel", 4), ("panel", 8),
@@ -84,6 +84,7 @@ _G = (2, 4, 8, 16)
 CONFIG_SWEEPS = [
     ("cfg1_1024x1024x512_fp16", "gemm1024x1024x512_fp16", (True,)),
     ("cfg2_4096_fp16_tile128x256", "gemm4096_fp16", (True, False)),
+    ("cfg2_4096_fp16_tile128x256_pair", "gemm4096_fp16_pair", (True, False)),
     ("cfg4_6144x10240x4096_fp16_tile128x128", "gemm6144x10240x4096_fp16_pair", (True,)),
 ]
 CONFIG_ORDERS = {
@@ -92,6 +93,9 @@ CONFIG_ORDERS = {
     "cfg2_4096_fp16_tile128x256": ([("row", 1), ("col", 1)] + [("panel", g) for g in _G]
                                    + [("serpentine", g) for g in _G]
                                    + [("morton", 1), ("xor", 1)]),
+    "cfg2_4096_fp16_tile128x256_pair": ([("row", 1), ("col", 1)] + [("panel", g) for g in _G]
+                                        + [("serpentine", g) for g in _G]
+                                        + [("morton", 1), ("xor", 1)]),
     "cfg4_6144x10240x4096_fp16_tile128x128": ([("row", 1), ("col", 1)]
                                               + [("panel", g) for g in (4, 8, 16)]
                                               + [("serpentine", g) for g in (4, 8, 16)]),

@@ -155,6 +155,8 @@ def test_config_sweeps_cover_the_specification():
     o4 = bench.CONFIG_ORDERS["cfg4_6144x10240x4096_fp16_tile128x128"]
     assert not {o for o, _ in o4} & {"morton", "xor"}  # not bijective on 48 x 80
     assert len(bench.CONFIG_ORDERS["cfg1_1024x1024x512_fp16"]) == 6
+    # configuration 2's tile grid runs as single CTAs and as CTA pairs
+    assert set(bench.CONFIG_ORDERS["cfg2_4096_fp16_tile128x256_pair"]) == set(o2)
     assert dict((k, m) for k, _, m in bench.CONFIG_SWEEPS)["cfg2_4096_fp16_tile128x256"] == (
         True, False)
     # the capture mode (--only sweep) of each workload covers the same orders
