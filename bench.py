@@ -33,6 +33,7 @@ import datetime
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -105,11 +106,12 @@ CONFIG_ORDERS = {
 # (`--only sweep`: the L2 hit rate lts__t_sector_hit_rate.pct and
 # dram__bytes_read.sum) and the DRAM traffic (read + write) of the headline
 # launch.  They are counters of a capture, not of this run, and hold only
-# for the gemm.cu source they were taken on (SHA-256 prefix); for any
-# other source they are left out of the line.
+# for the gemm.cu code they were taken on (code_hash: the SHA-256 prefix of
+# the source without comments and whitespace); for any other code they are
+# left out of the line.
 NCU = {
     "gemm8192_bf16_pair": {
-        "source": {"gemm_cu_sha256": "096ad46accffb076", "captured": "2026-12-02",
+        "source": {"gemm_cu_code_hash": "5f97b234cf879676", "captured": "2026-12-02",
                    "kernel": "gemm_kernel<256, 1, 0, 128, 0>", "stream_k": True,
                    "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum,"
                               "dram__bytes_write.sum --clock-control none -k regex:gemm_kernel "
@@ -124,7 +126,7 @@ NCU = {
                    ("serpentine", 16): (68.18, 1291457280), ("morton", 1): (67.04, 1387209984),
                    ("xor", 1): (64.04, 2061828608)}},
     "gemm4096_fp16": {
-        "source": {"gemm_cu_sha256": "096ad46accffb076", "captured": "2026-12-02",
+        "source": {"gemm_cu_code_hash": "5f97b234cf879676", "captured": "2026-12-02",
                    "kernel": "gemm_kernel<256, 0, 0, 128, 0>", "stream_k": True,
                    "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum "
                               "--clock-control none -k regex:gemm_kernel -s 12 -c 12 python "
@@ -136,7 +138,7 @@ NCU = {
                    ("serpentine", 16): (79.73, 87741440), ("morton", 1): (73.27, 111463168),
                    ("xor", 1): (76.17, 109999104), ("serpentine", 2): (75.41, 96200448)}},
     "gemm6144x10240x4096_fp16_pair": {
-        "source": {"gemm_cu_sha256": "096ad46accffb076", "captured": "2026-12-02",
+        "source": {"gemm_cu_code_hash": "5f97b234cf879676", "captured": "2026-12-02",
                    "kernel": "gemm_kernel<128, 1, 0, 128, 0>", "stream_k": True,
                    "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum "
                               "--clock-control none -k regex:gemm_kernel -s 8 -c 8 python "
@@ -149,16 +151,52 @@ NCU = {
 }
 
 
+def code_hash(text):
+    """SHA-256 prefix of C++ source text with its comments and whitespace
+    removed: two sources that differ only in comments or layout share it."""
+    parts, code, i, n = [], [], 0, len(text)
+
+    def flush():
+        parts.append(re.sub(r"\s+", " ", "".join(code)))
+        code.clear()
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # string or character literal, kept whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            flush()
+            parts.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            i = text.find("\n", i)
+            i = n if i < 0 else i
+            code.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            code.append(" ")
+        else:
+            code.append(c)
+            i += 1
+    flush()
+    joined = "".join(parts).strip()
+    # spaces next to punctuation carry no meaning either
+    joined = re.sub(r" ?([{}()\[\];,]) ?", r"\1", joined)
+    return hashlib.sha256(joined.encode()).hexdigest()[:16]
+
+
 def _gemm_src_hash():
-    with open(os.path.join(ROOT, "thread_block_smem_gb300", "csrc", "gemm.cu"), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """The code hash of csrc/gemm.cu (ncu figures hold for one kernel code)."""
+    with open(os.path.join(ROOT, "thread_block_smem_gb300", "csrc", "gemm.cu")) as f:
+        return code_hash(f.read())
 
 
 def ncu_record(workload):
     """The recorded ncu figures of `workload` if they were taken on the
     current gemm.cu source, else None."""
     rec = NCU.get(workload)
-    if rec is None or rec["source"]["gemm_cu_sha256"] != _gemm_src_hash():
+    if rec is None or rec["source"]["gemm_cu_code_hash"] != _gemm_src_hash():
         return None
     return rec
 

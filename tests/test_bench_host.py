@@ -162,3 +162,15 @@ def test_config_sweeps_cover_the_specification():
     # the capture mode (--only sweep) of each workload covers the same orders
     for key, wname, _ in bench.CONFIG_SWEEPS:
         assert set(bench.WORKLOADS[wname]["sweep"]) == set(bench.CONFIG_ORDERS[key]), key
+
+
+def test_code_hash_ignores_comments_and_layout_only():
+    # the ncu records are keyed on the kernel's code, not on its comments
+    a = 'int f(int x) {  // doubles\n  return 2 * x; /* twice */ }\nconst char* s = "// kept";'
+    b = 'int f(int x) {\n    return 2 * x;\n}\nconst char* s = "// kept";'
+    assert bench.code_hash(a) == bench.code_hash(b)
+    assert bench.code_hash(a) != bench.code_hash(a.replace("2 * x", "3 * x"))
+    assert bench.code_hash(a) != bench.code_hash(a.replace('"// kept"', '"/ kept"'))
+    # the records in the bench are keyed this way
+    for rec in bench.NCU.values():
+        assert len(rec["source"]["gemm_cu_code_hash"]) == 16

@@ -32,9 +32,11 @@
 //     Each CTA loads its own 128 rows of A and its half of B's columns;
 //     the leader issues the MMAs and its commits are multicast to both CTAs.
 //   * Work items come from the static schedule (Schedule: work_idx striding,
-//     optional Stream-K tail) or, with DYN, from an atomic counter published
-//     one item ahead to all roles through a shared-memory ring.  A Stream-K tile's owner streams its peers' partial sums into a
-//     ring of slots in its idle operand stages with bulk copies.
+//     optional Stream-K tail, optional split of the units between the two
+//     dies) or, with DYN, from an atomic counter published one item ahead to
+//     all roles through a shared-memory ring.  The pieces of a Stream-K tail
+//     come first; their partial sums are published to a workspace and
+//     reduced by the tiles' participants while the whole tiles run.
 //   * Every wait is bounded (globaltimer); on expiry the kernel records
 //     SWZ_ETIMEOUT in a device status word, drains what it issued, frees TMEM
 //     and returns.
