@@ -111,43 +111,41 @@ CONFIG_ORDERS = {
 # left out of the line.
 NCU = {
     "gemm8192_bf16_pair": {
-        "source": {"gemm_cu_code_hash": "5f97b234cf879676", "captured": "2026-12-02",
+        "source": {"gemm_cu_code_hash": "d4e7cd45bec4295c", "captured": "2026-12-02",
                    "kernel": "gemm_kernel<256, 1, 0, 128, 0>", "stream_k": True,
-                   "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum,"
-                              "dram__bytes_write.sum --clock-control none -k regex:gemm_kernel "
-                              "-s 10 -c 10 python bench.py --only sweep --no-cpu; traffic: ncu "
-                              "--set full -k regex:gemm_kernel -s 3 -c 1 python bench.py --only "
-                              "gemm --steps 1 --warmup 3 --no-cpu"},
-        "traffic_bytes": 1067531008 + 277865472, "traffic_order": ("serpentine", 8),
-        "orders": {("row", 1): (62.92, 2059461120), ("col", 1): (61.23, 2063038464),
-                   ("panel", 4): (69.3, 1434872320), ("panel", 8): (71.85, 1117402880),
-                   ("panel", 16): (68.19, 1321885952), ("serpentine", 4): (69.35, 1280536576),
-                   ("serpentine", 8): (73.31, 1067172352),
-                   ("serpentine", 16): (68.18, 1291457280), ("morton", 1): (67.04, 1387209984),
-                   ("xor", 1): (64.04, 2061828608)}},
+                   "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum --clock-control none "
+                              "-k regex:gemm_kernel -s 10 -c 10 python bench.py --workload gemm8192_bf16_pair "
+                              "--only sweep --no-cpu; traffic: ncu --set full -k regex:gemm_kernel -s 3 -c 1 "
+                              "python bench.py --only gemm --steps 1 --warmup 3 --no-cpu"},
+        "traffic_bytes": 1048829696 + 277200128, "traffic_order": ("serpentine", 8),
+        "orders": {("row", 1): (63.58, 2057126144), ("col", 1): (62.98, 2060891392),
+                   ("panel", 4): (70.07, 1432582144), ("panel", 8): (72.95, 1097583104),
+                   ("panel", 16): (69.75, 1307718912), ("serpentine", 4): (69.93, 1276448512),
+                   ("serpentine", 8): (74.06, 1049195264),
+                   ("serpentine", 16): (69.46, 1267827968), ("morton", 1): (71.16, 1381846016),
+                   ("xor", 1): (63.98, 2059494912)}},
     "gemm4096_fp16": {
-        "source": {"gemm_cu_code_hash": "5f97b234cf879676", "captured": "2026-12-02",
+        "source": {"gemm_cu_code_hash": "d4e7cd45bec4295c", "captured": "2026-12-02",
                    "kernel": "gemm_kernel<256, 0, 0, 128, 0>", "stream_k": True,
-                   "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum "
-                              "--clock-control none -k regex:gemm_kernel -s 12 -c 12 python "
-                              "bench.py --workload gemm4096_fp16 --only sweep --no-cpu"},
-        "orders": {("row", 1): (80.88, 87051008), ("col", 1): (74.59, 94524672),
-                   ("panel", 2): (79.88, 91400448), ("panel", 4): (80.43, 97858304),
-                   ("panel", 8): (76.39, 96978944), ("panel", 16): (75.2, 110340608),
-                   ("serpentine", 4): (78.73, 96502272), ("serpentine", 8): (77.4, 99362048),
-                   ("serpentine", 16): (79.73, 87741440), ("morton", 1): (73.27, 111463168),
-                   ("xor", 1): (76.17, 109999104), ("serpentine", 2): (75.41, 96200448)}},
+                   "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum --clock-control none "
+                              "-k regex:gemm_kernel -s 12 -c 12 python bench.py --workload gemm4096_fp16 "
+                              "--only sweep --no-cpu"},
+        "orders": {("row", 1): (82.59, 80590336), ("col", 1): (77.05, 85499392),
+                   ("panel", 2): (80.86, 83067648), ("panel", 4): (79.5, 87556352),
+                   ("panel", 8): (78.96, 90414848), ("panel", 16): (76.3, 104478208),
+                   ("serpentine", 4): (80.36, 91335936), ("serpentine", 8): (79.14, 95404288),
+                   ("serpentine", 16): (82.13, 80965888), ("morton", 1): (73.73, 103136256),
+                   ("xor", 1): (74.64, 104296960), ("serpentine", 2): (77.61, 89719552)}},
     "gemm6144x10240x4096_fp16_pair": {
-        "source": {"gemm_cu_code_hash": "5f97b234cf879676", "captured": "2026-12-02",
+        "source": {"gemm_cu_code_hash": "d4e7cd45bec4295c", "captured": "2026-12-02",
                    "kernel": "gemm_kernel<128, 1, 0, 128, 0>", "stream_k": True,
-                   "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum "
-                              "--clock-control none -k regex:gemm_kernel -s 8 -c 8 python "
-                              "bench.py --workload gemm6144x10240x4096_fp16_pair --only sweep "
-                              "--no-cpu"},
-        "orders": {("row", 1): (67.3, 1091503616), ("col", 1): (82.36, 289594368),
-                   ("panel", 4): (77.85, 559854080), ("panel", 8): (83.94, 321771264),
-                   ("panel", 16): (85.1, 252550144), ("serpentine", 4): (80.51, 426306816),
-                   ("serpentine", 8): (82.17, 359916544), ("serpentine", 16): (83.81, 305609472)}},
+                   "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum --clock-control none "
+                              "-k regex:gemm_kernel -s 8 -c 8 python bench.py --workload gemm6144x10240x4096_fp16_pair "
+                              "--only sweep --no-cpu"},
+        "orders": {("row", 1): (69.47, 1007622400), ("col", 1): (83.03, 242816256),
+                   ("panel", 4): (78.88, 559004928), ("panel", 8): (82.27, 320462336),
+                   ("panel", 16): (85.6, 245413632), ("serpentine", 4): (81.76, 375097344),
+                   ("serpentine", 8): (82.69, 333279232), ("serpentine", 16): (82.45, 293577984)}},
 }
 
 

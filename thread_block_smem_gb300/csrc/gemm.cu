@@ -530,6 +530,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       bool skip = (p.debug_flags & SWZ_DEBUG_SKIP_FIRST_LOAD) != 0;
+      // operand tiles are read again by other CTAs from L2: kept longer than
+      // the C lines the epilogues write (+1 to +2 % where A and B fit in L2)
+      const uint64_t pol = ptx::l2_policy_evict_last();
       uint32_t w, kbeg, kend;
       int kind;
       // Swizzle span sw: a stage's 128-byte rows are split into 128/sw
@@ -576,58 +579,58 @@ __global__ void __launch_bounds__(kThreads, 1)
               if constexpr (PAIR) {
 #pragma unroll
                 for (int g = 0; g < KA; ++g)
-                  ptx::tma_load_2d_pair(a_dst + g * (BM * 128), &tmA, fb, k0 + g * ke, m0);
+                  ptx::tma_load_2d_pair(a_dst + g * (BM * 128), &tmA, fb, k0 + g * ke, m0, pol);
                 if (p.b_kmajor)
 #pragma unroll
                   for (int g = 0; g < KA; ++g)
-                    ptx::tma_load_2d_pair(b_dst + g * local * 128, &tmB, fb, k0 + g * ke, n0);
+                    ptx::tma_load_2d_pair(b_dst + g * local * 128, &tmB, fb, k0 + g * ke, n0, pol);
                 else if (one_box)
-                  ptx::tma_load_3d_pair(b_dst, &tmB3, fb, 0, k0, n0 / 64);
+                  ptx::tma_load_3d_pair(b_dst, &tmB3, fb, 0, k0, n0 / 64, pol);
                 else
                   for (int j = 0; j < boxes; ++j)
-                    ptx::tma_load_2d_pair(b_dst + j * (BK * KA * 128), &tmB, fb, n0 + 64 * j, k0);
+                    ptx::tma_load_2d_pair(b_dst + j * (BK * KA * 128), &tmB, fb, n0 + 64 * j, k0, pol);
               } else {
 #pragma unroll
                 for (int g = 0; g < KA; ++g)
-                  ptx::tma_load_2d(a_dst + g * (BM * 128), &tmA, fb, k0 + g * ke, m0);
+                  ptx::tma_load_2d(a_dst + g * (BM * 128), &tmA, fb, k0 + g * ke, m0, pol);
                 if (p.b_kmajor)
 #pragma unroll
                   for (int g = 0; g < KA; ++g)
-                    ptx::tma_load_2d(b_dst + g * local * 128, &tmB, fb, k0 + g * ke, n0);
+                    ptx::tma_load_2d(b_dst + g * local * 128, &tmB, fb, k0 + g * ke, n0, pol);
                 else if (one_box)
-                  ptx::tma_load_3d(b_dst, &tmB3, fb, 0, k0, n0 / 64);
+                  ptx::tma_load_3d(b_dst, &tmB3, fb, 0, k0, n0 / 64, pol);
                 else
                   for (int j = 0; j < boxes; ++j)
-                    ptx::tma_load_2d(b_dst + j * (BK * KA * 128), &tmB, fb, n0 + 64 * j, k0);
+                    ptx::tma_load_2d(b_dst + j * (BK * KA * 128), &tmB, fb, n0 + 64 * j, k0, pol);
               }
             } else if constexpr (PAIR) {
               if (p.a3d)
-                ptx::tma_load_3d_pair(a_dst, &tmA3, fb, 0, m0, k0 / xe);
+                ptx::tma_load_3d_pair(a_dst, &tmA3, fb, 0, m0, k0 / xe, pol);
               else
                 for (int g = 0; g < groups; ++g)
-                  ptx::tma_load_2d_pair(a_dst + g * BM * sw, &tmA, fb, k0 + g * xe, m0);
+                  ptx::tma_load_2d_pair(a_dst + g * BM * sw, &tmA, fb, k0 + g * xe, m0, pol);
               if (p.b_kmajor)
                 for (int g = 0; g < groups; ++g)
-                  ptx::tma_load_2d_pair(b_dst + g * local * sw, &tmB, fb, k0 + g * xe, n0);
+                  ptx::tma_load_2d_pair(b_dst + g * local * sw, &tmB, fb, k0 + g * xe, n0, pol);
               else if (one_box)
-                ptx::tma_load_3d_pair(b_dst, &tmB3, fb, 0, k0, n0 / xn);
+                ptx::tma_load_3d_pair(b_dst, &tmB3, fb, 0, k0, n0 / xn, pol);
               else
                 for (int j = 0; j < boxes; ++j)
-                  ptx::tma_load_2d_pair(b_dst + j * b_box_bytes, &tmB, fb, n0 + xn * j, k0);
+                  ptx::tma_load_2d_pair(b_dst + j * b_box_bytes, &tmB, fb, n0 + xn * j, k0, pol);
             } else {
               if (p.a3d)
-                ptx::tma_load_3d(a_dst, &tmA3, fb, 0, m0, k0 / xe);
+                ptx::tma_load_3d(a_dst, &tmA3, fb, 0, m0, k0 / xe, pol);
               else
                 for (int g = 0; g < groups; ++g)
-                  ptx::tma_load_2d(a_dst + g * BM * sw, &tmA, fb, k0 + g * xe, m0);
+                  ptx::tma_load_2d(a_dst + g * BM * sw, &tmA, fb, k0 + g * xe, m0, pol);
               if (p.b_kmajor)
                 for (int g = 0; g < groups; ++g)
-                  ptx::tma_load_2d(b_dst + g * local * sw, &tmB, fb, k0 + g * xe, n0);
+                  ptx::tma_load_2d(b_dst + g * local * sw, &tmB, fb, k0 + g * xe, n0, pol);
               else if (one_box)
-                ptx::tma_load_3d(b_dst, &tmB3, fb, 0, k0, n0 / xn);
+                ptx::tma_load_3d(b_dst, &tmB3, fb, 0, k0, n0 / xn, pol);
               else
                 for (int j = 0; j < boxes; ++j)
-                  ptx::tma_load_2d(b_dst + j * b_box_bytes, &tmB, fb, n0 + xn * j, k0);
+                  ptx::tma_load_2d(b_dst + j * b_box_bytes, &tmB, fb, n0 + xn * j, k0, pol);
             }
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -763,6 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kind;
     const uint32_t stg_warp = sStg + (warp - 2u) * 2u * K_::STG_BOX_BYTES;
     uint32_t nstored = 0;  // chunks stored so far (they alternate between two boxes)
+    const uint64_t cpol = ptx::l2_policy_evict_first();  // C is written once
     // One 32 x 32 chunk: registers -> staging box (row r at r*128 bytes, its
     // 16-byte piece j at slot j ^ (r mod 8): the 8 lanes of each 16-byte
     // phase hit 8 different bank groups) -> TMA store at C (col, row), parts
@@ -783,7 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        ptx::tma_store_2d(&tmC, box, col, row);
+        ptx::tma_store_2d(&tmC, box, col, row, cpol);
         ptx::bulk_commit_group();
       }
     };
