@@ -10,8 +10,9 @@ events on the launching stream.
 Also reported on the same JSON line:
   sweep        every order of the headline configuration: TFLOP/s, fraction
                of the measured peak, the offline L2 model's hit rate and DRAM
-               bytes (the first page's model and the two-die reading), and
-               the ncu figures recorded for this kernel source
+               bytes (the first page's model, and the two-die reading run on
+               the kernel's own K order: odd waves descending in persistent
+               launches), and the ncu figures recorded for this kernel source
   configs      the same sweep for the specification's other configurations:
                1024x1024x512 fp16, 4096^3 fp16 (1-CTA 128 x 256 tiles,
                persistent and one CTA per tile), 6144x10240x4096 fp16
@@ -474,11 +475,12 @@ def run_swz(args):
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in ev]
 
-    def model(order, g, w, conc, parts):
+    def model(order, g, w, conc, parts, k_alternate=False):
         """The offline L2 model at the kernel's tiling: hit % and DRAM bytes."""
         tk = 128 if w["tile"][1] == 128 else 64  # K per stage: two atoms for 128-wide tiles
         return swz.l2_model_predict(order, g, w["M"], w["N"], w["K"], w["tile"][0], w["tile"][1],
-                                    tk, 2, model_l2, conc, w["cluster_m"], l2_partitions=parts)
+                                    tk, 2, model_l2, conc, w["cluster_m"], l2_partitions=parts,
+                                    k_alternate=k_alternate)
 
     model_l2 = int(args.l2_cache_mb * 2**20) if args.l2_cache_mb else l2_bytes
 
@@ -517,7 +519,9 @@ def run_swz(args):
                 continue
             med = statistics.median(t)
             hit, dram = model(order, g, w, conc, 1)
-            hit2, dram2 = model(order, g, w, conc, 2)
+            # the two-die reading on the K order the kernel runs: in a
+            # persistent launch every other wave takes K descending
+            hit2, dram2 = model(order, g, w, conc, 2, k_alternate=persist)
             o = {"order": order, "group": g, "ms": med, "tflops": wf / med / 1e9,
                  "frac_of_peak": wf / med / 1e9 / peaks["bf16_tflops"],
                  "l2_model_hit_pct": hit, "l2_model_dram_read_bytes": dram,
@@ -547,6 +551,49 @@ def run_swz(args):
             res["l2_model_2die_dram_abs_err_max"] = max(abs(o["l2_model_2die_dram_err"])
                                                         for o in meas)
         return res
+
+    def back_to_back(w, order, g, calls=50, reps=7):
+        """Device time per call of `calls` GEMMs of workload `w` recorded in one
+        CUDA graph and replayed back to back (each kernel starts its prologue
+        while the previous one finishes: programmatic dependent launch).  L2
+        is flushed before each replay; the operands stay in L2 after the
+        first call."""
+        bM, bN, bK = w["M"], w["N"], w["K"]
+        bA, bB = si.gemm_inputs(bM, bN, bK, w["dtype"], w["dist"], seed=0)
+        bA, bB = bA.to(dev), bB.to(dev)
+        bC = torch.empty((bM, bN), dtype=torch.float32, device=dev)
+
+        def run():
+            for _ in range(calls):
+                swz.gemm(bA, bB, order, g, True, out=bC, **w["cfg"])
+
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            run()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run()
+        graph.replay()
+        torch.cuda.synchronize()
+        per = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            per.append(e0.elapsed_time(e1) / 1e3 / calls)
+        del graph, bA, bB, bC
+        t = statistics.median(per)
+        return {"order": order, "group": g, "calls": calls, "persistent": True,
+                "device_us_per_call": t * 1e6, "tflops": 2.0 * bM * bN * bK / t / 1e12,
+                "how": "one CUDA graph of back-to-back calls, CUDA events around each "
+                       "replay; L2 flushed before each replay"}
 
     sampler = ClockSampler(local)
     ms = None
@@ -588,6 +635,8 @@ def run_swz(args):
                                                                "m": 0, "n": 0, "k": 0}))
                     cf[key] = {("persistent" if p else "non_persistent"): sweep(wname, w, p, 5, 3)
                                for p in modes}
+                    if key.startswith("cfg1"):
+                        cf[key]["back_to_back"] = back_to_back(w, "row", 1)
                 line["configs"] = cf
         # ---- operand-stage swizzle span (TMA + tensor-core layout) ---------
         spans = []

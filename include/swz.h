@@ -116,6 +116,17 @@ int swz_is_bijective(int order, int grid_m, int grid_n, int group);
  * CTA b takes tile ids b, b + P, b + 2P, ... ([TBS] persistent loop, [CPS]
  * work_idx striding).  Ragged M, N, K are handled (TMA zero-fill on loads,
  * clipped stores).  K = 0 writes zeros; M = 0 or N = 0 is a no-op.
+ * Summation order: a tile's K blocks are accumulated in ascending order,
+ * except that in a persistent launch the whole tiles of every other wave
+ * (tile id / P odd, P = programs, or clusters with cta_pair) take them in
+ * descending order, so that each wave starts on the operand slices the
+ * previous wave read last (fewer DRAM reads).  The order depends on the
+ * tile id and P only: results are deterministic, equal for the static and
+ * dynamic schedulers and the die split, and between launches with another
+ * P agree up to FP32 rounding order.
+ * Launches allow programmatic dependent launch: the kernel may start while
+ * the previous kernel of `stream` finishes, and touches no global memory
+ * before that kernel has completed.
  * Requirements: A, B 16-byte aligned; C 16-byte aligned; rows of A (and of
  * B in either layout) a multiple of 16 bytes (K % 8 == 0 for fp16/bf16,
  * K % 4 == 0 for TF32; N % 8 == 0 for B as K x N); N % 4 == 0; M, N, K <
@@ -354,12 +365,15 @@ int swz_l2_model(int order, int group, int M, int N, int K, int tile_m, int tile
  * read by SMs of every die and each half keeps its own copy: each half
  * replays the whole trace with l2_bytes / p of capacity, and the counts are
  * those of one half.  This is a reading of the hardware, not the page's
- * model.  Errors: SWZ_EINVAL (as swz_l2_model, l2_partitions < 1, or
- * h_miss_bytes NULL). */
+ * model.  k_alternate = 1 replays the K order of swz_gemm's persistent
+ * launches instead of the page's: the tiles of odd waves take the K steps
+ * from the last to the first (0: every wave ascending, the page's model).
+ * Errors: SWZ_EINVAL (as swz_l2_model, l2_partitions < 1, k_alternate not 0
+ * or 1, or h_miss_bytes NULL). */
 int swz_l2_model_bytes(int order, int group, int M, int N, int K, int tile_m, int tile_n,
                        int tile_k, int elem_bytes, int64_t l2_bytes, int l2_partitions,
-                       int concurrency, int cluster_m, int64_t* h_hits, int64_t* h_misses,
-                       int64_t* h_miss_bytes);
+                       int k_alternate, int concurrency, int cluster_m, int64_t* h_hits,
+                       int64_t* h_misses, int64_t* h_miss_bytes);
 
 /*
  * swz_gemm_streamk_noalloc -- Stream-K GEMM for callers that cannot allocate

@@ -15,6 +15,11 @@ The model, restated:
     each tile of the wave (in id order) touches its A tile (m, k) and then its
     B tile (k, n).
   * Hit rate = hits / (hits + misses), in percent.
+
+``simulate(..., k_alternate=True)`` is not the page's model but the K order
+of the library's persistent GEMM: the tiles of every other wave (waves 1, 3,
+5, ...) step through K from the last step to the first, the others from the
+first to the last.  Everything else is the page's model.
 """
 from __future__ import annotations
 
@@ -56,13 +61,15 @@ class ByteLRU:
 
 
 def simulate(tiles, grid_k, a_tile_bytes, b_tile_bytes, capacity_bytes,
-             concurrency):
+             concurrency, k_alternate=False):
     """Replay the wave trace of ``tiles`` (a list of (m, n) in program-id
-    order) through a ByteLRU.  Returns the cache (hits, misses inside)."""
+    order) through a ByteLRU.  Returns the cache (hits, misses inside).
+    ``k_alternate``: odd waves take the K steps in descending order."""
     cache = ByteLRU(capacity_bytes)
     for w0 in range(0, len(tiles), concurrency):
         wave = tiles[w0:w0 + concurrency]
-        for k in range(grid_k):
+        descending = k_alternate and (w0 // concurrency) % 2 == 1
+        for k in (range(grid_k - 1, -1, -1) if descending else range(grid_k)):
             for m, n in wave:
                 cache.touch(("A", m, k), a_tile_bytes)
                 cache.touch(("B", k, n), b_tile_bytes)

@@ -46,9 +46,12 @@ def test_host_pipeline_8192(swz):
     ii, jj = si.sample_indices(8192, 8192, 128, 256, 1, seed=5)
     mx, rel = errors(C.numpy()[ii, jj], ref.gemm_entries_f64(A, B, ii, jj))
     assert mx <= MAX_ABS and rel <= REL_FRO
-    # same bits as the device-resident call on each slab's rows
+    # against the device-resident call: a slab launch is a launch of its own,
+    # whose waves (and so the K direction of each tile) differ, so the two
+    # agree within the GEMM tolerance rather than bit for bit
     D = swz.gemm(A.cuda(), B.cuda(), "panel", 8, True, cta_pair=True)
-    assert (D.cpu() - C).abs().max().item() <= 1e-3
+    mx, rel = errors(C.numpy(), D.cpu().numpy())
+    assert mx <= MAX_ABS and rel <= REL_FRO
 
 
 def test_host_pipeline_degenerate(swz):

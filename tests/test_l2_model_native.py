@@ -17,12 +17,12 @@ def swz():
     return m
 
 
-def _oracle_counts(order, group, M, N, K, tm, tn, tk, eb, l2b, conc, cm):
+def _oracle_counts(order, group, M, N, K, tm, tn, tk, eb, l2b, conc, cm, k_alternate=False):
     gm = cm * math.ceil(M / (tm * cm))
     gn = math.ceil(N / tn)
     gk = math.ceil(K / tk)
     seq = l2.cta_tiles_of_clusters(order, gm, gn, group, cm)
-    c = l2.simulate(seq, gk, tm * tk * eb, tk * tn * eb, l2b, conc)
+    c = l2.simulate(seq, gk, tm * tk * eb, tk * tn * eb, l2b, conc, k_alternate)
     return c.hits, c.misses, c.miss_bytes
 
 
@@ -62,6 +62,17 @@ def test_partitioned_model_is_the_oracle_at_a_fraction_of_the_capacity(swz, case
     assert (h, m, b) == _oracle_counts(*c)
 
 
+@pytest.mark.parametrize("parts", [1, 2])
+@pytest.mark.parametrize("case", CASES)
+def test_k_alternate_matches_oracle(swz, case, parts):
+    # the persistent GEMM's K order: odd waves descending
+    rc, h, m, b = swz.swz_l2_model_bytes(*case, l2_partitions=parts, k_alternate=1)
+    assert rc == 0
+    c = list(case)
+    c[9] = case[9] // parts
+    assert (h, m, b) == _oracle_counts(*c, k_alternate=True)
+
+
 @pytest.mark.slow
 def test_native_model_reproduces_printed_rates(swz):
     rows = [ln for ln in read_lines("tbs_l2_model_8192.txt") if ln[0] not in ("config", "spearman")]
@@ -88,3 +99,5 @@ def test_native_model_rejects_bad_args(swz):
     assert swz.swz_l2_model(to.ROW, 1, 64, 64, 64, 16, 16, 16, 2, 1024, 0, 1)[0] == swz.SWZ_EINVAL
     assert swz.swz_l2_model_bytes(to.ROW, 1, 64, 64, 64, 16, 16, 16, 2, 1024, 4, 1,
                                   l2_partitions=0)[0] == swz.SWZ_EINVAL
+    assert swz.swz_l2_model_bytes(to.ROW, 1, 64, 64, 64, 16, 16, 16, 2, 1024, 4, 1,
+                                  k_alternate=2)[0] == swz.SWZ_EINVAL

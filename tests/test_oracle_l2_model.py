@@ -87,3 +87,44 @@ def test_cluster_cta_sequence():
     # cluster grid 2 x 3 walked group-major with G=2 (= col-major here)
     assert seq[:6] == [(0, 0), (1, 0), (2, 0), (3, 0), (0, 1), (1, 1)]
     assert sorted(seq) == [(m, n) for m in range(4) for n in range(3)]
+
+
+def test_k_alternate_by_hand():
+    # two waves of one tile each, (0, 0) then (0, 1), four K steps, a cache
+    # of two 1-byte tiles.  Ascending in both waves, the second wave finds
+    # nothing: 16 misses.  With the second wave descending it starts on
+    # A(0, 3), the line the first wave touched last but one: a hit; then
+    # B(3, 1) evicts B(3, 0), A(0, 2) evicts A(0, 3), and everything else
+    # misses: 1 hit, 15 misses.
+    tiles = [(0, 0), (0, 1)]
+    up = l2.simulate(tiles, 4, 1, 1, 2, concurrency=1)
+    assert (up.hits, up.misses) == (0, 16)
+    alt = l2.simulate(tiles, 4, 1, 1, 2, concurrency=1, k_alternate=True)
+    assert (alt.hits, alt.misses) == (1, 15)
+
+
+def test_k_alternate_leaves_first_wave_and_compulsory_misses():
+    tiles = to.tile_sequence(to.SERPENTINE, 6, 7, 2)
+    # one wave: nothing descends
+    a = l2.simulate(tiles, 5, 100, 300, 4000, concurrency=len(tiles))
+    b = l2.simulate(tiles, 5, 100, 300, 4000, concurrency=len(tiles), k_alternate=True)
+    assert (a.hits, a.misses) == (b.hits, b.misses)
+    # an unbounded cache: still only the compulsory misses
+    c = l2.simulate(tiles, 5, 100, 300, 10**12, concurrency=4, k_alternate=True)
+    assert c.misses == 6 * 5 + 7 * 5
+    # one K step: the direction does not matter
+    d = l2.simulate(tiles, 1, 100, 300, 500, concurrency=4)
+    e = l2.simulate(tiles, 1, 100, 300, 500, concurrency=4, k_alternate=True)
+    assert (d.hits, d.misses) == (e.hits, e.misses)
+
+
+def test_k_alternate_reuses_across_waves():
+    # row order, one row of 8 tiles in waves of 2: the A tiles of row 0 are
+    # shared by every wave; with the K direction alternating, each wave
+    # starts on the A tile the previous wave touched last and hits it
+    tiles = to.tile_sequence(to.ROW, 1, 8)
+    gk, cap = 6, 3
+    up = l2.simulate(tiles, gk, 1, 1, cap, concurrency=2)
+    alt = l2.simulate(tiles, gk, 1, 1, cap, concurrency=2, k_alternate=True)
+    assert up.hits == 4 * gk  # within a wave only: the second tile's A
+    assert alt.hits == up.hits + 3  # plus one A tile at each of 3 wave boundaries

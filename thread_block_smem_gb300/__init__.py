@@ -83,7 +83,7 @@ def lib() -> ctypes.CDLL:
         L.swz_device_info.argtypes = [ip, ip, ip, ip]
         i64p = ctypes.POINTER(ctypes.c_int64)
         L.swz_l2_model.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.c_int64, i, i, i64p, i64p]
-        L.swz_l2_model_bytes.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.c_int64, i, i, i,
+        L.swz_l2_model_bytes.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.c_int64, i, i, i, i,
                                          i64p, i64p, i64p]
         L.swz_gemm_workspace_size.argtypes = [i, i, i, i, ctypes.POINTER(swz_gemm_opts),
                                               ctypes.POINTER(ctypes.c_uint64)]
@@ -275,22 +275,24 @@ def swz_l2_model(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_b
 
 
 def swz_l2_model_bytes(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_bytes,
-                       concurrency, cluster_m=1, l2_partitions=1):
+                       concurrency, cluster_m=1, l2_partitions=1, k_alternate=0):
     h, m, b = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
     rc = lib().swz_l2_model_bytes(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes,
-                                  l2_bytes, l2_partitions, concurrency, cluster_m,
-                                  ctypes.byref(h), ctypes.byref(m), ctypes.byref(b))
+                                  l2_bytes, l2_partitions, int(k_alternate), concurrency,
+                                  cluster_m, ctypes.byref(h), ctypes.byref(m), ctypes.byref(b))
     return rc, h.value, m.value, b.value
 
 
 def l2_model_predict(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_bytes,
-                     concurrency, cluster_m=1, l2_partitions=1):
+                     concurrency, cluster_m=1, l2_partitions=1, k_alternate=False):
     """(predicted L2 hit rate in percent, predicted operand DRAM bytes);
     ``l2_partitions`` = 2 is the two-die reading (each half of the L2 keeps
-    its own copy of the whole trace), 1 the first page's model."""
+    its own copy of the whole trace), 1 the first page's model;
+    ``k_alternate`` replays the K order of the persistent GEMM (odd waves
+    descending) instead of the page's ascending one."""
     rc, h, m, b = swz_l2_model_bytes(_order(order), group, M, N, K, tile_m, tile_n, tile_k,
                                      elem_bytes, l2_bytes, concurrency, cluster_m,
-                                     l2_partitions)
+                                     l2_partitions, k_alternate)
     _check(rc, "swz_l2_model_bytes")
     return (100.0 * h / (h + m) if h + m else 0.0), b
 

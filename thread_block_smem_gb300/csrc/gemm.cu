@@ -164,6 +164,17 @@ enum ItemKind : int { kWhole = 0, kFirst = 1, kPartial = 2 };
 // and the head of the next tile.  The pieces of a tile are added in K order
 // and the sum written to C by the tile's participants together, each taking
 // a share of its chunks (the epilogue).
+// Quotient and remainder of 64-bit operands that nearly always fit in 32
+// bits: a 32-bit division is a short inline sequence, a 64-bit one a
+// subroutine of a few hundred cycles, and the schedule's arithmetic runs
+// before the first load is issued.
+__device__ __forceinline__ uint64_t div_u64(uint64_t a, uint64_t b) {
+  return ((a | b) >> 32) == 0 ? uint64_t(uint32_t(a) / uint32_t(b)) : a / b;
+}
+__device__ __forceinline__ uint64_t mod_u64(uint64_t a, uint64_t b) {
+  return ((a | b) >> 32) == 0 ? uint64_t(uint32_t(a) % uint32_t(b)) : a % b;
+}
+
 struct Schedule {
   uint32_t c, P, U, kb;
   uint32_t dp_end;    // units below this are whole tiles
@@ -187,14 +198,20 @@ struct Schedule {
     const uint32_t R = sk ? U % P : 0u;
     dp_end = U - R;
     n_dp = c < dp_end ? (dp_end - c + P - 1) / P : 0u;
-    I = sk ? uint64_t(R) * kb : 0u;
+    I = uint64_t(R) * kb;
+    s = e = Iq = 0;
+    Ir = 0;
+    n_pieces = 0;
+    if (I == 0) return;  // whole tiles only
     s = range_start(c);
     e = range_start(c + 1);
-    n_pieces = s < e ? uint32_t((e - 1) / kb - s / kb + 1) : 0u;
-    Iq = I / P;
-    Ir = uint32_t(I % P);
+    n_pieces = s < e ? uint32_t(div_u64(e - 1, kb) - div_u64(s, kb) + 1) : 0u;
+    Iq = div_u64(I, P);
+    Ir = uint32_t(mod_u64(I, P));
   }
-  __device__ __forceinline__ uint64_t range_start(uint32_t cc) const { return I * cc / P; }
+  __device__ __forceinline__ uint64_t range_start(uint32_t cc) const {
+    return div_u64(I * cc, P);
+  }
   // Walks the range starts of clusters cc, cc + 1, ...: s = range_start(cc),
   // r = (I * cc) mod P, so that range_start(cc + 1) = s + Iq + carry.
   struct Cursor {
@@ -203,7 +220,7 @@ struct Schedule {
   };
   __device__ __forceinline__ Cursor cursor(uint32_t cc) const {
     const uint64_t t = I * cc;
-    return Cursor{t / P, uint32_t(t % P), cc};
+    return Cursor{div_u64(t, P), uint32_t(mod_u64(t, P)), cc};
   }
   __device__ __forceinline__ void step(Cursor& k) const {
     k.s += Iq;
@@ -222,7 +239,7 @@ struct Schedule {
   // tile sits in its workspace slot 1 when its range started in an earlier
   // tile (the piece is the head of t), else in slot 0.
   __device__ __forceinline__ uint32_t holder(uint64_t x) const {
-    return uint32_t(((x + 1) * P - 1) / I);  // largest cc with range_start(cc) <= x
+    return uint32_t(div_u64((x + 1) * P - 1, I));  // largest cc with range_start(cc) <= x
   }
   __device__ __forceinline__ Cursor first_part(uint32_t t) const {
     return cursor(holder(uint64_t(t) * kb));
@@ -267,7 +284,7 @@ struct Schedule {
   __device__ __forceinline__ bool item(uint32_t i, uint32_t& unit, uint32_t& k0, uint32_t& k1,
                                        int& kind) const {
     if (i < n_pieces) {
-      const uint64_t t = s / kb + i;
+      const uint64_t t = div_u64(s, kb) + i;
       const uint64_t t0 = t * kb;
       const uint32_t a = s > t0 ? uint32_t(s - t0) : 0u;
       const uint32_t b = e < t0 + kb ? uint32_t(e - t0) : kb;
@@ -442,6 +459,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     sch.init(blockIdx.x / CL, gridDim.x / CL, units, p.num_kb, p.stream_k != 0);
   }
+  // Everything above touches no global memory: with programmatic dependent
+  // launch it overlaps the end of the previous kernel of the stream.  The
+  // operands, C, the Stream-K workspace and the dynamic counter are touched
+  // only after that kernel has completed; the next GEMM of the stream may
+  // then start its own prologue on SMs this grid leaves free.
+  ptx::grid_dep_wait();
+  if (threadIdx.x == 0) ptx::grid_dep_launch_dependents();
   bool aborted = false;
 
   // Dynamic scheduler (DYN): the producer of the leader CTA claims work
@@ -547,8 +571,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int xe = int(sw) / (KIND == 0 ? 2 : 4);
       const int xn = int(sw) / 2;
       const uint32_t b_box_bytes = uint32_t(BK) * sw;
+      const uint32_t n_clusters = gridDim.x / CL;
       for (uint32_t i = 0; !aborted && next_item(i, leader, w, kbeg, kend, kind); ++i) {
         const TileCoord t = tile_of(p.order, w, p.sched_m, p.sched_n, uint32_t(p.group));
+        // K ping-pong: the whole tiles of every other wave (w / P odd) take
+        // their K blocks in descending order, so that a wave starts on the
+        // K slices of the operand panels the previous wave read last, while
+        // they are still in L2.  The direction is a function of the tile,
+        // not of the cluster, so every scheduler gives a tile the same sums.
+        const bool desc = kind == kWhole && ((w / n_clusters) & 1u) != 0;
         const int32_t m0 = int32_t((t.m * CL + rank) * BM);
         // B columns this CTA loads: its share of the tile
         constexpr int local = K_::BN_LOCAL;
@@ -562,7 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             skip = false;
           } else {
             const uint32_t fb = PAIR ? ptx::map_to_rank(full_bar(stage), 0) : full_bar(stage);
-            const int32_t k0 = int32_t(kb * bk_elems<KIND>() * KA);
+            const uint32_t kq = desc ? kend - 1u - (kb - kbeg) : kb;
+            const int32_t k0 = int32_t(kq * bk_elems<KIND>() * KA);
             const uint32_t a_dst = sA + stage * K_::A_BYTES, b_dst = sB + stage * K_::B_BYTES;
             // A: one box of 128 rows per column group, or one 3-D box
             // (xe elements x 128 rows x groups) when the map allows it.
@@ -1246,14 +1278,20 @@ static int launch(const Plan& pl, const CUtensorMap& ta, const CUtensorMap& ta3,
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = K_::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  // programmatic stream serialisation: the kernel may start while the
+  // previous kernel of the stream finishes (it waits for that kernel's
+  // completion before its first access to global memory)
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if constexpr (PAIR) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   SWZ_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, ta, ta3, tb, tb3, tc, prm));
   return SWZ_OK;

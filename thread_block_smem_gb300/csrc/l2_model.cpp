@@ -15,6 +15,9 @@
 // every die read every operand line of a wave, and each die's half keeps its
 // own copy of what its SMs read, so each half replays the whole trace with
 // 1 / l2_partitions of the capacity.  The prediction is that of one half.
+//
+// k_alternate = 1 is the K order of the library's persistent GEMM, not the
+// page's: the tiles of odd waves take the K steps from the last to the first.
 #include <stdint.h>
 
 #include <list>
@@ -67,12 +70,13 @@ inline uint64_t key_b(uint64_t k, uint64_t n) { return (uint64_t(1) << 63) | (n 
 
 extern "C" int swz_l2_model_bytes(int order, int group, int M, int N, int K, int tile_m,
                                   int tile_n, int tile_k, int elem_bytes, int64_t l2_bytes,
-                                  int l2_partitions, int concurrency, int cluster_m,
-                                  int64_t* hits, int64_t* misses, int64_t* miss_bytes) {
+                                  int l2_partitions, int k_alternate, int concurrency,
+                                  int cluster_m, int64_t* hits, int64_t* misses,
+                                  int64_t* miss_bytes) {
   if (!swz::order_is_valid(order) || (swz::order_uses_group(order) && group < 1)) return SWZ_EINVAL;
   if (M <= 0 || N <= 0 || K <= 0 || tile_m <= 0 || tile_n <= 0 || tile_k <= 0) return SWZ_EINVAL;
   if (elem_bytes <= 0 || l2_bytes < 0 || concurrency <= 0 || cluster_m <= 0) return SWZ_EINVAL;
-  if (l2_partitions < 1) return SWZ_EINVAL;
+  if (l2_partitions < 1 || (k_alternate != 0 && k_alternate != 1)) return SWZ_EINVAL;
   if (!hits || !misses || !miss_bytes) return SWZ_EINVAL;
   const int64_t span_m = int64_t(tile_m) * cluster_m;
   const uint32_t sm = uint32_t((int64_t(M) + span_m - 1) / span_m);
@@ -94,7 +98,9 @@ extern "C" int swz_l2_model_bytes(int order, int group, int M, int N, int K, int
   LruBytes cache(l2_bytes / l2_partitions);
   for (size_t w0 = 0; w0 < seq.size(); w0 += size_t(concurrency)) {
     const size_t w1 = w0 + size_t(concurrency) < seq.size() ? w0 + size_t(concurrency) : seq.size();
-    for (uint32_t k = 0; k < gk; ++k) {
+    const bool descending = k_alternate && (w0 / size_t(concurrency)) % 2 == 1;
+    for (uint32_t kk = 0; kk < gk; ++kk) {
+      const uint32_t k = descending ? gk - 1 - kk : kk;
       for (size_t i = w0; i < w1; ++i) {
         cache.touch(key_a(seq[i].first, k), a_bytes);
         cache.touch(key_b(k, seq[i].second), b_bytes);
@@ -113,5 +119,5 @@ extern "C" int swz_l2_model(int order, int group, int M, int N, int K, int tile_
   if (!hits || !misses) return SWZ_EINVAL;
   int64_t bytes = 0;
   return swz_l2_model_bytes(order, group, M, N, K, tile_m, tile_n, tile_k, elem_bytes, l2_bytes,
-                            1, concurrency, cluster_m, hits, misses, &bytes);
+                            1, 0, concurrency, cluster_m, hits, misses, &bytes);
 }

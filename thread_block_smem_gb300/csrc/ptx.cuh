@@ -25,6 +25,19 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+// Waits until the grids this one depends on (the previous kernel of its
+// stream, when it was launched with programmatic stream serialisation) have
+// completed and their memory operations are visible; immediate otherwise.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next grid of the stream be scheduled once every CTA of this grid
+// has issued it or exited.
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier ---------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
