@@ -35,6 +35,11 @@ CASES = [
     (768, 640, 1024, dict(cta_pair=True), 4),    # 9 cluster tiles, 2 clusters, R = 1
     (1280, 1024, 576, dict(cta_pair=True), 6),   # 20 cluster tiles, 3 clusters
     (768, 640, 192, dict(cta_pair=True), 8),     # kb = 3, 4 clusters, R = 1: I = 3 < 4
+    # a few tiles over every resident program (0): more reducers per tile
+    # than chunks per warp row, the fine reduction; ragged M and N
+    (200, 360, 8192, dict(cta_pair=True), 0),    # 2 cluster tiles, ~38 clusters each
+    (100, 256, 4096, dict(tile_n=256), 0),       # 1 tile, 64 K blocks over 64 programs
+    (300, 200, 8192, dict(tile_n=128), 0),       # 6 tiles of 128 x 128, ~25 programs each
 ]
 
 
