@@ -876,19 +876,25 @@ def run_swz(args):
         A32 = (torch.rand((M, K), generator=g) * 2 - 1).to(dev)
         Bt32 = (torch.rand((N, K), generator=g) * 2 - 1).to(dev)
         C32 = torch.empty((M, N), dtype=torch.float32, device=dev)
+        # the headline's scheduler (Stream-K tail when the headline uses it)
+        sk32 = {}
+        if args.stream_k:
+            n32 = swz.workspace_size(M, N, K, True, cta_pair=True)
+            sk32 = dict(stream_k=True,
+                        workspace=torch.zeros(max(n32, 256), dtype=torch.uint8, device=dev))
         t = timed(lambda: swz.gemm(A32, Bt32, head_order, head_group, True, out=C32,
-                                   b_transposed=True, cta_pair=True),
+                                   b_transposed=True, cta_pair=True, **sk32),
                   10 if args.only == "all" else 1, 3)
         med = statistics.median(t)
         # the measured bf16 peak scaled by the TF32 / bf16 rate ratio of the
         # library's own tcgen05 MMAs: 1/2 (4,095 vs 8,190 FLOP per clock per
         # SM); replaced below by this run's ratio when tc_rate runs
         peak_tf32 = peaks["bf16_tflops"] * 0.5
-        line["tf32_8192"] = {"ms": med, "tflops": flops / med / 1e9,
+        line["tf32_8192"] = {"ms": med, "tflops": flops / med / 1e9, "stream_k": bool(sk32),
                              "peak": peak_tf32, "frac": flops / med / 1e9 / peak_tf32,
                              "peak_source": "measured bf16 burst x the tcgen05 tf32/bf16 rate "
                                             "ratio 1/2"}
-        del A32, Bt32, C32
+        del A32, Bt32, C32, sk32
 
     # ---- tensor-core rate of the library's own tcgen05 code (swz_tc_rate) ----
     # FLOP per clock per SM from back-to-back MMAs on shared-memory operands;
