@@ -700,7 +700,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         return uint64_t(((uint32_t(kk) * 32u / sw) * rows * sw + (uint32_t(kk) * 32u) % sw) >> 4);
       };
       const uint32_t idesc = p.idesc;
+      const bool bkm = p.b_kmajor != 0;
       constexpr uint32_t b_rows = uint32_t(K_::BN_LOCAL);
+      // 128-byte span: the descriptors of stage 0, built once; stage st's
+      // are these plus its offset in 16-byte units (the address field cannot
+      // carry).  Building them per stage from the stage address, with the B
+      // layout re-read from the parameters after every MMA (whose asm
+      // clobbers memory), cost the 128-wide tiles, whose issuing thread is
+      // their bound, 1.4-2.5 %.
+      const uint64_t adesc0 = make_sdesc(sA, 16, 1024, 2);
+      const uint64_t bdesc0 =
+          bkm ? make_sdesc(sB, 16, 1024, 2) : make_sdesc(sB, BK * KA * 128, 1024, 2);
       for (uint32_t i = 0; !aborted && next_item(i, false, w, kbeg, kend, kind); ++i) {
         if (!wait(tempty_bar(acc), acc_phase ^ 1u, ctl)) { aborted = true; break; }
         ptx::tc_fence_after();
@@ -710,34 +720,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             a_step[kk] = kmajor_off(kk, BM);
-            b_step[kk] = p.b_kmajor ? kmajor_off(kk, b_rows) : uint64_t((16u * sw * kk) >> 4);
+            b_step[kk] = bkm ? kmajor_off(kk, b_rows) : uint64_t((16u * sw * kk) >> 4);
           }
         }
         // One stage's MMAs (4 * KA k-slices of 16 / 8 elements) and the
         // commit that releases the stage when they complete.
         auto issue_stage = [&](uint32_t st, bool first) {
-          const uint32_t a_addr = sA + st * K_::A_BYTES;
-          const uint32_t b_addr = sB + st * K_::B_BYTES;
           if constexpr (SW == 128) {
             // slice kk of the KA atoms: atom kk / 4, 32 bytes per slice
             // inside it; N-major B: 16 K-rows of 128 bytes per slice
-            const uint64_t adesc = make_sdesc(a_addr, 16, 1024, 2);
-            const uint64_t bdesc = p.b_kmajor ? make_sdesc(b_addr, 16, 1024, 2)
-                                              : make_sdesc(b_addr, BK * KA * 128, 1024, 2);
+            const uint64_t adesc = adesc0 + uint64_t(st * uint32_t(K_::A_BYTES >> 4));
+            const uint64_t bdesc = bdesc0 + uint64_t(st * uint32_t(K_::B_BYTES >> 4));
             const uint32_t b_atom = b_rows * 128u;  // K-major B: bytes of one atom
             ptx::mma<CL, KIND>(d, adesc, bdesc, idesc, first ? 0u : 1u);
 #pragma unroll
             for (int kk = 1; kk < 4 * KA; ++kk) {
               const uint64_t ao = uint64_t(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4);
               const uint64_t bo =
-                  p.b_kmajor ? uint64_t(((kk / 4) * b_atom + (kk % 4) * 32u) >> 4)
-                             : uint64_t(128 * kk);
+                  bkm ? uint64_t(((kk / 4) * b_atom + (kk % 4) * 32u) >> 4)
+                      : uint64_t(128 * kk);
               ptx::mma<CL, KIND>(d, adesc + ao, bdesc + bo, idesc, 1u);
             }
           } else {
+            const uint32_t a_addr = sA + st * K_::A_BYTES;
+            const uint32_t b_addr = sB + st * K_::B_BYTES;
             const uint64_t adesc = make_sdesc(a_addr, 16, 8 * sw, lay);
-            const uint64_t bdesc = p.b_kmajor ? make_sdesc(b_addr, 16, 8 * sw, lay)
-                                              : make_sdesc(b_addr, BK * sw, 8 * sw, lay);
+            const uint64_t bdesc = bkm ? make_sdesc(b_addr, 16, 8 * sw, lay)
+                                       : make_sdesc(b_addr, BK * sw, 8 * sw, lay);
             ptx::mma<CL, KIND>(d, adesc, bdesc, idesc, first ? 0u : 1u);
 #pragma unroll
             for (int kk = 1; kk < 4; ++kk)
