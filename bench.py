@@ -112,40 +112,40 @@ CONFIG_ORDERS = {
 # left out of the line.
 NCU = {
     "gemm8192_bf16_pair": {
-        "source": {"gemm_cu_code_hash": "78bc71ca67e2bb4e", "captured": "2026-12-02",
+        "source": {"gemm_cu_code_hash": "61c4fd4006e5d62d", "captured": "2026-12-02",
                    "kernel": "gemm_kernel<256, 1, 0, 128, 0>", "stream_k": True,
                    "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum --clock-control none "
                               "-k regex:gemm_kernel -s 10 -c 10 python bench.py --workload gemm8192_bf16_pair "
                               "--only sweep --no-cpu; traffic: ncu --set full -k regex:gemm_kernel -s 3 -c 1 "
                               "python bench.py --only gemm --steps 1 --warmup 3 --no-cpu"},
-        "traffic_bytes": 875775232 + 276412672, "traffic_order": ("serpentine", 8),
-        "orders": {("row", 1): (67.32, 1517767168), ("col", 1): (67.4, 1499684608),
-                   ("panel", 4): (71.92, 1263878912), ("panel", 8): (76.01, 954856192),
-                   ("panel", 16): (72.85, 926722304), ("serpentine", 4): (72.16, 1081916928),
-                   ("serpentine", 8): (76.33, 876317696), ("serpentine", 16): (75.23, 922793984),
-                   ("morton", 1): (73.67, 1081933568), ("xor", 1): (69.56, 1465388032)}},
+        "traffic_bytes": 873719296 + 276592640, "traffic_order": ("serpentine", 8),
+        "orders": {("row", 1): (66.9, 1498279936), ("col", 1): (66.22, 1487829504),
+                   ("panel", 4): (70.69, 1263904000), ("panel", 8): (75.16, 952798720),
+                   ("panel", 16): (73.42, 925908224), ("serpentine", 4): (73.44, 1078299904),
+                   ("serpentine", 8): (76.76, 874268416), ("serpentine", 16): (75.54, 917067776),
+                   ("morton", 1): (70.1, 1084324096), ("xor", 1): (70.37, 1453511424)}},
     "gemm4096_fp16": {
-        "source": {"gemm_cu_code_hash": "78bc71ca67e2bb4e", "captured": "2026-12-02",
+        "source": {"gemm_cu_code_hash": "61c4fd4006e5d62d", "captured": "2026-12-02",
                    "kernel": "gemm_kernel<256, 0, 0, 128, 0>", "stream_k": True,
                    "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum --clock-control none "
                               "-k regex:gemm_kernel -s 12 -c 12 python bench.py --workload gemm4096_fp16 "
                               "--only sweep --no-cpu"},
-        "orders": {("row", 1): (81.12, 84568064), ("col", 1): (77.92, 87929600),
-                   ("panel", 2): (80.11, 88091392), ("panel", 4): (79.49, 93709056),
-                   ("panel", 8): (78.12, 97703936), ("panel", 16): (74.8, 112325376),
-                   ("serpentine", 4): (78.93, 99798016), ("serpentine", 8): (76.0, 100707328),
-                   ("serpentine", 16): (80.95, 84588800), ("morton", 1): (75.12, 111213056),
-                   ("xor", 1): (75.01, 112361472), ("serpentine", 2): (76.68, 93006848)}},
+        "orders": {("row", 1): (80.78, 84835328), ("col", 1): (75.93, 87338496),
+                   ("panel", 2): (79.43, 87023616), ("panel", 4): (80.59, 92467200),
+                   ("panel", 8): (78.62, 96026880), ("panel", 16): (74.01, 111985664),
+                   ("serpentine", 4): (79.83, 97025280), ("serpentine", 8): (78.52, 100045568),
+                   ("serpentine", 16): (81.52, 84868352), ("morton", 1): (75.17, 109900544),
+                   ("xor", 1): (73.91, 111733504), ("serpentine", 2): (76.14, 93911040)}},
     "gemm6144x10240x4096_fp16_pair": {
-        "source": {"gemm_cu_code_hash": "78bc71ca67e2bb4e", "captured": "2026-12-02",
+        "source": {"gemm_cu_code_hash": "61c4fd4006e5d62d", "captured": "2026-12-02",
                    "kernel": "gemm_kernel<128, 1, 0, 128, 0>", "stream_k": True,
                    "command": "ncu --metrics lts__t_sector_hit_rate.pct,dram__bytes_read.sum --clock-control none "
                               "-k regex:gemm_kernel -s 8 -c 8 python bench.py --workload gemm6144x10240x4096_fp16_pair "
                               "--only sweep --no-cpu"},
-        "orders": {("row", 1): (70.62, 874915840), ("col", 1): (83.2, 263562496),
-                   ("panel", 4): (77.21, 562641664), ("panel", 8): (84.49, 322518272),
-                   ("panel", 16): (85.15, 249229824), ("serpentine", 4): (81.05, 392333824),
-                   ("serpentine", 8): (82.79, 322275328), ("serpentine", 16): (83.82, 294553856)}},
+        "orders": {("row", 1): (70.57, 864301824), ("col", 1): (82.7, 264039680),
+                   ("panel", 4): (77.38, 561634048), ("panel", 8): (83.48, 322198784),
+                   ("panel", 16): (84.62, 247439360), ("serpentine", 4): (82.12, 380236032),
+                   ("serpentine", 8): (83.33, 323559168), ("serpentine", 16): (83.25, 294002432)}},
 }
 
 

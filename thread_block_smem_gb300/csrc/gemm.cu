@@ -732,14 +732,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t adesc = adesc0 + uint64_t(st * uint32_t(K_::A_BYTES >> 4));
             const uint64_t bdesc = bdesc0 + uint64_t(st * uint32_t(K_::B_BYTES >> 4));
             const uint32_t b_atom = b_rows * 128u;  // K-major B: bytes of one atom
-            ptx::mma<CL, KIND>(d, adesc, bdesc, idesc, first ? 0u : 1u);
+            const uint32_t alo = uint32_t(adesc), ahi = uint32_t(adesc >> 32);
+            const uint32_t blo = uint32_t(bdesc), bhi = uint32_t(bdesc >> 32);
+            ptx::mma<CL, KIND>(d, alo, ahi, blo, bhi, idesc, first ? 0u : 1u);
 #pragma unroll
             for (int kk = 1; kk < 4 * KA; ++kk) {
-              const uint64_t ao = uint64_t(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4);
-              const uint64_t bo =
-                  bkm ? uint64_t(((kk / 4) * b_atom + (kk % 4) * 32u) >> 4)
-                      : uint64_t(128 * kk);
-              ptx::mma<CL, KIND>(d, adesc + ao, bdesc + bo, idesc, 1u);
+              const uint32_t ao = uint32_t(((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4);
+              const uint32_t bo = bkm ? uint32_t(((kk / 4) * b_atom + (kk % 4) * 32u) >> 4)
+                                      : uint32_t(128 * kk);
+              ptx::mma<CL, KIND>(d, alo + ao, ahi, blo + bo, bhi, idesc, 1u);
             }
           } else {
             const uint32_t a_addr = sA + st * K_::A_BYTES;

@@ -285,6 +285,28 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b
         : "memory");
 }
 
+// The same with each descriptor given as its two 32-bit halves: per-slice
+// offsets are then 32-bit adds to the low half (the address field lies in
+// it and cannot carry), one instruction fewer per MMA for the issuing
+// thread that bounds the 128-wide tiles.
+#define SWZ_MMA_LH(CGS, KINDS)                                                         \
+  asm volatile(                                                                        \
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tsetp.ne.b32 p, %6, 0;\n\t"          \
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"                           \
+      "tcgen05.mma.cta_group::" CGS ".kind::" KINDS " [%0], da, db, %5, p;\n\t}" ::"r"( \
+          d_tmem),                                                                     \
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)          \
+      : "memory")
+template <int CG, int KIND>
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                    uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  if constexpr (CG == 1 && KIND == 0) SWZ_MMA_LH("1", "f16");
+  else if constexpr (CG == 2 && KIND == 0) SWZ_MMA_LH("2", "f16");
+  else if constexpr (CG == 1) SWZ_MMA_LH("1", "tf32");
+  else SWZ_MMA_LH("2", "tf32");
+}
+#undef SWZ_MMA_LH
+
 // Arrive once on `bar` when all previously issued tcgen05 ops of this thread
 // have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
