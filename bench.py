@@ -990,7 +990,8 @@ def run_swz(args):
     print(json.dumps(line), flush=True)
 
 
-def main():
+def make_parser():
+    """The command line of bench.py."""
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
@@ -1047,7 +1048,11 @@ def main():
                          "workload's shape for counter comparison (profiling modes); "
                          "launch: 50 calls back to back, eager and replayed from a CUDA "
                          "graph, per-call wall time")
-    args = ap.parse_args()
+    return ap
+
+
+def main():
+    args = make_parser().parse_args()
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
     if args.non_persistent:
         args.stream_k = False  # Stream-K shares the tail of a persistent launch

@@ -174,3 +174,26 @@ def test_code_hash_ignores_comments_and_layout_only():
     # the records in the bench are keyed this way
     for rec in bench.NCU.values():
         assert len(rec["source"]["gemm_cu_code_hash"]) == 16
+
+
+def test_profile_commands_parse():
+    # every `python bench.py ...` command the profile summaries give is a
+    # valid command line of this bench.py (placeholders of a command family
+    # replaced by one of their values)
+    import glob
+    import os
+    import re
+    import shlex
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    fill = {"W": ["gemm4096_fp16"], "O": ["row"], "G": ["1"], "P": ["76"],
+            "[F]": ["--stream-k", "--die-split"]}
+    ap = bench.make_parser()
+    seen = 0
+    for path in glob.glob(os.path.join(root, "profiles", "*.md")):
+        text = re.sub(r"\\\n\s*", " ", open(path).read())  # join continued lines
+        for m in re.finditer(r"python bench\.py([^\n#`]*)", text):
+            argv = [a for t in shlex.split(m.group(1)) for a in fill.get(t, [t])]
+            argv = [a for a in argv if a not in (">", "2>&1") and not a.startswith("gpurun_out")]
+            ap.parse_args(argv)
+            seen += 1
+    assert seen >= 10
