@@ -101,3 +101,33 @@ def test_write_after_read(swz, cfg):
         swz.check_status()
         assert torch.equal(C1.cpu().double(), want1)
         assert torch.equal(X.cpu().double(), wantx)
+
+
+@pytest.mark.parametrize("cfg,programs", [(dict(tile_n=128), 7), (dict(cta_pair=True), 6)])
+def test_schedulers_with_state_back_to_back(swz, cfg, programs):
+    # Stream-K launches sharing one workspace and dynamic-scheduler launches
+    # sharing one counter, enqueued back to back with no synchronisation,
+    # then a TF32 Stream-K GEMM reading the first result: every result exact
+    M, N, K = 768, 640, 1024
+    A1, B1 = si.small_int_gemm_inputs(M, N, K, "bf16", lo=-1, hi=1, seed=21)
+    A2, B2 = si.small_int_gemm_inputs(M, N, K, "bf16", lo=-1, hi=1, seed=22)
+    B3t = _ints((256, N), -2, 2, 23, torch.float32)
+    w1, w2 = ref.gemm_f64(A1, B1), ref.gemm_f64(A2, B2)
+    w3 = w1 @ B3t.double().t()
+    d = [X.cuda() for X in (A1, B1, A2, B2)]
+    n = swz.workspace_size(M, N, K, True, num_programs=programs, **cfg)
+    ws = torch.zeros(max(n, 256), dtype=torch.uint8, device="cuda")
+    n3 = swz.workspace_size(M, 256, N, True, num_programs=programs, **cfg)
+    ws3 = torch.zeros(max(n3, 256), dtype=torch.uint8, device="cuda")
+    wd = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    sk = dict(persistent=True, num_programs=programs, stream_k=True, **cfg)
+    dyn = dict(persistent=True, num_programs=programs, dynamic=True, workspace=wd, **cfg)
+    for _ in range(2):
+        C1 = swz.gemm(d[0], d[1], "panel", 2, workspace=ws, **sk)
+        C2 = swz.gemm(d[2], d[3], "panel", 2, workspace=ws, **sk)
+        C3 = swz.gemm(d[0], d[1], "serpentine", 2, **dyn)
+        C4 = swz.gemm(d[2], d[3], "serpentine", 2, **dyn)
+        C5 = swz.gemm(C1, B3t.cuda(), "row", 1, b_transposed=True, workspace=ws3, **sk)
+        swz.check_status()
+        for C, want in ((C1, w1), (C2, w2), (C3, w1), (C4, w2), (C5, w3)):
+            assert torch.equal(C.cpu().double(), want)
