@@ -5,7 +5,9 @@ id / P odd).  On real-valued inputs the two orders round differently, so the
 tiles of even waves must equal the one-CTA-per-tile result bit for bit and the
 tiles of odd waves must differ from it (with K = 2048, N(0, 1) products, some
 element of a 128 x 256 tile differs with overwhelming probability); both stay
-within the GEMM tolerance of the oracle."""
+within the GEMM tolerance of the oracle.  On integer inputs every order is
+exact, including a ragged K, where a descending tile starts on the partial
+K block."""
 import pytest
 import torch
 
@@ -57,3 +59,20 @@ def test_tiles_of_odd_waves_run_k_descending(swz, cfg, programs, order, g):
         got = X[torch.from_numpy(ii).cuda(), torch.from_numpy(jj).cuda()].cpu().numpy()
         mx, rel = errors(got, want)
         assert mx <= MAX_ABS and rel <= REL_FRO
+
+
+@pytest.mark.parametrize("cfg,programs", [(dict(tile_n=128), 7), (dict(tile_n=256), 5),
+                                          (dict(cta_pair=True), 6)])
+@pytest.mark.parametrize("dtype", ["bf16", "tf32"])
+def test_ragged_k_descending_exact(swz, cfg, programs, dtype):
+    # K = 1000 is no multiple of the K block: a tile of an odd wave starts on
+    # the partial block, zero-filled past K by TMA; with few programs there
+    # are several waves, and integer inputs make every sum exact
+    M, N, K = 768, 640, 1000
+    A, B = si.small_int_gemm_inputs(M, N, K, "bf16", lo=-3, hi=3, seed=programs)
+    want = ref.gemm_f64(A, B)
+    if dtype == "tf32":
+        A, B = A.float(), B.float()
+    C = swz.gemm(A.cuda(), B.cuda(), "serpentine", 2, True, num_programs=programs, **cfg)
+    swz.check_status()
+    assert torch.equal(C.cpu().double(), want)
